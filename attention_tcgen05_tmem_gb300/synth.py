@@ -1,0 +1,107 @@
+"""Seeded synthetic inputs and the named workloads.
+
+This module holds no attention arithmetic: it only draws random numbers and
+names shapes, so both the CUDA path and the fp64 oracle take their inputs
+from here.
+
+Recipe (the same for every workload): each tensor is drawn as fp32 N(0, 1)
+from its own ``torch.Generator`` seeded with ``seed * 16 + index`` (Q=0, K=1,
+V=2, dO=3), then rounded once to bf16 (round-to-nearest-even).  Both sides
+consume the rounded values; the oracle widens them to fp64.
+
+The shapes follow the pages' workloads: the CS336 README's benchmark grid
+(B=8, one head, d in {16, 32, 64}, S in {256, 1024, 4096}), the SpecForge
+post's long-context EAGLE3 training (16K tokens, GQA, TTT steps that append
+K/V segments) and HOT-Step's DiT trainer geometries (full self-attention and
+cross-attention with a short encoder sequence).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, replace
+
+import torch
+
+MASKS = ("full", "causal", "ttt")
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Sq: int
+    Skv: int
+    D: int
+    mask: str  # "full" | "causal" | "ttt"
+    ttt_step: int = 0
+    seed: int = 0
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.Hkv
+
+    def with_(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+    def describe(self) -> dict:
+        d = {"workload": self.name, "B": self.B, "Hq": self.Hq, "Hkv": self.Hkv, "Sq": self.Sq,
+             "Skv": self.Skv, "D": self.D, "mask": self.mask}
+        if self.mask == "ttt":
+            d["ttt_step"] = self.ttt_step
+        return d
+
+
+def ttt_workload(step: int, S: int = 8192, B: int = 1, Hq: int = 32, Hkv: int = 8, D: int = 128,
+                 seed: int = 3) -> Workload:
+    """EAGLE3 Training-Time-Test draft attention at TTT step ``step``: the
+    queries are one segment of S rows, the K/V cache holds step+1 segments."""
+    return Workload(f"eagle3_ttt_step{step}", B, Hq, Hkv, S, (step + 1) * S, D, "ttt", step, seed)
+
+
+# The named workloads (shapes only).
+TINY = Workload("tiny_causal_B1_H2_S128_D64", 1, 2, 2, 128, 128, 64, "causal", 0, 0)
+SWEEP = tuple(
+    Workload(f"sweep_causal_B8_H1_S{S}_D{D}", 8, 1, 1, S, S, D, "causal", 0, 1)
+    for D in (16, 32, 64) for S in (256, 1024, 4096))
+LONG_GQA = Workload("long_causal_gqa_B1_Hq32_Hkv4_S16384_D128", 1, 32, 4, 16384, 16384, 128,
+                    "causal", 0, 2)
+TTT_STEPS = tuple(ttt_workload(t) for t in range(7))
+DIT_SELF = Workload("dit_full_self_B2_H16_S12288_D64", 2, 16, 16, 12288, 12288, 64, "full", 0, 4)
+DIT_CROSS = Workload("dit_full_cross_B2_H16_Sq12288_Skv512_D64", 2, 16, 16, 12288, 512, 64,
+                     "full", 0, 4)
+
+ALL = (TINY,) + SWEEP + (LONG_GQA,) + TTT_STEPS + (DIT_SELF, DIT_CROSS)
+
+
+def by_name(name: str) -> Workload:
+    for w in ALL:
+        if w.name == name:
+            return w
+    raise KeyError(name)
+
+
+def _draw(shape, seed: int) -> torch.Tensor:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return torch.randn(*shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
+
+
+def make_inputs(w: Workload, seed: int | None = None, with_dout: bool = True) -> dict:
+    """Contiguous [B, H, S, D] bf16 CPU tensors q, k, v (and dout)."""
+    s = w.seed if seed is None else seed
+    out = {
+        "q": _draw((w.B, w.Hq, w.Sq, w.D), s * 16 + 0),
+        "k": _draw((w.B, w.Hkv, w.Skv, w.D), s * 16 + 1),
+        "v": _draw((w.B, w.Hkv, w.Skv, w.D), s * 16 + 2),
+    }
+    if with_dout:
+        out["dout"] = _draw((w.B, w.Hq, w.Sq, w.D), s * 16 + 3)
+    return out
+
+
+def zero_k(inputs: dict) -> dict:
+    """Copy of ``inputs`` with K set to zero (uniform attention weights)."""
+    d = dict(inputs)
+    d["k"] = torch.zeros_like(inputs["k"])
+    return d

@@ -1,0 +1,153 @@
+"""fp64 CPU oracle for masked training attention (TEST INFRASTRUCTURE ONLY).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never links,
+loads or calls it, and it shares no code with the CUDA path.
+
+The arithmetic lives in ``attn_oracle.c`` (plain C, fp64, OpenMP over the
+(b, h) pairs); this module only compiles it with gcc and marshals numpy
+arrays.  Every function follows the plain definition of attention:
+
+* SpecForge long-context post, "EAGLE3 Training": softmax(Q K^T / sqrt(d_k)) V.
+* SpecForge post, "Flex Attention": the eagle3 ``mask_mod`` =
+  or(causal_mask, suffix_mask), read with shift_left = t (the number of
+  appended TTT segments), Q_LEN = Sq and KV_LEN = (t+1) Sq.
+* CS336 README, "Flash Attention (Triton)": LSE saved by the forward; the
+  backward recomputes P from it.
+* HOT-Step flash-attn-training, section 6 trap 9: a row with no visible key
+  has O = 0 and LSE = 0.
+
+Parity is pinned (finite differences, brute force, invariants, the EAGLE3
+concatenated-score construction, torch fp64 sdpa, closed forms) by
+``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+MASK_FULL = 0
+MASK_CAUSAL = 1
+MASK_TTT = 2
+MASK_NAMES = {"full": MASK_FULL, "causal": MASK_CAUSAL, "ttt": MASK_TTT}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile attn_oracle.c into liboracle.so with gcc (-O3 -fopenmp)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O3", "-std=c99", "-fopenmp", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            dp = ctypes.POINTER(ctypes.c_double)
+            L = ctypes.c_long
+            lib.oracle_visible.restype = ctypes.c_int
+            lib.oracle_visible.argtypes = [ctypes.c_int, ctypes.c_int, L, L, L, L]
+            lib.oracle_mask.restype = None
+            lib.oracle_mask.argtypes = [ctypes.c_int, ctypes.c_int, L, L, ctypes.c_void_p]
+            lib.oracle_fwd.restype = ctypes.c_int
+            lib.oracle_fwd.argtypes = [ctypes.c_int] * 3 + [L, L] + [ctypes.c_int] * 3 + [
+                ctypes.c_double] + [dp] * 5
+            lib.oracle_bwd.restype = ctypes.c_int
+            lib.oracle_bwd.argtypes = [ctypes.c_int] * 3 + [L, L] + [ctypes.c_int] * 3 + [
+                ctypes.c_double] + [dp] * 7
+            lib.oracle_count_visible.restype = ctypes.c_longlong
+            lib.oracle_count_visible.argtypes = [ctypes.c_int, ctypes.c_int, L, L]
+            lib.oracle_num_threads.restype = ctypes.c_int
+            lib.oracle_num_threads.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def _mask_id(mask) -> int:
+    return MASK_NAMES[mask] if isinstance(mask, str) else int(mask)
+
+
+def _f64(a) -> np.ndarray:
+    """Contiguous fp64 numpy copy of a numpy array or a CPU torch tensor."""
+    if hasattr(a, "detach"):
+        a = a.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def default_scale(D: int) -> float:
+    return 1.0 / float(np.sqrt(D))
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def visible(mask, t: int, Sq: int, Skv: int, q: int, kv: int) -> bool:
+    return bool(_load().oracle_visible(_mask_id(mask), t, Sq, Skv, q, kv))
+
+
+def mask(mask, t: int, Sq: int, Skv: int) -> np.ndarray:
+    """Dense [Sq, Skv] uint8 visibility bitmap."""
+    out = np.zeros((Sq, Skv), dtype=np.uint8)
+    _load().oracle_mask(_mask_id(mask), t, Sq, Skv, out.ctypes.data)
+    return out
+
+
+def count_visible(mask, t: int, Sq: int, Skv: int) -> int:
+    return int(_load().oracle_count_visible(_mask_id(mask), t, Sq, Skv))
+
+
+def _dims(q, k):
+    B, Hq, Sq, D = q.shape
+    Bk, Hkv, Skv, Dk = k.shape
+    if Bk != B or Dk != D:
+        raise ValueError("q/k shape mismatch")
+    return B, Hq, Hkv, Sq, Skv, D
+
+
+def fwd(q, k, v, mask="causal", t: int = 0, scale: float | None = None):
+    """Returns (O [B,Hq,Sq,D], LSE [B,Hq,Sq]) in fp64."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Hq, Hkv, Sq, Skv, D = _dims(q, k)
+    scale = default_scale(D) if scale is None else float(scale)
+    o = np.zeros((B, Hq, Sq, D))
+    lse = np.zeros((B, Hq, Sq))
+    rc = _load().oracle_fwd(B, Hq, Hkv, Sq, Skv, D, _mask_id(mask), t, scale, _ptr(q), _ptr(k),
+                            _ptr(v), _ptr(o), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_fwd rejected the problem (code {rc})")
+    return o, lse
+
+
+def bwd(q, k, v, do, mask="causal", t: int = 0, scale: float | None = None):
+    """Returns (dQ, dK, dV) in fp64; dK/dV summed over each kv head's q heads."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, Hq, Hkv, Sq, Skv, D = _dims(q, k)
+    scale = default_scale(D) if scale is None else float(scale)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    rc = _load().oracle_bwd(B, Hq, Hkv, Sq, Skv, D, _mask_id(mask), t, scale, _ptr(q), _ptr(k),
+                            _ptr(v), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv))
+    if rc != 0:
+        raise ValueError(f"oracle_bwd rejected the problem (code {rc})")
+    return dq, dk, dv
