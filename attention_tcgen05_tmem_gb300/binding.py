@@ -1,0 +1,204 @@
+"""Thin ctypes binding over ``libattn_train.so`` (include/attn_train.h).
+
+Argument marshalling only: torch tensors become (pointer, strides) views,
+the current torch CUDA stream becomes the ``void* stream`` argument, and a
+non-OK status becomes an exception.  Every step of the computation runs in
+the library's CUDA kernels; there is no CPU or PyTorch fallback, and calling
+anything here without the built library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libattn_train.so")
+
+MASKS = {"full": 0, "causal": 1, "ttt": 2}
+STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_ALIGNMENT",
+          4: "ATTN_ERR_WORKSPACE", 5: "ATTN_ERR_CUDA", 6: "ATTN_ERR_DEVICE_TIMEOUT"}
+
+# Entry points of include/attn_train.h (checked against the header by the tests).
+EXPORTS = ("attn_train_supports", "attn_train_workspace_size", "attn_train_fwd", "attn_train_bwd",
+           "attn_train_last_error", "attn_train_device_status", "attn_train_set_wait_budget_ns",
+           "attn_train_mask_pattern", "attn_train_probe_mma", "attn_train_selftest_wait_timeout")
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class Tensor(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("stride_b", ctypes.c_int64),
+                ("stride_h", ctypes.c_int64), ("stride_s", ctypes.c_int64)]
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
+                ("Sq", ctypes.c_int), ("Skv", ctypes.c_int), ("D", ctypes.c_int),
+                ("mask", ctypes.c_int), ("ttt_step", ctypes.c_int), ("scale", ctypes.c_float)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load(path: str = LIB_PATH):
+    """Load the library (build it first with ``__graft_entry__.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library not built: {path} is missing "
+                               "(run __graft_entry__.build())")
+        lib = ctypes.CDLL(path)
+        P = ctypes.POINTER(Problem)
+        T = Tensor
+        vp = ctypes.c_void_p
+        st = ctypes.c_int
+        sig = {
+            "attn_train_supports": (st, [P]),
+            "attn_train_workspace_size": (st, [P, ctypes.POINTER(ctypes.c_size_t)]),
+            "attn_train_fwd": (st, [P, T, T, T, T, vp, vp]),
+            "attn_train_bwd": (st, [P, T, T, T, T, T, vp, T, T, T, vp, ctypes.c_size_t, vp]),
+            "attn_train_last_error": (ctypes.c_char_p, []),
+            "attn_train_device_status": (st, [vp]),
+            "attn_train_set_wait_budget_ns": (st, [ctypes.c_uint64]),
+            "attn_train_mask_pattern": (st, [P, vp, vp, vp]),
+            "attn_train_probe_mma": (st, [ctypes.c_int, ctypes.c_int, vp, vp, vp, vp]),
+            "attn_train_selftest_wait_timeout": (st, [vp]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != 0:
+        msg = load().attn_train_last_error().decode(errors="replace")
+        raise AttnError(status, msg)
+
+
+def problem(B, Hq, Hkv, Sq, Skv, D, mask="causal", ttt_step=0, scale=0.0) -> Problem:
+    m = MASKS[mask] if isinstance(mask, str) else int(mask)
+    return Problem(B, Hq, Hkv, Sq, Skv, D, m, ttt_step, float(scale))
+
+
+def problem_for(q, k, mask="causal", ttt_step=0, scale=None) -> Problem:
+    B, Hq, Sq, D = q.shape
+    _, Hkv, Skv, _ = k.shape
+    return problem(B, Hq, Hkv, Sq, Skv, D, mask, ttt_step, 0.0 if scale is None else scale)
+
+
+def view(t) -> Tensor:
+    """[B, H, S, D] torch tensor -> attn_tensor (D must be contiguous)."""
+    if t.dim() != 4:
+        raise ValueError("expected a [B, H, S, D] tensor")
+    if t.stride(3) != 1:
+        raise ValueError("the head dimension must be contiguous")
+    return Tensor(t.data_ptr(), t.stride(0), t.stride(1), t.stride(2))
+
+
+def _stream(stream):
+    if stream is not None:
+        return ctypes.c_void_p(int(stream))
+    import torch
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def supports(p: Problem) -> bool:
+    return load().attn_train_supports(ctypes.byref(p)) == 0
+
+
+def check_supported(p: Problem):
+    _check(load().attn_train_supports(ctypes.byref(p)))
+
+
+def workspace_size(p: Problem) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().attn_train_workspace_size(ctypes.byref(p), ctypes.byref(n)))
+    return int(n.value)
+
+
+def fwd_raw(p: Problem, q, k, v, o, lse, stream=None):
+    """attn_train_fwd on caller-owned tensors (o, lse are written)."""
+    _check(load().attn_train_fwd(ctypes.byref(p), view(q), view(k), view(v), view(o),
+                                 ctypes.c_void_p(lse.data_ptr()), _stream(stream)))
+
+
+def bwd_raw(p: Problem, q, k, v, o, dout, lse, dq, dk, dv, workspace, stream=None):
+    """attn_train_bwd on caller-owned tensors (dq, dk, dv are written)."""
+    _check(load().attn_train_bwd(ctypes.byref(p), view(q), view(k), view(v), view(o), view(dout),
+                                 ctypes.c_void_p(lse.data_ptr()), view(dq), view(dk), view(dv),
+                                 ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                                 _stream(stream)))
+
+
+def device_status(stream=None):
+    _check(load().attn_train_device_status(_stream(stream)))
+
+
+def set_wait_budget_ns(ns: int):
+    _check(load().attn_train_set_wait_budget_ns(int(ns)))
+
+
+# ------------------------------------------------------------ conveniences
+def fwd(q, k, v, mask="causal", ttt_step=0, scale=None, stream=None):
+    """Allocates O and LSE with torch, runs the forward; returns (o, lse)."""
+    import torch
+    p = problem_for(q, k, mask, ttt_step, scale)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[0], q.shape[1], q.shape[2], dtype=torch.float32, device=q.device)
+    fwd_raw(p, q, k, v, o, lse, stream)
+    return o, lse
+
+
+def bwd(q, k, v, o, lse, dout, mask="causal", ttt_step=0, scale=None, stream=None, workspace=None):
+    """Allocates dQ, dK, dV (and workspace unless given); returns (dq, dk, dv)."""
+    import torch
+    p = problem_for(q, k, mask, ttt_step, scale)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    if workspace is None:
+        workspace = torch.empty(workspace_size(p), dtype=torch.uint8, device=q.device)
+    bwd_raw(p, q, k, v, o, dout, lse, dq, dk, dv, workspace, stream)
+    return dq, dk, dv
+
+
+def mask_pattern(Sq, Skv, mask, ttt_step=0, device="cuda", with_tiles=True):
+    """Device view of the mask: (bits[2, Sq, Skv] uint8, tiles or None)."""
+    import torch
+    p = problem(1, 1, 1, Sq, Skv, 64, mask, ttt_step)
+    bits = torch.zeros(2, Sq, Skv, dtype=torch.uint8, device=device)
+    tiles = None
+    if with_tiles:
+        kv_main = Sq if p.mask == 2 else Skv
+        tiles = torch.zeros(math.ceil(Sq / 128), math.ceil(kv_main / 128), dtype=torch.uint8,
+                            device=device)
+    _check(load().attn_train_mask_pattern(ctypes.byref(p), ctypes.c_void_p(bits.data_ptr()),
+                                          ctypes.c_void_p(tiles.data_ptr() if tiles is not None else 0),
+                                          _stream(None)))
+    return bits, tiles
+
+
+def probe_mma(mode: int, a, b, D: int):
+    """One-tile tcgen05 probe; returns the fp32 product (see attn_train.h)."""
+    import torch
+    c = torch.zeros(128, 128 if mode == 0 else D, dtype=torch.float32, device=a.device)
+    _check(load().attn_train_probe_mma(mode, D, ctypes.c_void_p(a.data_ptr()),
+                                       ctypes.c_void_p(b.data_ptr()), ctypes.c_void_p(c.data_ptr()),
+                                       _stream(None)))
+    return c
+
+
+def selftest_wait_timeout():
+    _check(load().attn_train_selftest_wait_timeout(_stream(None)))

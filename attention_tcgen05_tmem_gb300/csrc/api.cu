@@ -1,0 +1,349 @@
+// api.cu -- the C ABI (include/attn_train.h): argument validation, TMA tensor
+// maps, workspace carving, launch sequencing and error reporting.  Validation
+// runs entirely on the host before anything is enqueued; an unsupported or
+// malformed call returns a status and never falls back to another path
+// (HOT-Step flash-attn-training, section 2: a silent fallback is
+// indistinguishable from a pass, so unsupported shapes must fail hard).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/attn_train.h"
+#include "kernels.h"
+
+namespace {
+
+using attn::Ctl;
+using attn::Dims;
+using attn::View;
+
+thread_local char g_msg[512] = "";
+
+attn_status fail(attn_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+attn_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(ATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+std::atomic<uint64_t> g_budget_ns{2000000000ull};
+
+// ----------------------------------------------------- device error word
+__device__ uint32_t g_device_error;
+
+constexpr int kMaxDevices = 64;
+uint32_t* g_err_ptr[kMaxDevices] = {};
+std::mutex g_err_mu;
+
+attn_status device_error_word(uint32_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  if (g_err_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_error);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+    g_err_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  *out = g_err_ptr[dev];
+  return ATTN_OK;
+}
+
+// ------------------------------------------------------- tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+attn_status get_encode(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+  std::call_once(g_encode_once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                    cudaEnableDefault, &q);
+    if (g_encode_err == cudaSuccess && q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  if (g_encode == nullptr)
+    return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)",
+                cudaGetErrorString(g_encode_err));
+  *fn = g_encode;
+  return ATTN_OK;
+}
+
+// 4-D map over a [B, H, S, D] bf16 view; box = [128 rows x min(D, 64) cols].
+attn_status make_map(CUtensorMap* m, const View& v, int B, int H, int S, int D, const char* name) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  attn_status st = get_encode(&enc);
+  if (st != ATTN_OK) return st;
+  const int64_t sS = v.ss * 2;
+  const int64_t sH = (H > 1 ? v.sh : v.ss * S) * 2;
+  const int64_t sB = (B > 1 ? v.sb : sH / 2 * H) * 2;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)H, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)sS, (cuuint64_t)sH, (cuuint64_t)sB};
+  const int boxc = D >= 64 ? 64 : D;
+  cuuint32_t box[4] = {(cuuint32_t)boxc, 128, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapSwizzle sw = D >= 64   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : D == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                          : CU_TENSOR_MAP_SWIZZLE_32B;
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(v.ptr), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "tensor map for %s failed (CUresult %d)", name, (int)r);
+  return ATTN_OK;
+}
+
+// ------------------------------------------------------------ validation
+attn_status check_problem(const attn_problem* p) {
+  if (p == nullptr) return fail(ATTN_ERR_INVALID, "problem is NULL");
+  if (p->B <= 0 || p->Hq <= 0 || p->Hkv <= 0 || p->Sq <= 0 || p->Skv <= 0 || p->D <= 0)
+    return fail(ATTN_ERR_INVALID, "sizes must be positive (B=%d Hq=%d Hkv=%d Sq=%d Skv=%d D=%d)",
+                p->B, p->Hq, p->Hkv, p->Sq, p->Skv, p->D);
+  if (p->Hq % p->Hkv != 0)
+    return fail(ATTN_ERR_INVALID, "Hq (%d) must be a multiple of Hkv (%d)", p->Hq, p->Hkv);
+  if (p->D != 16 && p->D != 32 && p->D != 64 && p->D != 128)
+    return fail(ATTN_ERR_UNSUPPORTED, "head dim %d unsupported (16, 32, 64, 128)", p->D);
+  if (p->mask != ATTN_MASK_FULL && p->mask != ATTN_MASK_CAUSAL && p->mask != ATTN_MASK_TTT)
+    return fail(ATTN_ERR_UNSUPPORTED, "unknown mask kind %d", p->mask);
+  if (p->mask == ATTN_MASK_TTT) {
+    if (p->ttt_step < 0) return fail(ATTN_ERR_INVALID, "ttt_step %d < 0", p->ttt_step);
+    if ((int64_t)p->Skv != (int64_t)(p->ttt_step + 1) * p->Sq)
+      return fail(ATTN_ERR_INVALID, "TTT step %d needs Skv == (t+1)*Sq = %lld, got %d",
+                  p->ttt_step, (long long)(p->ttt_step + 1) * p->Sq, p->Skv);
+  }
+  if (!std::isfinite(p->scale)) return fail(ATTN_ERR_INVALID, "scale is not finite");
+  const int64_t grid_q = (int64_t)((p->Sq + 127) / 128) * p->B * p->Hq;
+  const int64_t grid_k = (int64_t)((p->Skv + 127) / 128) * p->B * p->Hkv;
+  if (grid_q > 0x7fffffffLL || grid_k > 0x7fffffffLL)
+    return fail(ATTN_ERR_UNSUPPORTED, "problem too large for one launch");
+  return ATTN_OK;
+}
+
+attn_status check_tensor(const attn_tensor& t, int B, int H, int S, int D, const char* name) {
+  if (t.ptr == nullptr) return fail(ATTN_ERR_INVALID, "%s is NULL", name);
+  if (reinterpret_cast<uintptr_t>(t.ptr) % 16 != 0)
+    return fail(ATTN_ERR_ALIGNMENT, "%s pointer is not 16-byte aligned", name);
+  const int64_t strides[3] = {t.stride_b, t.stride_h, t.stride_s};
+  const int sizes[3] = {B, H, S};
+  const char* names[3] = {"stride_b", "stride_h", "stride_s"};
+  for (int i = 0; i < 3; ++i) {
+    if (sizes[i] == 1 && i < 2) continue;  // stride of a size-1 dim is never used
+    if (strides[i] <= 0) return fail(ATTN_ERR_INVALID, "%s.%s must be positive", name, names[i]);
+    if ((strides[i] * 2) % 16 != 0)
+      return fail(ATTN_ERR_ALIGNMENT, "%s.%s * 2 bytes is not a multiple of 16", name, names[i]);
+    if (strides[i] * 2 >= (int64_t)1 << 40)
+      return fail(ATTN_ERR_UNSUPPORTED, "%s.%s too large", name, names[i]);
+  }
+  if (t.stride_s < D) return fail(ATTN_ERR_INVALID, "%s rows overlap (stride_s < D)", name);
+  return ATTN_OK;
+}
+
+Dims make_dims(const attn_problem* p) {
+  Dims d;
+  d.B = p->B;
+  d.Hq = p->Hq;
+  d.Hkv = p->Hkv;
+  d.Sq = p->Sq;
+  d.Skv = p->Skv;
+  d.D = p->D;
+  d.G = p->Hq / p->Hkv;
+  d.geom = attn::make_geom(p->mask, p->mask == ATTN_MASK_TTT ? p->ttt_step : 0, p->Sq, p->Skv);
+  d.scale = p->scale > 0.f ? p->scale : 1.0f / std::sqrt((float)p->D);
+  d.scale_log2 = d.scale * 1.4426950408889634f;
+  return d;
+}
+
+View to_view(const attn_tensor& t) {
+  View v;
+  v.ptr = const_cast<void*>(t.ptr);
+  v.sb = t.stride_b;
+  v.sh = t.stride_h;
+  v.ss = t.stride_s;
+  return v;
+}
+
+size_t ws_bytes_for(const attn_problem* p) {
+  const size_t delta = (size_t)p->B * p->Hq * p->Sq * sizeof(float);
+  return (delta + 255) & ~(size_t)255;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_train_supports(const attn_problem* p) {
+  attn_status st = check_problem(p);
+  if (st == ATTN_OK) g_msg[0] = '\0';
+  return st;
+}
+
+attn_status attn_train_workspace_size(const attn_problem* p, size_t* bytes) {
+  attn_status st = check_problem(p);
+  if (st != ATTN_OK) return st;
+  if (bytes == nullptr) return fail(ATTN_ERR_INVALID, "bytes is NULL");
+  *bytes = ws_bytes_for(p);
+  return ATTN_OK;
+}
+
+attn_status attn_train_fwd(const attn_problem* p, attn_tensor q, attn_tensor k, attn_tensor v,
+                           attn_tensor o, float* lse, void* stream) {
+  attn_status st = check_problem(p);
+  if (st != ATTN_OK) return st;
+  if ((st = check_tensor(q, p->B, p->Hq, p->Sq, p->D, "q")) != ATTN_OK) return st;
+  if ((st = check_tensor(k, p->B, p->Hkv, p->Skv, p->D, "k")) != ATTN_OK) return st;
+  if ((st = check_tensor(v, p->B, p->Hkv, p->Skv, p->D, "v")) != ATTN_OK) return st;
+  if ((st = check_tensor(o, p->B, p->Hq, p->Sq, p->D, "o")) != ATTN_OK) return st;
+  if (lse == nullptr) return fail(ATTN_ERR_INVALID, "lse is NULL");
+  if (reinterpret_cast<uintptr_t>(lse) % 4 != 0)
+    return fail(ATTN_ERR_ALIGNMENT, "lse is not 4-byte aligned");
+
+  attn::FwdArgs a;
+  a.d = make_dims(p);
+  a.q = to_view(q);
+  a.k = to_view(k);
+  a.v = to_view(v);
+  a.o = to_view(o);
+  a.lse = lse;
+  if ((st = device_error_word(&a.ctl.err)) != ATTN_OK) return st;
+  a.ctl.budget_ns = g_budget_ns.load();
+  attn::Maps m;
+  if ((st = make_map(&m.q, a.q, p->B, p->Hq, p->Sq, p->D, "q")) != ATTN_OK) return st;
+  if ((st = make_map(&m.k, a.k, p->B, p->Hkv, p->Skv, p->D, "k")) != ATTN_OK) return st;
+  if ((st = make_map(&m.v, a.v, p->B, p->Hkv, p->Skv, p->D, "v")) != ATTN_OK) return st;
+  m.dout = m.q;
+  cudaError_t e = attn::launch_fwd(a, m, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  return ATTN_OK;
+}
+
+attn_status attn_train_bwd(const attn_problem* p, attn_tensor q, attn_tensor k, attn_tensor v,
+                           attn_tensor o, attn_tensor dout, const float* lse, attn_tensor dq,
+                           attn_tensor dk, attn_tensor dv, void* workspace, size_t ws_bytes,
+                           void* stream) {
+  attn_status st = check_problem(p);
+  if (st != ATTN_OK) return st;
+  if ((st = check_tensor(q, p->B, p->Hq, p->Sq, p->D, "q")) != ATTN_OK) return st;
+  if ((st = check_tensor(k, p->B, p->Hkv, p->Skv, p->D, "k")) != ATTN_OK) return st;
+  if ((st = check_tensor(v, p->B, p->Hkv, p->Skv, p->D, "v")) != ATTN_OK) return st;
+  if ((st = check_tensor(o, p->B, p->Hq, p->Sq, p->D, "o")) != ATTN_OK) return st;
+  if ((st = check_tensor(dout, p->B, p->Hq, p->Sq, p->D, "dout")) != ATTN_OK) return st;
+  if ((st = check_tensor(dq, p->B, p->Hq, p->Sq, p->D, "dq")) != ATTN_OK) return st;
+  if ((st = check_tensor(dk, p->B, p->Hkv, p->Skv, p->D, "dk")) != ATTN_OK) return st;
+  if ((st = check_tensor(dv, p->B, p->Hkv, p->Skv, p->D, "dv")) != ATTN_OK) return st;
+  if (lse == nullptr) return fail(ATTN_ERR_INVALID, "lse is NULL");
+  if (reinterpret_cast<uintptr_t>(lse) % 4 != 0)
+    return fail(ATTN_ERR_ALIGNMENT, "lse is not 4-byte aligned");
+  if (workspace == nullptr) return fail(ATTN_ERR_WORKSPACE, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return fail(ATTN_ERR_ALIGNMENT, "workspace is not 256-byte aligned");
+  if (ws_bytes < ws_bytes_for(p))
+    return fail(ATTN_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", ws_bytes,
+                ws_bytes_for(p));
+
+  attn::BwdArgs a;
+  a.d = make_dims(p);
+  a.q = to_view(q);
+  a.k = to_view(k);
+  a.v = to_view(v);
+  a.o = to_view(o);
+  a.dout = to_view(dout);
+  a.dq = to_view(dq);
+  a.dk = to_view(dk);
+  a.dv = to_view(dv);
+  a.lse = lse;
+  a.delta = static_cast<float*>(workspace);
+  if ((st = device_error_word(&a.ctl.err)) != ATTN_OK) return st;
+  a.ctl.budget_ns = g_budget_ns.load();
+  attn::Maps m;
+  if ((st = make_map(&m.q, a.q, p->B, p->Hq, p->Sq, p->D, "q")) != ATTN_OK) return st;
+  if ((st = make_map(&m.k, a.k, p->B, p->Hkv, p->Skv, p->D, "k")) != ATTN_OK) return st;
+  if ((st = make_map(&m.v, a.v, p->B, p->Hkv, p->Skv, p->D, "v")) != ATTN_OK) return st;
+  if ((st = make_map(&m.dout, a.dout, p->B, p->Hq, p->Sq, p->D, "dout")) != ATTN_OK) return st;
+  cudaError_t e = attn::launch_bwd(a, m, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+  return ATTN_OK;
+}
+
+const char* attn_train_last_error(void) { return g_msg; }
+
+attn_status attn_train_device_status(void* stream) {
+  uint32_t* w = nullptr;
+  attn_status st = device_error_word(&w);
+  if (st != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  uint32_t word = 0;
+  e = cudaMemcpy(&word, w, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+  if (word != 0) {
+    const uint32_t zero = 0;
+    e = cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+    return fail(ATTN_ERR_DEVICE_TIMEOUT, "a device-side wait ran out of budget (code %u)", word);
+  }
+  return ATTN_OK;
+}
+
+attn_status attn_train_set_wait_budget_ns(uint64_t ns) {
+  g_budget_ns.store(ns < 1000000ull ? 1000000ull : ns);
+  return ATTN_OK;
+}
+
+attn_status attn_train_mask_pattern(const attn_problem* p, uint8_t* bits, uint8_t* tiles,
+                                    void* stream) {
+  attn_status st = check_problem(p);
+  if (st != ATTN_OK) return st;
+  if (bits == nullptr) return fail(ATTN_ERR_INVALID, "bits is NULL");
+  cudaError_t e = attn::launch_mask_pattern(make_dims(p), bits, tiles, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mask pattern launch");
+  return ATTN_OK;
+}
+
+attn_status attn_train_probe_mma(int mode, int D, const void* a, const void* b, float* c,
+                                 void* stream) {
+  if (mode != 0 && mode != 1) return fail(ATTN_ERR_INVALID, "probe mode %d", mode);
+  if (D != 16 && D != 32 && D != 64 && D != 128) return fail(ATTN_ERR_UNSUPPORTED, "probe D %d", D);
+  if (a == nullptr || b == nullptr || c == nullptr) return fail(ATTN_ERR_INVALID, "probe NULL");
+  if (reinterpret_cast<uintptr_t>(a) % 16 || reinterpret_cast<uintptr_t>(b) % 16)
+    return fail(ATTN_ERR_ALIGNMENT, "probe operands not 16-byte aligned");
+  Ctl ctl;
+  attn_status st = device_error_word(&ctl.err);
+  if (st != ATTN_OK) return st;
+  ctl.budget_ns = g_budget_ns.load();
+  View va{const_cast<void*>(a), 0, 0, mode == 0 ? D : 128};
+  View vb{const_cast<void*>(b), 0, 0, D};
+  CUtensorMap ta, tb;
+  // mode 1 reads `a` with plain loads; its map is built but unused
+  if ((st = make_map(&ta, va, 1, 1, 128, D, "probe a")) != ATTN_OK) return st;
+  if ((st = make_map(&tb, vb, 1, 1, 128, D, "probe b")) != ATTN_OK) return st;
+  cudaError_t e = attn::launch_probe(mode, D, ta, tb, a, c, ctl, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "probe launch");
+  return ATTN_OK;
+}
+
+attn_status attn_train_selftest_wait_timeout(void* stream) {
+  Ctl ctl;
+  attn_status st = device_error_word(&ctl.err);
+  if (st != ATTN_OK) return st;
+  ctl.budget_ns = 50000000ull;  // 50 ms
+  cudaError_t e = attn::launch_selftest_wait(ctl, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "selftest launch");
+  return ATTN_OK;
+}
+
+}  // extern "C"

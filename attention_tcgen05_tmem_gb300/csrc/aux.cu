@@ -1,0 +1,209 @@
+// aux.cu -- test-only kernels: the device view of the mask (both the row-side
+// schedule used by the forward and dQ passes and the column-side schedule used
+// by the dK/dV pass), a one-tile tcgen05 descriptor probe, and a bounded-wait
+// self-test that times out on purpose (nothing ever arrives on its barrier).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "sched.cuh"
+#include "tile.cuh"
+
+namespace attn {
+namespace {
+
+// bits[0][q][kv]: pair visited and unmasked by the row-side schedule
+// bits[1][q][kv]: same for the column-side schedule
+// Both include the TTT suffix diagonals exactly as the kernels address them
+// (key row i*Sq + q, i = 1..t).  tiles[qt][kt] = tile class of the tiled part.
+__global__ void mask_pattern_kernel(const Dims d, uint8_t* bits, uint8_t* tiles) {
+  const MaskGeom g = d.geom;
+  const int64_t n = (int64_t)d.Sq * d.Skv;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int q = (int)(idx / d.Skv);
+    const int kv = (int)(idx % d.Skv);
+    uint8_t row_side = 0, col_side = 0;
+    if (kv < g.kv_main) {
+      const int k0 = (kv / kBN) * kBN;
+      // row side: the forward pairs query tiles; its key range covers both
+      const int qp0 = (q / (2 * kBM)) * 2 * kBM;
+      const int qt0 = (q / kBM) * kBM;
+      const bool fwd_visits = k0 < kv_end_for_rows(g, qp0, 2 * kBM);
+      const bool dq_visits = k0 < kv_end_for_rows(g, qt0, kBM);
+      const bool unmasked = tile_is_full(g, qt0, k0) || (kv - k0) <= col_limit(g, q, k0);
+      row_side = (fwd_visits && dq_visits && unmasked) ? 1 : 0;
+      // column side: query tiles from q_begin_for_kv(k0) upward
+      const int qt_first = q_begin_for_kv(g, k0) / kBM;
+      const bool visits = q / kBM >= qt_first;
+      const bool keep = tile_is_full(g, qt0, k0) || g.kind == kMaskFull || q >= kv + g.shift;
+      col_side = (visits && keep) ? 1 : 0;
+    } else if (g.ttt > 0) {
+      const int64_t rel = (int64_t)kv - q;
+      const bool diag = kv >= d.Sq && rel > 0 && rel % d.Sq == 0 && rel / d.Sq <= g.ttt;
+      row_side = col_side = diag ? 1 : 0;
+    }
+    bits[idx] = row_side;
+    bits[n + idx] = col_side;
+  }
+  if (tiles != nullptr) {
+    const int nqt = cdiv(d.Sq, kBM), nkt = cdiv(g.kv_main, kBN);
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < (int64_t)nqt * nkt;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+      const int qt = (int)(idx / nkt), kt = (int)(idx % nkt);
+      tiles[idx] = (uint8_t)tile_class(g, qt * kBM, kt * kBN);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- probe
+template <int D>
+__global__ void __launch_bounds__(128, 1)
+    probe_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
+                 const __nv_bfloat16* a_global, float* c, int mode, Ctl cc) {
+  using TG = TileGeom<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + (((smem_u32(smem_raw) + 1023u) & ~1023u) - smem_u32(smem_raw));
+  uint8_t* tA = smem;
+  uint8_t* tB = smem + TG::TILE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * TG::TILE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl ctl{cc.err, abort_flag, cc.budget_ns};
+  const int r = threadIdx.x;
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+
+  if (mode == 1) {
+    // A row r (128 bf16) into TMEM columns [128, 192), two values per column
+    const uint32_t* arow = reinterpret_cast<const uint32_t*>(a_global + (int64_t)r * 128);
+    uint32_t v[32];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] = arow[h * 32 + e];
+      tmem_st32(tmem + lane_base + 128 + h * 32, v);
+    }
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (threadIdx.x == 0) {
+    if (mode == 0) {
+      mbar_arrive_expect_tx(&bars[0], 2 * TG::TILE_BYTES);
+      TG::load(tA, &ta, &bars[0], 0, 0, 0);
+      TG::load(tB, &tb, &bars[0], 0, 0, 0);
+    } else {
+      mbar_arrive_expect_tx(&bars[0], TG::TILE_BYTES);
+      TG::load(tB, &tb, &bars[0], 0, 0, 0);
+    }
+    if (mbar_wait(&bars[0], 0, ctl)) {
+      tc_fence_after();
+      if (mode == 0) {
+        constexpr uint32_t idesc = make_idesc_bf16(128, 128, false, false);
+        for (int kk = 0; kk < TG::KSTEPS; ++kk)
+          umma_ss(tmem, TG::kmajor(smem_u32(tA), kk), TG::kmajor(smem_u32(tB), kk), idesc, kk > 0);
+      } else {
+        constexpr uint32_t idesc = make_idesc_bf16(128, D, false, true);
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(tmem, tmem + 128 + 8 * kk, TG::mnmajor(smem_u32(tB), kk), idesc, kk > 0);
+      }
+      umma_commit(&bars[1]);
+    } else {
+      umma_commit(&bars[1]);
+    }
+  }
+  __syncwarp();
+  const bool ok = mbar_wait_warp(&bars[1], 0, ctl);
+  if (ok) {
+    tc_fence_after();
+    const int ncol = (mode == 0) ? 128 : D;
+    for (int c0 = 0; c0 < ncol; c0 += 16) {
+      uint32_t v[16];
+      tmem_ld16(tmem + lane_base + c0, v);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) c[(int64_t)r * ncol + c0 + e] = __uint_as_float(v[e]);
+    }
+  }
+  (void)lane;
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// ------------------------------------------------------- wait self-test
+// Waits on a barrier that nothing will ever complete; the bounded wait must
+// give up, record kErrWaitTimeout and let the kernel return normally.
+__global__ void selftest_wait_kernel(Ctl cc) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const WaitCtl ctl{cc.err, &abort_flag, cc.budget_ns};
+  mbar_wait_warp(&bar, 0, ctl);
+}
+
+template <int D>
+cudaError_t launch_probe_d(int mode, const CUtensorMap& ta, const CUtensorMap& tb,
+                           const void* a_global, float* c, Ctl ctl, cudaStream_t s) {
+  const int smem = 2 * TileGeom<D>::TILE_BYTES + 64 + 1024;
+  auto kern = probe_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<1, 128, smem, s>>>(ta, tb, static_cast<const __nv_bfloat16*>(a_global), c, mode, ctl);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_mask_pattern(const Dims& d, uint8_t* bits, uint8_t* tiles, cudaStream_t s) {
+  const int64_t n = (int64_t)d.Sq * d.Skv;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  if (blocks < 1) blocks = 1;
+  mask_pattern_kernel<<<(unsigned)blocks, 256, 0, s>>>(d, bits, tiles);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_probe(int mode, int D, const CUtensorMap& ta, const CUtensorMap& tb,
+                         const void* a_global, float* c, Ctl ctl, cudaStream_t s) {
+  switch (D) {
+    case 16: return launch_probe_d<16>(mode, ta, tb, a_global, c, ctl, s);
+    case 32: return launch_probe_d<32>(mode, ta, tb, a_global, c, ctl, s);
+    case 64: return launch_probe_d<64>(mode, ta, tb, a_global, c, ctl, s);
+    case 128: return launch_probe_d<128>(mode, ta, tb, a_global, c, ctl, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_selftest_wait(Ctl ctl, cudaStream_t s) {
+  selftest_wait_kernel<<<1, 32, 0, s>>>(ctl);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

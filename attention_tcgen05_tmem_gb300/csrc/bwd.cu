@@ -1,0 +1,824 @@
+// bwd.cu -- deterministic fused attention backward on tcgen05 (sm_103a).
+//
+// The backward recomputes the weights from the saved LSE (CS336 README,
+// "Flash Attention (Triton)": P is recomputed from L) and never stores the
+// S x S score matrix.  It is atomic-free with fixed schedules, so results are
+// bitwise reproducible (HOT-Step flash-attn-training, section 1: "no fp
+// atomics, fixed schedules"):
+//
+//   1. prep:  Delta[q] = sum_d dO[q,d] O[q,d]               (fp32, from bf16)
+//   2. dK/dV: one CTA per (b, kv head, 128-key tile) owns its dK and dV rows.
+//             It walks the group's q heads in ascending order and, for each,
+//             its visible query tiles in ascending order:
+//               S^T = K Q^T,  P^T = exp(c S^T - LSE),  dV += P^T dO,
+//               dP^T = V dO^T,  dS^T = P^T (dP^T - Delta),  dK += dS^T Q
+//             and writes dK (times c) and dV once.
+//   3. dQ:    one CTA per (b, q head, 128-query tile) walks its visible key
+//             tiles in ascending order:
+//               S = Q K^T, dP = dO V^T, dS = P (dP - Delta), dQ += dS K
+//             then adds the TTT suffix-diagonal terms and writes c dQ once.
+//   4. TTT:   the keys of appended segments (one diagonal each) get
+//             dV = sum_g p dO and dK = c sum_g dS q, summed over the group's
+//             q heads in ascending order, from a per-row warp pass.
+//
+// Tensor-core kernels use 10 warps: 0-7 elementwise (two warpgroups split the
+// 128 columns of each S / dP tile; thread = TMEM lane = row), 8 TMA producer,
+// 9 tcgen05 issuer.  P^T, dS^T and dS are written back to tensor memory as
+// bf16 and used as the A operand of the next MMA directly from there.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "sched.cuh"
+#include "tile.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  const uint32_t a = smem_u32(p);
+  return p + (((a + 1023u) & ~1023u) - a);
+}
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > 200000000ull) break;
+  }
+}
+
+__device__ __forceinline__ const __nv_bfloat16* row_ptr(const View& v, int b, int h, int64_t s) {
+  return reinterpret_cast<const __nv_bfloat16*>(v.ptr) + b * v.sb + h * v.sh + s * v.ss;
+}
+__device__ __forceinline__ __nv_bfloat16* row_ptr_w(const View& v, int b, int h, int64_t s) {
+  return reinterpret_cast<__nv_bfloat16*>(v.ptr) + b * v.sb + h * v.sh + s * v.ss;
+}
+
+// Dot product of two bf16 rows of length D (fp32 accumulate).
+template <int D>
+__device__ __forceinline__ float dot_rows(const __nv_bfloat16* x, const __nv_bfloat16* y) {
+  float acc = 0.f;
+#pragma unroll
+  for (int c0 = 0; c0 < D; c0 += 8) {
+    const uint4 xa = *reinterpret_cast<const uint4*>(x + c0);
+    const uint4 ya = *reinterpret_cast<const uint4*>(y + c0);
+    const __nv_bfloat162* xv = reinterpret_cast<const __nv_bfloat162*>(&xa);
+    const __nv_bfloat162* yv = reinterpret_cast<const __nv_bfloat162*>(&ya);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 xf = __bfloat1622float2(xv[e]);
+      const float2 yf = __bfloat1622float2(yv[e]);
+      acc = fmaf(xf.x, yf.x, acc);
+      acc = fmaf(xf.y, yf.y, acc);
+    }
+  }
+  return acc;
+}
+
+// Store 16 fp32 values (times mul) as bf16 at row + c0.
+__device__ __forceinline__ void store16_bf16(__nv_bfloat16* row, const float* v, float mul) {
+#pragma unroll
+  for (int e = 0; e < 16; e += 8) {
+    uint4 pkt;
+    pkt.x = pack_bf16x2(v[e + 0] * mul, v[e + 1] * mul);
+    pkt.y = pack_bf16x2(v[e + 2] * mul, v[e + 3] * mul);
+    pkt.z = pack_bf16x2(v[e + 4] * mul, v[e + 5] * mul);
+    pkt.w = pack_bf16x2(v[e + 6] * mul, v[e + 7] * mul);
+    *reinterpret_cast<uint4*>(row + e) = pkt;
+  }
+}
+
+// ===================================================================== prep
+// Delta[b, h, q] = sum_d dO * O.  D/8 threads per row, 16-byte loads.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdArgs a) {
+  constexpr int TPR = D / 8;  // threads per row
+  constexpr int RPB = 256 / TPR;
+  const int64_t total = (int64_t)a.d.B * a.d.Hq * a.d.Sq;
+  const int64_t row = (int64_t)blockIdx.x * RPB + threadIdx.x / TPR;
+  const int sub = threadIdx.x % TPR;
+  float acc = 0.f;
+  if (row < total) {
+    const int q = (int)(row % a.d.Sq);
+    const int bh = (int)(row / a.d.Sq);
+    const int h = bh % a.d.Hq, b = bh / a.d.Hq;
+    const __nv_bfloat16* o = row_ptr(a.o, b, h, q) + sub * 8;
+    const __nv_bfloat16* g = row_ptr(a.dout, b, h, q) + sub * 8;
+    const uint4 oa = *reinterpret_cast<const uint4*>(o);
+    const uint4 ga = *reinterpret_cast<const uint4*>(g);
+    const __nv_bfloat162* ov = reinterpret_cast<const __nv_bfloat162*>(&oa);
+    const __nv_bfloat162* gv = reinterpret_cast<const __nv_bfloat162*>(&ga);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 of = __bfloat1622float2(ov[e]);
+      const float2 gf = __bfloat1622float2(gv[e]);
+      acc = fmaf(of.x, gf.x, acc);
+      acc = fmaf(of.y, gf.y, acc);
+    }
+  }
+#pragma unroll
+  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, TPR);
+  if (row < total && sub == 0) a.delta[row] = acc;
+}
+
+// ===================================================================== dK/dV
+template <int D>
+struct DkdvLayout {
+  using TG = TileGeom<D>;
+  static constexpr int NST = (D == 128) ? 2 : (D == 64 ? 4 : 6);
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = TG::TILE_BYTES;
+  static constexpr int ST_OFF = 2 * TG::TILE_BYTES;              // stages: Q, dO
+  static constexpr int STAGE_BYTES = 2 * TG::TILE_BYTES;
+  static constexpr int STAT_OFF = ST_OFF + NST * STAGE_BYTES;     // per stage: lse2[128], delta[128]
+  static constexpr int BAR_OFF = STAT_OFF + NST * 2 * 128 * 4;
+  // kv_full, qdo_full[NST], qdo_empty[NST], s_full, dp_full, p_ready, ds_ready, done, drain
+  static constexpr int NBAR = 1 + 2 * NST + 6;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int BYTES = MISC_OFF + 16;
+  // at least 116 KB so that only one CTA fits per SM: each holds all 512 TMEM columns
+  static constexpr int ALLOC = (BYTES + 1024 > 116 * 1024) ? BYTES + 1024 : 116 * 1024;
+  static_assert(ALLOC <= 227 * 1024, "shared memory budget");
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                    const BwdArgs a) {
+  using TG = TileGeom<D>;
+  using L = DkdvLayout<D>;
+  constexpr int NST = L::NST;
+  extern __shared__ uint8_t smem_raw[];
+  if (*reinterpret_cast<volatile uint32_t*>(a.ctl.err) != 0) return;
+
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  uint64_t* kv_full = bars;
+  uint64_t* qdo_full = bars + 1;
+  uint64_t* qdo_empty = qdo_full + NST;
+  uint64_t* s_full = qdo_empty + NST;
+  uint64_t* dp_full = s_full + 1;
+  uint64_t* p_ready = dp_full + 1;
+  uint64_t* ds_ready = p_ready + 1;
+  uint64_t* done = ds_ready + 1;
+  uint64_t* drain = done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
+  float* stats = reinterpret_cast<float*>(smem + L::STAT_OFF);  // [NST][2][128]
+
+  const Dims& d = a.d;
+  const MaskGeom g = d.geom;
+  const int n_kt = cdiv(g.kv_main, kBN);
+  const int BH = d.B * d.Hkv;
+  // heaviest key tiles (smallest k0 under causal/TTT) first
+  const int kt = (int)(blockIdx.x / BH);
+  const int bh = blockIdx.x % BH;
+  const int hk = bh % d.Hkv;
+  const int b = bh / d.Hkv;
+  const int k0 = kt * kBN;
+  const int n_qt_all = cdiv(d.Sq, kBM);
+  const int qt_begin = q_begin_for_kv(g, k0) / kBM;
+  const int n_q = n_qt_all - qt_begin;  // visible query tiles per q head
+  const int N = (n_q > 0 ? n_q : 0) * d.G;
+  (void)n_kt;
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&qdo_full[s], 1);
+      mbar_init(&qdo_empty[s], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(p_ready, 256);
+    mbar_init(ds_ready, 256);
+    mbar_init(done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl ctl{a.ctl.err, abort_flag, a.ctl.budget_ns};
+
+  auto iter_head = [&](int it) { return hk * d.G + it / n_q; };
+  auto iter_q0 = [&](int it) { return (qt_begin + it % n_q) * kBM; };
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (N > 0) {
+      if (lane == 0) {
+        tma_prefetch_desc(&tq);
+        tma_prefetch_desc(&tdo);
+        mbar_arrive_expect_tx(kv_full, 2 * TG::TILE_BYTES);
+        TG::load(smem + L::K_OFF, &tk, kv_full, k0, hk, b);
+        TG::load(smem + L::V_OFF, &tv, kv_full, k0, hk, b);
+      }
+      int issued = 0;
+      for (int it = 0; it < N; ++it) {
+        const int s = it % NST;
+        const uint32_t ph = (uint32_t)(it / NST) & 1u;
+        if (!mbar_wait_warp(&qdo_empty[s], ph ^ 1u, ctl)) break;
+        const int h = iter_head(it);
+        const int q0 = iter_q0(it);
+        float* st = stats + s * 256;
+        const int64_t rbase = ((int64_t)b * d.Hq + h) * d.Sq;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = lane * 4 + e;
+          const int qq = q0 + r;
+          const bool in = qq < d.Sq;
+          st[r] = in ? a.lse[rbase + qq] * kLog2e : INFINITY;
+          st[128 + r] = in ? a.delta[rbase + qq] : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&qdo_full[s], 2 * TG::TILE_BYTES);
+          uint8_t* dst = smem + L::ST_OFF + s * L::STAGE_BYTES;
+          TG::load(dst, &tq, &qdo_full[s], q0, h, b);
+          TG::load(dst + TG::TILE_BYTES, &tdo, &qdo_full[s], q0, h, b);
+        }
+        issued = it + 1;
+      }
+      if (lane == 0 && *abort_flag) {
+        drain_wait(kv_full, 0);
+        for (int it = issued - NST < 0 ? 0 : issued - NST; it < issued; ++it)
+          drain_wait(&qdo_full[it % NST], (uint32_t)(it / NST) & 1u);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------- MMA
+    if (lane == 0 && N > 0) {
+      constexpr uint32_t idesc_s = make_idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc_g = make_idesc_bf16(128, D, false, true);
+      const uint32_t sK = smem_u32(smem + L::K_OFF);
+      const uint32_t sV = smem_u32(smem + L::V_OFF);
+      const uint32_t sST = smem_u32(smem + L::ST_OFF);
+      auto sq = [&](int it) { return sST + (it % NST) * L::STAGE_BYTES; };
+      auto sdo = [&](int it) { return sST + (it % NST) * L::STAGE_BYTES + TG::TILE_BYTES; };
+      auto issue_st = [&](int it) {  // S^T = K Q^T
+#pragma unroll
+        for (int kk = 0; kk < TG::KSTEPS; ++kk)
+          umma_ss(tmem + 0, TG::kmajor(sK, kk), TG::kmajor(sq(it), kk), idesc_s, kk > 0);
+      };
+      auto issue_dpt = [&](int it) {  // dP^T = V dO^T
+#pragma unroll
+        for (int kk = 0; kk < TG::KSTEPS; ++kk)
+          umma_ss(tmem + 128, TG::kmajor(sV, kk), TG::kmajor(sdo(it), kk), idesc_s, kk > 0);
+      };
+      // A operand in TMEM: q columns 16kk.. of warpgroup kk/4 live at 64*(kk/4) + 8*(kk%4)
+      auto issue_grad = [&](uint32_t acc_col, uint32_t a_col, uint32_t bt, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < kBM / 16; ++kk)
+          umma_ts(tmem + acc_col, tmem + a_col + 64 * (kk / 4) + 8 * (kk % 4),
+                  TG::mnmajor(bt, kk), idesc_g, (acc || kk > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(kv_full, 0, ctl) && mbar_wait(&qdo_full[0], 0, ctl);
+      if (ok) {
+        tc_fence_after();
+        issue_st(0);
+        umma_commit(s_full);
+        issue_dpt(0);
+        umma_commit(dp_full);
+      }
+      for (int it = 0; ok && it < N; ++it) {
+        if (!(ok = mbar_wait(p_ready, (uint32_t)it & 1u, ctl))) break;
+        tc_fence_after();
+        issue_grad(256, 0, sdo(it), it > 0);  // dV += P^T dO
+        const bool more = it + 1 < N;
+        if (more) {
+          if (!(ok = mbar_wait(&qdo_full[(it + 1) % NST], (uint32_t)((it + 1) / NST) & 1u, ctl)))
+            break;
+          tc_fence_after();
+          issue_st(it + 1);
+          umma_commit(s_full);
+        }
+        if (!(ok = mbar_wait(ds_ready, (uint32_t)it & 1u, ctl))) break;
+        tc_fence_after();
+        issue_grad(256 + D, 128, sq(it), it > 0);  // dK += dS^T Q
+        umma_commit(&qdo_empty[it % NST]);
+        if (more) {
+          issue_dpt(it + 1);
+          umma_commit(dp_full);
+        }
+      }
+      if (ok) {
+        umma_commit(done);
+      } else {
+        umma_commit(drain);
+        drain_wait(drain, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------- elementwise
+    const int wg = warp >> 2;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const int kv = k0 + r;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_base + 64 * wg;         // S^T / P^T columns of this WG
+    const uint32_t tdP = tmem + lane_base + 128 + 64 * wg;  // dP^T / dS^T
+    const float sl2 = d.scale_log2;
+    bool ok = true;
+    for (int it = 0; it < N; ++it) {
+      const int s = it % NST;
+      const int q0 = iter_q0(it);
+      const float* lse2 = stats + s * 256 + 64 * wg;
+      const float* dl = stats + s * 256 + 128 + 64 * wg;
+      if (!(ok = mbar_wait_warp(s_full, (uint32_t)it & 1u, ctl))) break;
+      tc_fence_after();
+      uint32_t raw[64];
+      tmem_ld32x2(tS, tS + 32, raw);
+      // keys see queries q >= kv + shift (non-full masks); rows past Sq have lse2 = inf
+      const bool full = tile_is_full(g, q0, k0);
+      const int cmin = (g.kind == kMaskFull) ? 0 : kv + g.shift - q0 - 64 * wg;
+      float p[64];
+#pragma unroll
+      for (int c = 0; c < 64; c += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float v = ex2_approx(fmaf(__uint_as_float(raw[c + e]), sl2, -lv[e]));
+          if (!full && c + e < cmin) v = 0.f;
+          p[c + e] = v;
+        }
+      }
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
+      tmem_st32(tS, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(p_ready);
+
+      if (!(ok = mbar_wait_warp(dp_full, (uint32_t)it & 1u, ctl))) break;
+      tc_fence_after();
+      tmem_ld32x2(tdP, tdP + 32, raw);
+#pragma unroll
+      for (int c = 0; c < 64; c += 4) {
+        const float4 d4 = *reinterpret_cast<const float4*>(dl + c);
+        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) p[c + e] = p[c + e] * (__uint_as_float(raw[c + e]) - dv[e]);
+      }
+#pragma unroll
+      for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
+      tmem_st32(tdP, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(ds_ready);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && N > 0) ok = mbar_wait_warp(done, 0, ctl);
+    if (ok) {
+      const bool store = kv < g.kv_main;
+      __nv_bfloat16* dvrow = row_ptr_w(a.dv, b, hk, kv);
+      __nv_bfloat16* dkrow = row_ptr_w(a.dk, b, hk, kv);
+      if (N > 0) tc_fence_after();
+      for (int c0 = 16 * wg; c0 < D; c0 += 32) {
+        float vals[16];
+        uint32_t raw[16];
+        if (N > 0) {
+          tmem_ld16(tmem + lane_base + 256 + c0, raw);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) vals[e] = __uint_as_float(raw[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) vals[e] = 0.f;
+        }
+        if (store) store16_bf16(dvrow + c0, vals, 1.f);
+        if (N > 0) {
+          tmem_ld16(tmem + lane_base + 256 + D + c0, raw);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) vals[e] = __uint_as_float(raw[e]);
+        }
+        if (store) store16_bf16(dkrow + c0, vals, d.scale);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ======================================================================= dQ
+template <int D>
+struct DqLayout {
+  using TG = TileGeom<D>;
+  static constexpr int NSLOT = (D == 128) ? 4 : (D == 64 ? 8 : 10);
+  static constexpr int Q_OFF = 0;
+  static constexpr int DO_OFF = TG::TILE_BYTES;
+  static constexpr int KV_OFF = 2 * TG::TILE_BYTES;
+  static constexpr int BAR_OFF = KV_OFF + NSLOT * TG::TILE_BYTES;
+  // qdo_full, kv_full[NSLOT], kv_empty[NSLOT], sdp_full, sdp_used, ds_ready, ds_free, done, drain
+  static constexpr int NBAR = 1 + 2 * NSLOT + 6;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int BYTES = MISC_OFF + 16;
+  // at least 116 KB so that only one CTA fits per SM: each holds all 512 TMEM columns
+  static constexpr int ALLOC = (BYTES + 1024 > 116 * 1024) ? BYTES + 1024 : 116 * 1024;
+  static_assert(ALLOC <= 227 * 1024, "shared memory budget");
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                  const BwdArgs a) {
+  using TG = TileGeom<D>;
+  using L = DqLayout<D>;
+  constexpr int NSLOT = L::NSLOT;
+  constexpr int T_S = 0, T_DP = 128, T_DQ = 256, T_DS = 384;
+  extern __shared__ uint8_t smem_raw[];
+  if (*reinterpret_cast<volatile uint32_t*>(a.ctl.err) != 0) return;
+
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  uint64_t* qdo_full = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = kv_full + NSLOT;
+  uint64_t* sdp_full = kv_empty + NSLOT;
+  uint64_t* sdp_used = sdp_full + 1;
+  uint64_t* ds_ready = sdp_used + 1;
+  uint64_t* ds_free = ds_ready + 1;
+  uint64_t* done = ds_free + 1;
+  uint64_t* drain = done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
+
+  const Dims& d = a.d;
+  const MaskGeom g = d.geom;
+  const int n_qt = cdiv(d.Sq, kBM);
+  const int BH = d.B * d.Hq;
+  int qt, bh;
+  if (g.kind == kMaskFull) {
+    qt = blockIdx.x % n_qt;
+    bh = blockIdx.x / n_qt;
+  } else {
+    qt = n_qt - 1 - (int)(blockIdx.x / BH);
+    bh = blockIdx.x % BH;
+  }
+  const int h = bh % d.Hq;
+  const int b = bh / d.Hq;
+  const int hk = h / d.G;
+  const int q0 = qt * kBM;
+  const int n_kv = cdiv(kv_end_for_rows(g, q0, kBM), kBN);
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+  if (threadIdx.x == 0) {
+    mbar_init(qdo_full, 1);
+    for (int s = 0; s < NSLOT; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    mbar_init(sdp_full, 1);
+    mbar_init(sdp_used, 256);
+    mbar_init(ds_ready, 256);
+    mbar_init(ds_free, 1);
+    mbar_init(done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl ctl{a.ctl.err, abort_flag, a.ctl.budget_ns};
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n_kv > 0) {
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      mbar_arrive_expect_tx(qdo_full, 2 * TG::TILE_BYTES);
+      TG::load(smem + L::Q_OFF, &tq, qdo_full, q0, h, b);
+      TG::load(smem + L::DO_OFF, &tdo, qdo_full, q0, h, b);
+      int issued = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        bool ok = true;
+        for (int w = 0; w < 2; ++w) {
+          const int idx = 2 * j + w;
+          const int s = idx % NSLOT;
+          const uint32_t ph = (uint32_t)(idx / NSLOT) & 1u;
+          if (!mbar_wait(&kv_empty[s], ph ^ 1u, ctl)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&kv_full[s], TG::TILE_BYTES);
+          TG::load(smem + L::KV_OFF + s * TG::TILE_BYTES, w == 0 ? &tk : &tv, &kv_full[s],
+                   j * kBN, hk, b);
+          issued = idx + 1;
+        }
+        if (!ok) break;
+      }
+      if (*abort_flag) {
+        drain_wait(qdo_full, 0);
+        for (int idx = issued - NSLOT < 0 ? 0 : issued - NSLOT; idx < issued; ++idx)
+          drain_wait(&kv_full[idx % NSLOT], (uint32_t)(idx / NSLOT) & 1u);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------- MMA
+    if (lane == 0 && n_kv > 0) {
+      constexpr uint32_t idesc_s = make_idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc_g = make_idesc_bf16(128, D, false, true);
+      const uint32_t sQ = smem_u32(smem + L::Q_OFF);
+      const uint32_t sDO = smem_u32(smem + L::DO_OFF);
+      const uint32_t sKV = smem_u32(smem + L::KV_OFF);
+      auto slot = [&](int idx) { return sKV + (idx % NSLOT) * TG::TILE_BYTES; };
+      auto phase = [](int idx) { return (uint32_t)(idx / NSLOT) & 1u; };
+      bool ok = mbar_wait(qdo_full, 0, ctl);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int ki = 2 * j, vi = 2 * j + 1;
+        ok = mbar_wait(&kv_full[ki % NSLOT], phase(ki), ctl) &&
+             mbar_wait(&kv_full[vi % NSLOT], phase(vi), ctl);
+        if (ok && j > 0) ok = mbar_wait(sdp_used, (uint32_t)(j - 1) & 1u, ctl);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < TG::KSTEPS; ++kk)
+          umma_ss(tmem + T_S, TG::kmajor(sQ, kk), TG::kmajor(slot(ki), kk), idesc_s, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < TG::KSTEPS; ++kk)
+          umma_ss(tmem + T_DP, TG::kmajor(sDO, kk), TG::kmajor(slot(vi), kk), idesc_s, kk > 0);
+        umma_commit(sdp_full);
+        umma_commit(&kv_empty[vi % NSLOT]);
+        if (j > 0) {
+          if (!(ok = mbar_wait(ds_ready, (uint32_t)(j - 1) & 1u, ctl))) break;
+          tc_fence_after();
+          const int kp = 2 * (j - 1);
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            umma_ts(tmem + T_DQ, tmem + T_DS + 8 * kk, TG::mnmajor(slot(kp), kk), idesc_g,
+                    (j - 1 > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(ds_free);
+          umma_commit(&kv_empty[kp % NSLOT]);
+        }
+      }
+      if (ok) ok = mbar_wait(ds_ready, (uint32_t)(n_kv - 1) & 1u, ctl);
+      if (ok) {
+        tc_fence_after();
+        const int kp = 2 * (n_kv - 1);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          umma_ts(tmem + T_DQ, tmem + T_DS + 8 * kk, TG::mnmajor(slot(kp), kk), idesc_g,
+                  (n_kv - 1 > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(done);
+        umma_commit(&kv_empty[kp % NSLOT]);
+      } else {
+        umma_commit(drain);
+        drain_wait(drain, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------- elementwise
+    const int wg = warp >> 2;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const int q = q0 + r;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const float sl2 = d.scale_log2;
+    const int64_t rrow = ((int64_t)b * d.Hq + h) * d.Sq + q;
+    const bool qin = q < d.Sq;
+    const float lse2 = qin ? a.lse[rrow] * kLog2e : INFINITY;
+    const float delta = qin ? a.delta[rrow] : 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      if (!(ok = mbar_wait_warp(sdp_full, (uint32_t)j & 1u, ctl))) break;
+      tc_fence_after();
+      uint32_t rs[64], rp[64];
+      tmem_ld32x2(tmem + lane_base + T_S + 64 * wg, tmem + lane_base + T_S + 64 * wg + 32, rs);
+      tmem_ld32x2(tmem + lane_base + T_DP + 64 * wg, tmem + lane_base + T_DP + 64 * wg + 32, rp);
+      tc_fence_before();
+      mbar_arrive(sdp_used);
+      const int k0 = j * kBN;
+      const bool full = tile_is_full(g, q0, k0);
+      const int lim = col_limit(g, q, k0) - 64 * wg;
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 64; c += 2) {
+        float p0 = ex2_approx(fmaf(__uint_as_float(rs[c]), sl2, -lse2));
+        float p1 = ex2_approx(fmaf(__uint_as_float(rs[c + 1]), sl2, -lse2));
+        if (!full && c > lim) p0 = 0.f;
+        if (!full && c + 1 > lim) p1 = 0.f;
+        const float ds0 = p0 * (__uint_as_float(rp[c]) - delta);
+        const float ds1 = p1 * (__uint_as_float(rp[c + 1]) - delta);
+        pk[c / 2] = pack_bf16x2(ds0, ds1);
+      }
+      if (j > 0) {
+        if (!(ok = mbar_wait_warp(ds_free, (uint32_t)(j - 1) & 1u, ctl))) break;
+        tc_fence_after();
+      }
+      tmem_st32(tmem + lane_base + T_DS + 32 * wg, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(ds_ready);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && n_kv > 0) ok = mbar_wait_warp(done, 0, ctl);
+    if (ok) {
+      if (n_kv > 0) tc_fence_after();
+      // TTT suffix diagonals: ds_i = p_i (dO . v_i - Delta), dQ += ds_i k_i
+      float ds_i[8];
+      int n_diag = 0;
+      const __nv_bfloat16* qrow = row_ptr(a.q, b, h, q);
+      const __nv_bfloat16* dorow = row_ptr(a.dout, b, h, q);
+      for (int c0 = 16 * wg; c0 < D; c0 += 32) {
+        float acc[16];
+        if (n_kv > 0) {
+          uint32_t raw[16];
+          tmem_ld16(tmem + lane_base + T_DQ + c0, raw);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) acc[e] = __uint_as_float(raw[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+        }
+        if (qin && g.ttt > 0) {
+          for (int i0 = 1; i0 <= g.ttt; i0 += 8) {
+            const int cnt = min(8, g.ttt - i0 + 1);
+            if (c0 == 16 * wg || n_diag != i0) {
+              // (re)compute this batch of diagonal weights
+              for (int u = 0; u < cnt; ++u) {
+                const int64_t kr = (int64_t)(i0 + u) * d.Sq + q;
+                const float sv = dot_rows<D>(qrow, row_ptr(a.k, b, hk, kr));
+                const float dp = dot_rows<D>(dorow, row_ptr(a.v, b, hk, kr));
+                const float pv = ex2_approx(fmaf(sv, sl2, -lse2));
+                ds_i[u] = pv * (dp - delta);
+              }
+              n_diag = i0;
+            }
+            for (int u = 0; u < cnt; ++u) {
+              const __nv_bfloat16* krow = row_ptr(a.k, b, hk, (int64_t)(i0 + u) * d.Sq + q) + c0;
+#pragma unroll
+              for (int e = 0; e < 16; e += 8) {
+                const uint4 ka = *reinterpret_cast<const uint4*>(krow + e);
+                const __nv_bfloat162* kv2 = reinterpret_cast<const __nv_bfloat162*>(&ka);
+#pragma unroll
+                for (int f = 0; f < 4; ++f) {
+                  const float2 kf = __bfloat1622float2(kv2[f]);
+                  acc[e + 2 * f] = fmaf(ds_i[u], kf.x, acc[e + 2 * f]);
+                  acc[e + 2 * f + 1] = fmaf(ds_i[u], kf.y, acc[e + 2 * f + 1]);
+                }
+              }
+            }
+          }
+        }
+        if (qin) store16_bf16(row_ptr_w(a.dq, b, h, q) + c0, acc, d.scale);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ================================================================ TTT diag
+// dK/dV of the keys of appended segments i = 1..t: key row i*Sq + r is seen
+// only by query row r of every q head of its group.  One warp per key row;
+// dot products reduce with warp shuffles in a fixed butterfly order.
+template <int D>
+__global__ void __launch_bounds__(256) ttt_diag_bwd_kernel(const BwdArgs a) {
+  constexpr int EPL = (D + 31) / 32;  // elements per lane
+  const Dims& d = a.d;
+  const int t = d.geom.ttt;
+  const int64_t rows = (int64_t)d.B * d.Hkv * t * d.Sq;
+  const int64_t wrow = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (wrow >= rows) return;
+  const int lane = threadIdx.x & 31;
+  const int r = (int)(wrow % d.Sq);
+  int64_t rest = wrow / d.Sq;
+  const int i = 1 + (int)(rest % t);
+  rest /= t;
+  const int hk = (int)(rest % d.Hkv);
+  const int b = (int)(rest / d.Hkv);
+  const int64_t kr = (int64_t)i * d.Sq + r;
+  const __nv_bfloat16* krow = row_ptr(a.k, b, hk, kr);
+  const __nv_bfloat16* vrow = row_ptr(a.v, b, hk, kr);
+  float kf[EPL], vf[EPL], dk[EPL], dv[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    const int c = lane + 32 * e;
+    kf[e] = c < D ? __bfloat162float(krow[c]) : 0.f;
+    vf[e] = c < D ? __bfloat162float(vrow[c]) : 0.f;
+    dk[e] = 0.f;
+    dv[e] = 0.f;
+  }
+  for (int gq = 0; gq < d.G; ++gq) {
+    const int h = hk * d.G + gq;
+    const __nv_bfloat16* qrow = row_ptr(a.q, b, h, r);
+    const __nv_bfloat16* dorow = row_ptr(a.dout, b, h, r);
+    float qf[EPL], gf[EPL];
+    float s = 0.f, dp = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      const int c = lane + 32 * e;
+      qf[e] = c < D ? __bfloat162float(qrow[c]) : 0.f;
+      gf[e] = c < D ? __bfloat162float(dorow[c]) : 0.f;
+      s = fmaf(qf[e], kf[e], s);
+      dp = fmaf(gf[e], vf[e], dp);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      s += __shfl_xor_sync(0xffffffffu, s, off);
+      dp += __shfl_xor_sync(0xffffffffu, dp, off);
+    }
+    const int64_t rrow = ((int64_t)b * d.Hq + h) * d.Sq + r;
+    const float p = ex2_approx(fmaf(s, d.scale_log2, -a.lse[rrow] * kLog2e));
+    const float ds = p * (dp - a.delta[rrow]);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      dv[e] = fmaf(p, gf[e], dv[e]);
+      dk[e] = fmaf(ds, qf[e], dk[e]);
+    }
+  }
+  __nv_bfloat16* dkrow = row_ptr_w(a.dk, b, hk, kr);
+  __nv_bfloat16* dvrow = row_ptr_w(a.dv, b, hk, kr);
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    const int c = lane + 32 * e;
+    if (c < D) {
+      dkrow[c] = __float2bfloat16_rn(dk[e] * d.scale);
+      dvrow[c] = __float2bfloat16_rn(dv[e]);
+    }
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdArgs& a, const Maps& m, cudaStream_t s) {
+  cudaError_t e;
+  {
+    constexpr int RPB = 256 / (D / 8);
+    const int64_t rows = (int64_t)a.d.B * a.d.Hq * a.d.Sq;
+    bwd_prep_kernel<D><<<(unsigned)((rows + RPB - 1) / RPB), 256, 0, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  {
+    using L = DkdvLayout<D>;
+    auto kern = bwd_dkdv_kernel<D>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC)) !=
+        cudaSuccess)
+      return e;
+    const unsigned grid = (unsigned)(cdiv(a.d.geom.kv_main, kBN) * a.d.B * a.d.Hkv);
+    kern<<<grid, kThreads, L::ALLOC, s>>>(m.q, m.k, m.v, m.dout, a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  {
+    using L = DqLayout<D>;
+    auto kern = bwd_dq_kernel<D>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC)) !=
+        cudaSuccess)
+      return e;
+    const unsigned grid = (unsigned)(cdiv(a.d.Sq, kBM) * a.d.B * a.d.Hq);
+    kern<<<grid, kThreads, L::ALLOC, s>>>(m.q, m.k, m.v, m.dout, a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (a.d.geom.ttt > 0) {
+    const int64_t rows = (int64_t)a.d.B * a.d.Hkv * a.d.geom.ttt * a.d.Sq;
+    ttt_diag_bwd_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdArgs& a, const Maps& m, cudaStream_t s) {
+  switch (a.d.D) {
+    case 16: return launch_bwd_d<16>(a, m, s);
+    case 32: return launch_bwd_d<32>(a, m, s);
+    case 64: return launch_bwd_d<64>(a, m, s);
+    case 128: return launch_bwd_d<128>(a, m, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace attn

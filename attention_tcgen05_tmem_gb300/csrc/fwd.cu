@@ -1,0 +1,444 @@
+// fwd.cu -- fused attention forward on tcgen05 (sm_103a).
+//
+// Computes, per (b, q head), O = softmax(c Q K^T + mask) V and the per-row
+// natural-log LSE, streaming K/V tiles through an online softmax (CS336
+// README, "Flash Attention (Triton)": running max and sum, O rescaled as tiles
+// stream, LSE kept for the backward; SpecForge post, "Flex Attention": empty
+// tiles skipped, full tiles skip the mask test).  The TTT suffix diagonals of
+// the EAGLE3 mask (SpecForge post, "EAGLE3 Training" and "Flex Attention")
+// are merged per row in the epilogue by log-sum-exp, without a dense mask.
+//
+// One CTA owns two 128-row query tiles of one (b, h) and 10 warps:
+//   warps 0-3  softmax for query tile 0 (thread = row = TMEM lane)
+//   warps 4-7  softmax for query tile 1
+//   warp  8    TMA producer: Q0, Q1 once, then K_j, V_j into a slot ring
+//   warp  9    tcgen05 issuer (one thread) and TMEM owner
+// Tensor memory (512 columns x 128 lanes of 32 bit):
+//   [0,128) S0 / P0   [128,256) S1 / P1   [256,256+D) O0   [256+D,256+2D) O1
+// P (bf16, two per column) overwrites the first 64 columns of its S tile and
+// is the A operand of O += P V straight from tensor memory.
+//
+// MMA issue order per key tile j (FA-style ping-pong, so one tile's softmax
+// overlaps the other tile's MMAs):  PV0(j-1), S0(j), PV1(j-1), S1(j).
+// Because tcgen05 MMAs of one thread run in issue order, S_x(j) completing
+// implies PV_x(j-1) completed, which makes the O rescale wait free.
+//
+// The running max is refreshed only when it grows by more than 8 (log2
+// units); otherwise the stale max is kept and P stays <= 256.  O, l and m
+// always share one reference, so the result is exact up to rounding.
+#include <cuda_runtime.h>
+
+#include <cfloat>
+#include <cstdint>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "sched.cuh"
+#include "tile.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kFwdThreads = 320;
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D>
+struct FwdLayout {
+  using TG = TileGeom<D>;
+  static constexpr int NSLOT = (D == 128) ? 4 : (D == 64 ? 6 : 8);
+  static constexpr int Q_OFF = 0;
+  static constexpr int KV_OFF = 2 * TG::TILE_BYTES;
+  static constexpr int BAR_OFF = KV_OFF + NSLOT * TG::TILE_BYTES;
+  // q_full, kv_full[NSLOT], kv_empty[NSLOT], s_full[2], p_ready[2], o_done[2], drain
+  static constexpr int NBAR = 1 + 2 * NSLOT + 7;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int BYTES = MISC_OFF + 16;
+  // at least 116 KB so that only one CTA fits per SM: each holds all 512 TMEM columns
+  static constexpr int ALLOC = (BYTES + 1024 > 116 * 1024) ? BYTES + 1024 : 116 * 1024;
+  static_assert(ALLOC <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  const uint32_t a = smem_u32(p);
+  return p + (((a + 1023u) & ~1023u) - a);
+}
+
+// Wait for a barrier phase with a fixed budget, ignoring the abort flag (used
+// to drain copies and MMAs still in flight before the CTA exits).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > 200000000ull) break;
+  }
+}
+
+__device__ __forceinline__ float neg_inf() { return -INFINITY; }
+
+template <int D>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+               const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
+  using TG = TileGeom<D>;
+  using L = FwdLayout<D>;
+  constexpr int NSLOT = L::NSLOT;
+  extern __shared__ uint8_t smem_raw[];
+
+  if (*reinterpret_cast<volatile uint32_t*>(a.ctl.err) != 0) return;  // sticky device error
+
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = kv_full + NSLOT;
+  uint64_t* s_full = kv_empty + NSLOT;
+  uint64_t* p_ready = s_full + 2;
+  uint64_t* o_done = p_ready + 2;
+  uint64_t* drain = o_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
+
+  const Dims& d = a.d;
+  const MaskGeom g = d.geom;
+  // ---- work decode: causal/TTT launch the longest query-tile pairs first
+  const int n_qp = cdiv(d.Sq, 2 * kBM);
+  const int BH = d.B * d.Hq;
+  int qp, bh;
+  if (g.kind == kMaskFull) {
+    qp = blockIdx.x % n_qp;
+    bh = blockIdx.x / n_qp;
+  } else {
+    qp = n_qp - 1 - (int)(blockIdx.x / BH);
+    bh = blockIdx.x % BH;
+  }
+  const int h = bh % d.Hq;
+  const int b = bh / d.Hq;
+  const int hk = h / d.G;
+  const int q0 = qp * 2 * kBM;
+  const int n_kv = cdiv(kv_end_for_rows(g, q0, 2 * kBM), kBN);
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < NSLOT; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&p_ready[x], 128);
+      mbar_init(&o_done[x], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl ctl{a.ctl.err, abort_flag, a.ctl.budget_ns};
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n_kv > 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      mbar_arrive_expect_tx(q_full, 2 * TG::TILE_BYTES);
+      TG::load(smem + L::Q_OFF, &tq, q_full, q0, h, b);
+      TG::load(smem + L::Q_OFF + TG::TILE_BYTES, &tq, q_full, q0 + kBM, h, b);
+      int issued = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        bool ok = true;
+        for (int w = 0; w < 2; ++w) {
+          const int idx = 2 * j + w;
+          const int s = idx % NSLOT;
+          const uint32_t ph = (uint32_t)(idx / NSLOT) & 1u;
+          if (!mbar_wait(&kv_empty[s], ph ^ 1u, ctl)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&kv_full[s], TG::TILE_BYTES);
+          TG::load(smem + L::KV_OFF + s * TG::TILE_BYTES, w == 0 ? &tk : &tv, &kv_full[s],
+                   j * kBN, hk, b);
+          issued = idx + 1;
+        }
+        if (!ok) break;
+      }
+      if (*abort_flag) {
+        // let every copy in flight land before the CTA can exit
+        drain_wait(q_full, 0);
+        for (int idx = issued - NSLOT < 0 ? 0 : issued - NSLOT; idx < issued; ++idx)
+          drain_wait(&kv_full[idx % NSLOT], (uint32_t)(idx / NSLOT) & 1u);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------- MMA
+    if (lane == 0 && n_kv > 0) {
+      constexpr uint32_t idesc_s = make_idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc_o = make_idesc_bf16(128, D, false, true);
+      const uint32_t sQ = smem_u32(smem + L::Q_OFF);
+      const uint32_t sKV = smem_u32(smem + L::KV_OFF);
+      auto slot_of = [](int idx) { return idx % NSLOT; };
+      auto phase_of = [](int idx) { return (uint32_t)(idx / NSLOT) & 1u; };
+      auto issue_s = [&](int x, int slot) {
+        const uint32_t qa = sQ + x * TG::TILE_BYTES;
+        const uint32_t ka = sKV + slot * TG::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < TG::KSTEPS; ++kk)
+          umma_ss(tmem + x * 128, TG::kmajor(qa, kk), TG::kmajor(ka, kk), idesc_s, kk > 0);
+      };
+      auto issue_pv = [&](int x, int slot, bool acc) {
+        const uint32_t va = sKV + slot * TG::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          umma_ts(tmem + 256 + x * D, tmem + x * 128 + kk * 8, TG::mnmajor(va, kk), idesc_o,
+                  (acc || kk > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(q_full, 0, ctl);
+      if (ok) ok = mbar_wait(&kv_full[slot_of(0)], phase_of(0), ctl);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, slot_of(0));
+        umma_commit(&s_full[0]);
+        issue_s(1, slot_of(0));
+        umma_commit(&s_full[1]);
+        umma_commit(&kv_empty[slot_of(0)]);
+      }
+      for (int j = 1; ok && j < n_kv; ++j) {
+        const int vi = 2 * (j - 1) + 1, ki = 2 * j;
+        ok = mbar_wait(&kv_full[slot_of(vi)], phase_of(vi), ctl) &&
+             mbar_wait(&kv_full[slot_of(ki)], phase_of(ki), ctl) &&
+             mbar_wait(&p_ready[0], (uint32_t)(j - 1) & 1u, ctl);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(0, slot_of(vi), j - 1 > 0);
+        umma_commit(&o_done[0]);
+        issue_s(0, slot_of(ki));
+        umma_commit(&s_full[0]);
+        if (!(ok = mbar_wait(&p_ready[1], (uint32_t)(j - 1) & 1u, ctl))) break;
+        tc_fence_after();
+        issue_pv(1, slot_of(vi), j - 1 > 0);
+        umma_commit(&o_done[1]);
+        umma_commit(&kv_empty[slot_of(vi)]);
+        issue_s(1, slot_of(ki));
+        umma_commit(&s_full[1]);
+        umma_commit(&kv_empty[slot_of(ki)]);
+      }
+      if (ok) {
+        const int vi = 2 * (n_kv - 1) + 1;
+        ok = mbar_wait(&kv_full[slot_of(vi)], phase_of(vi), ctl) &&
+             mbar_wait(&p_ready[0], (uint32_t)(n_kv - 1) & 1u, ctl);
+        if (ok) {
+          tc_fence_after();
+          issue_pv(0, slot_of(vi), n_kv - 1 > 0);
+          umma_commit(&o_done[0]);
+          ok = mbar_wait(&p_ready[1], (uint32_t)(n_kv - 1) & 1u, ctl);
+        }
+        if (ok) {
+          tc_fence_after();
+          issue_pv(1, slot_of(vi), n_kv - 1 > 0);
+          umma_commit(&o_done[1]);
+          umma_commit(&kv_empty[slot_of(vi)]);
+        }
+      }
+      if (!ok) {
+        // every MMA issued so far must finish before tensor memory is freed
+        umma_commit(drain);
+        drain_wait(drain, 0);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- softmax
+    const int x = warp >> 2;    // query tile of this warpgroup
+    const int quad = warp & 3;  // TMEM lane quadrant
+    const int r = quad * 32 + lane;
+    const int qt0 = q0 + x * kBM;
+    const int q = qt0 + r;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_base + x * 128;
+    const uint32_t tO = tmem + lane_base + 256 + x * D;
+    const float sl2 = d.scale_log2;
+
+    float m_run = neg_inf();  // running max of c*log2(e)*s
+    float l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      if (!(ok = mbar_wait_warp(&s_full[x], (uint32_t)j & 1u, ctl))) break;
+      tc_fence_after();
+      uint32_t sr[128];  // S row as raw fp32 bits; columns k0 .. k0+127
+      tmem_ld32x2(tS + 0, tS + 32, *reinterpret_cast<uint32_t(*)[64]>(&sr[0]));
+      tmem_ld32x2(tS + 64, tS + 96, *reinterpret_cast<uint32_t(*)[64]>(&sr[64]));
+
+      const int k0 = j * kBN;
+      if (!tile_is_full(g, qt0, k0)) {
+        const int lim = col_limit(g, q, k0);
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c > lim) sr[c] = __float_as_uint(neg_inf());
+      }
+      float mt = __uint_as_float(sr[0]);
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mt = fmaxf(mt, __uint_as_float(sr[c]));
+      const float m_new = mt * sl2;  // -inf stays -inf (sl2 > 0)
+      const bool need = m_new > m_run + kRescaleThreshold;
+      float alpha = 1.f;
+      if (need) {
+        alpha = (m_run == neg_inf()) ? 0.f : ex2_approx(m_run - m_new);
+        m_run = m_new;
+        l_run *= alpha;
+      }
+      const float mu = (m_run == neg_inf()) ? 0.f : m_run;
+      float rs = 0.f;
+#pragma unroll
+      for (int qtr = 0; qtr < 4; ++qtr) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[qtr * 32 + 2 * c]), sl2, -mu));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[qtr * 32 + 2 * c + 1]), sl2, -mu));
+          rs += p0 + p1;
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tS + qtr * 16, pk);
+      }
+      l_run += rs;
+      if (j > 0) {
+        // PV(j-1) finished before S(j) (in-order MMA); consume its phase
+        if (!(ok = mbar_wait_warp(&o_done[x], (uint32_t)(j - 1) & 1u, ctl))) break;
+        if (__any_sync(0xffffffffu, need)) {
+          tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 16) {
+            uint32_t ov[16];
+            tmem_ld16(tO + c0, ov);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+            tmem_st16(tO + c0, ov);
+          }
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&p_ready[x]);
+    }
+
+    // ------------------------------------------------------------ epilogue
+    if (ok && n_kv > 0) ok = mbar_wait_warp(&o_done[x], (uint32_t)(n_kv - 1) & 1u, ctl);
+    if (ok) {
+      float o[D];
+      if (n_kv > 0) {
+        tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 16) {
+          uint32_t ov[16];
+          tmem_ld16(tO + c0, ov);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) o[c0 + c] = __uint_as_float(ov[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < D; ++c) o[c] = 0.f;
+      }
+      if (q < d.Sq) {
+        // TTT suffix diagonals: key/value row i*Sq + q of each appended segment
+        if (g.ttt > 0) {
+          const __nv_bfloat16* qrow = reinterpret_cast<const __nv_bfloat16*>(a.q.ptr) +
+                                      b * a.q.sb + h * a.q.sh + (int64_t)q * a.q.ss;
+          for (int i = 1; i <= g.ttt; ++i) {
+            const int64_t kr = (int64_t)i * d.Sq + q;
+            const __nv_bfloat16* krow = reinterpret_cast<const __nv_bfloat16*>(a.k.ptr) +
+                                        b * a.k.sb + hk * a.k.sh + kr * a.k.ss;
+            const __nv_bfloat16* vrow = reinterpret_cast<const __nv_bfloat16*>(a.v.ptr) +
+                                        b * a.v.sb + hk * a.v.sh + kr * a.v.ss;
+            float dot = 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 8) {
+              const uint4 qa = *reinterpret_cast<const uint4*>(qrow + c0);
+              const uint4 ka = *reinterpret_cast<const uint4*>(krow + c0);
+              const __nv_bfloat162* qv = reinterpret_cast<const __nv_bfloat162*>(&qa);
+              const __nv_bfloat162* kv = reinterpret_cast<const __nv_bfloat162*>(&ka);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 qf = __bfloat1622float2(qv[e]);
+                const float2 kf = __bfloat1622float2(kv[e]);
+                dot = fmaf(qf.x, kf.x, dot);
+                dot = fmaf(qf.y, kf.y, dot);
+              }
+            }
+            const float xs = dot * sl2;
+            const float m_new = fmaxf(m_run, xs);
+            const float al = (m_run == neg_inf()) ? 0.f : ex2_approx(m_run - m_new);
+            const float w = ex2_approx(xs - m_new);
+            l_run = l_run * al + w;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 8) {
+              const uint4 va = *reinterpret_cast<const uint4*>(vrow + c0);
+              const __nv_bfloat162* vv = reinterpret_cast<const __nv_bfloat162*>(&va);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 vf = __bfloat1622float2(vv[e]);
+                o[c0 + 2 * e] = fmaf(o[c0 + 2 * e], al, w * vf.x);
+                o[c0 + 2 * e + 1] = fmaf(o[c0 + 2 * e + 1], al, w * vf.y);
+              }
+            }
+            m_run = m_new;
+          }
+        }
+        const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o.ptr) + b * a.o.sb +
+                              h * a.o.sh + (int64_t)q * a.o.ss;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 8) {
+          uint4 pkt;
+          pkt.x = pack_bf16x2(o[c0 + 0] * inv, o[c0 + 1] * inv);
+          pkt.y = pack_bf16x2(o[c0 + 2] * inv, o[c0 + 3] * inv);
+          pkt.z = pack_bf16x2(o[c0 + 4] * inv, o[c0 + 5] * inv);
+          pkt.w = pack_bf16x2(o[c0 + 6] * inv, o[c0 + 7] * inv);
+          *reinterpret_cast<uint4*>(orow + c0) = pkt;
+        }
+        const float lse = (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * 0.69314718055994531f : 0.f;
+        a.lse[((int64_t)b * d.Hq + h) * d.Sq + q] = lse;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdArgs& a, const Maps& m, cudaStream_t s) {
+  using L = FwdLayout<D>;
+  auto kern = fwd_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+  if (e != cudaSuccess) return e;
+  const int n_qp = cdiv(a.d.Sq, 2 * kBM);
+  const unsigned grid = (unsigned)(n_qp * a.d.B * a.d.Hq);
+  kern<<<grid, kFwdThreads, L::ALLOC, s>>>(m.q, m.k, m.v, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdArgs& a, const Maps& m, cudaStream_t s) {
+  switch (a.d.D) {
+    case 16: return launch_fwd_d<16>(a, m, s);
+    case 32: return launch_fwd_d<32>(a, m, s);
+    case 64: return launch_fwd_d<64>(a, m, s);
+    case 128: return launch_fwd_d<128>(a, m, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace attn

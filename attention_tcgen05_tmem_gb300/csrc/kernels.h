@@ -1,0 +1,60 @@
+// kernels.h -- internal interface between the C ABI (api.cu) and the kernel
+// translation units.  Not installed; the public interface is
+// include/attn_train.h.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "sched.cuh"
+
+namespace attn {
+
+// A [B, H, S, D] bf16 view; strides in elements, D stride 1.
+struct View {
+  void* ptr;
+  int64_t sb, sh, ss;
+};
+
+struct Dims {
+  int B, Hq, Hkv, Sq, Skv, D, G;
+  MaskGeom geom;
+  float scale;       // softmax scale c
+  float scale_log2;  // c * log2(e)
+};
+
+struct Ctl {
+  uint32_t* err;       // device error word
+  uint64_t budget_ns;  // per-wait budget
+};
+
+struct FwdArgs {
+  Dims d;
+  View q, k, v, o;
+  float* lse;  // [B, Hq, Sq]
+  Ctl ctl;
+};
+
+struct BwdArgs {
+  Dims d;
+  View q, k, v, o, dout, dq, dk, dv;
+  const float* lse;  // [B, Hq, Sq]
+  float* delta;      // workspace [B, Hq, Sq]
+  Ctl ctl;
+};
+
+struct Maps {
+  CUtensorMap q, k, v, dout;
+};
+
+cudaError_t launch_fwd(const FwdArgs& a, const Maps& m, cudaStream_t s);
+cudaError_t launch_bwd(const BwdArgs& a, const Maps& m, cudaStream_t s);
+cudaError_t launch_mask_pattern(const Dims& d, uint8_t* bits, uint8_t* tiles, cudaStream_t s);
+// One-tile descriptor probe (test only).  mode 0: C[128x128] = A[128xD] B[128xD]^T with
+// both operands K-major in shared memory; mode 1: C[128xD] = A[128x128] B[128xD] with A in
+// tensor memory and B MN-major in shared memory.
+cudaError_t launch_probe(int mode, int D, const CUtensorMap& ta, const CUtensorMap& tb,
+                         const void* a_global, float* c, Ctl ctl, cudaStream_t s);
+cudaError_t launch_selftest_wait(Ctl ctl, cudaStream_t s);
+
+}  // namespace attn

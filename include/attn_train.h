@@ -1,0 +1,165 @@
+/*
+ * attn_train.h -- C ABI of the GB300 (sm_103a) fused training-attention
+ * library: forward (O and LSE) and a deterministic backward (dQ, dK, dV)
+ * for full, causal and EAGLE3 Training-Time-Test masks, with GQA.
+ *
+ * What the operations compute
+ * ---------------------------
+ * Forward (SpecForge long-context post, "EAGLE3 Training": attention(Q,K,V)
+ * = softmax(Q K^T / sqrt(d_k)) V; CS336 README, "Flash Attention (Triton)":
+ * the forward also keeps the per-row logsumexp L):
+ *     S = scale * Q K^T (+ mask: invisible pairs are -inf)
+ *     LSE[q] = ln sum_kv exp(S[q,kv]),  O = exp(S - LSE) V
+ * Backward (HOT-Step flash-attn-training, section 1: the fused backward
+ * emits dQ|dK|dV; CS336 README: P is recomputed from L):
+ *     P = exp(S - LSE), dV = P^T dO, dP = dO V^T, Delta = rowsum(dO * O),
+ *     dS = P * (dP - Delta), dQ = scale dS K, dK = scale dS^T Q.
+ * GQA: q head h reads kv head h / (Hq / Hkv); dK and dV of a kv head are the
+ * sum over its q heads, accumulated in ascending head order.
+ * A query row that sees no key gets O = 0 and LSE = 0 (HOT-Step section 6,
+ * trap 9); none of the three masks produces such a row for a valid problem.
+ *
+ * Masks (SpecForge post, "Flex Attention", eagle3 mask_mod):
+ *   ATTN_MASK_FULL    every key visible (self- or cross-attention, Skv != Sq ok)
+ *   ATTN_MASK_CAUSAL  key kv visible to query q iff kv <= q (top-left aligned)
+ *   ATTN_MASK_TTT     TTT step t = ttt_step with Skv == (t+1)*Sq: K/V hold t+1
+ *                     segments of Sq rows; query q sees segment-0 keys
+ *                     kv <= q - t (the causal part shrinks one diagonal per
+ *                     appended segment) plus key i*Sq + q of each appended
+ *                     segment i = 1..t (one diagonal entry each).
+ *
+ * Layout and types
+ * ----------------
+ * Every Q/K/V/O/dO/dQ/dK/dV tensor is bf16 [B, H, S, D] with D contiguous
+ * (stride 1) and arbitrary element strides for B, H and S (so BHSD and BSHD
+ * both work).  Pointers must be 16-byte aligned and every stride times 2 bytes
+ * a multiple of 16.  D is 16, 32, 64 or 128.  LSE is fp32 contiguous
+ * [B, Hq, Sq].  Arithmetic: bf16 MMA operands, fp32 accumulation and softmax.
+ *
+ * Ownership and streams
+ * ---------------------
+ * All tensor pointers are device pointers owned by the caller; the library
+ * allocates no device memory and keeps no state between calls besides a
+ * device error word and cached driver entry points.  Work is enqueued on the
+ * caller's stream (a cudaStream_t passed as void*, NULL = legacy default) and
+ * the calls return before it finishes.  Outputs are overwritten, not
+ * accumulated; summing gradients over TTT steps is the caller's job.
+ *
+ * Errors
+ * ------
+ * Every entry point validates its arguments on the host before it enqueues
+ * anything and returns a status; there is no fallback path.  The message for
+ * the last non-OK status of the calling thread is attn_train_last_error().
+ * Device-side pipeline waits are bounded: a wait that runs out records an
+ * error in a device word and the kernel returns; attn_train_device_status()
+ * synchronizes the stream, reads and clears that word.  While the word is set,
+ * further kernels of this library return without doing work.
+ */
+#ifndef ATTN_TRAIN_H
+#define ATTN_TRAIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_MASK_FULL = 0,
+  ATTN_MASK_CAUSAL = 1,
+  ATTN_MASK_TTT = 2
+} attn_mask_kind;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID = 1,        /* malformed arguments (null pointer, bad size) */
+  ATTN_ERR_UNSUPPORTED = 2,    /* well-formed but not supported (head dim, mask) */
+  ATTN_ERR_ALIGNMENT = 3,      /* pointer or stride breaks the 16-byte rule */
+  ATTN_ERR_WORKSPACE = 4,      /* workspace missing or too small */
+  ATTN_ERR_CUDA = 5,           /* a CUDA runtime/driver call failed */
+  ATTN_ERR_DEVICE_TIMEOUT = 6  /* a device-side wait ran out of budget */
+} attn_status;
+
+/* A bf16 [B, H, S, D] tensor view: D has stride 1, the other strides are in
+ * elements. */
+typedef struct {
+  const void* ptr;
+  int64_t stride_b, stride_h, stride_s;
+} attn_tensor;
+
+/* Problem shape.  mask is an attn_mask_kind; ttt_step is t for ATTN_MASK_TTT
+ * (ignored otherwise); scale <= 0 selects 1/sqrt(D). */
+typedef struct {
+  int B, Hq, Hkv, Sq, Skv, D;
+  int mask;
+  int ttt_step;
+  float scale;
+} attn_problem;
+
+/* Whether the problem is supported.  Pure host check, no side effects.
+ * Requires B, Hq, Hkv, Sq, Skv > 0, Hq % Hkv == 0, D in {16, 32, 64, 128},
+ * a known mask, ttt_step >= 0 and Skv == (ttt_step + 1) * Sq for TTT. */
+attn_status attn_train_supports(const attn_problem* p);
+
+/* Bytes of device workspace attn_train_bwd needs: the fp32 Delta row
+ * statistic, B * Hq * Sq * 4 bytes rounded up to 256. */
+attn_status attn_train_workspace_size(const attn_problem* p, size_t* bytes);
+
+/* Forward.  Inputs q [B,Hq,Sq,D], k and v [B,Hkv,Skv,D]; outputs o
+ * [B,Hq,Sq,D] (bf16) and lse [B,Hq,Sq] (fp32, natural log).  Kernels: one
+ * tcgen05 kernel (two 128-row query tiles per CTA). */
+attn_status attn_train_fwd(const attn_problem* p, attn_tensor q, attn_tensor k, attn_tensor v,
+                           attn_tensor o, float* lse, void* stream);
+
+/* Backward.  Inputs q, k, v, o (the forward's output), dout [B,Hq,Sq,D] and
+ * lse (the forward's); outputs dq [B,Hq,Sq,D], dk and dv [B,Hkv,Skv,D],
+ * overwritten.  workspace: device buffer of at least attn_train_workspace_size
+ * bytes, 256-byte aligned, contents ignored.  Fixed schedule, no atomics: the
+ * result is bitwise identical across runs.  Kernels: Delta prep, dK/dV pass,
+ * dQ pass, and for TTT the suffix-diagonal pass. */
+attn_status attn_train_bwd(const attn_problem* p, attn_tensor q, attn_tensor k, attn_tensor v,
+                           attn_tensor o, attn_tensor dout, const float* lse, attn_tensor dq,
+                           attn_tensor dk, attn_tensor dv, void* workspace, size_t ws_bytes,
+                           void* stream);
+
+/* Message for the calling thread's last non-OK status ("" if none). */
+const char* attn_train_last_error(void);
+
+/* Synchronizes `stream`, then reads and clears the device error word of the
+ * current device.  Returns ATTN_ERR_DEVICE_TIMEOUT if a kernel recorded a wait
+ * that ran out of budget since the last call. */
+attn_status attn_train_device_status(void* stream);
+
+/* Per-wait budget of the device-side pipeline waits, in nanoseconds (default
+ * 2e9).  Host-side setting for kernels launched afterwards by this thread's
+ * process; values < 1e6 are raised to 1e6. */
+attn_status attn_train_set_wait_budget_ns(uint64_t ns);
+
+/* ---- test-only entry points ------------------------------------------- */
+
+/* Device evaluation of the mask as the kernels schedule it.  bits: device
+ * buffer of 2 * Sq * Skv bytes; plane 0 = pairs the forward/dQ row schedule
+ * visits unmasked, plane 1 = pairs the dK/dV column schedule keeps, TTT
+ * suffix diagonals included.  tiles (may be NULL): ceil(Sq/128) x
+ * ceil(kv_main/128) tile classes (0 empty, 1 partial, 2 full) of the tiled
+ * part, kv_main = Sq for TTT else Skv.  Must equal the visibility predicate. */
+attn_status attn_train_mask_pattern(const attn_problem* p, uint8_t* bits, uint8_t* tiles,
+                                    void* stream);
+
+/* One-tile tcgen05 descriptor probe.  mode 0: c[128][128] = a[128][D] b[128][D]^T
+ * (both operands K-major in shared memory); mode 1: c[128][D] = a[128][128]
+ * b[128][D] (a in tensor memory, b MN-major in shared memory).  a, b: device
+ * bf16 row-major; c: device fp32. */
+attn_status attn_train_probe_mma(int mode, int D, const void* a, const void* b, float* c,
+                                 void* stream);
+
+/* Launches a kernel whose bounded wait can never be satisfied, with a 50 ms
+ * budget; attn_train_device_status() must then return ATTN_ERR_DEVICE_TIMEOUT. */
+attn_status attn_train_selftest_wait_timeout(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_TRAIN_H */
