@@ -22,7 +22,7 @@ STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID", 2: "ATTN_ERR_UNSUPPORTED", 3: "AT
 
 # Entry points of include/attn_train.h (checked against the header by the tests).
 EXPORTS = ("attn_train_supports", "attn_train_workspace_size", "attn_train_fwd", "attn_train_bwd",
-           "attn_train_last_error", "attn_train_device_status", "attn_train_set_wait_budget_ns",
+           "attn_train_bwd_passes", "attn_train_last_error", "attn_train_device_status", "attn_train_set_wait_budget_ns",
            "attn_train_mask_pattern", "attn_train_probe_mma", "attn_train_selftest_wait_timeout")
 
 
@@ -40,7 +40,11 @@ class Tensor(ctypes.Structure):
 class Problem(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
                 ("Sq", ctypes.c_int), ("Skv", ctypes.c_int), ("D", ctypes.c_int),
-                ("mask", ctypes.c_int), ("ttt_step", ctypes.c_int), ("scale", ctypes.c_float)]
+                ("mask", ctypes.c_int), ("ttt_step", ctypes.c_int), ("scale", ctypes.c_float),
+                ("out_dtype", ctypes.c_int)]
+
+
+OUT_DTYPES = {"bf16": 0, "fp32": 1}
 
 
 _lib = None
@@ -66,6 +70,8 @@ def load(path: str = LIB_PATH):
             "attn_train_workspace_size": (st, [P, ctypes.POINTER(ctypes.c_size_t)]),
             "attn_train_fwd": (st, [P, T, T, T, T, vp, vp]),
             "attn_train_bwd": (st, [P, T, T, T, T, T, vp, T, T, T, vp, ctypes.c_size_t, vp]),
+            "attn_train_bwd_passes": (st, [P, ctypes.c_uint, T, T, T, T, T, vp, T, T, T, vp,
+                                           ctypes.c_size_t, vp]),
             "attn_train_last_error": (ctypes.c_char_p, []),
             "attn_train_device_status": (st, [vp]),
             "attn_train_set_wait_budget_ns": (st, [ctypes.c_uint64]),
@@ -87,15 +93,20 @@ def _check(status: int):
         raise AttnError(status, msg)
 
 
-def problem(B, Hq, Hkv, Sq, Skv, D, mask="causal", ttt_step=0, scale=0.0) -> Problem:
+def problem(B, Hq, Hkv, Sq, Skv, D, mask="causal", ttt_step=0, scale=0.0, out="bf16") -> Problem:
     m = MASKS[mask] if isinstance(mask, str) else int(mask)
-    return Problem(B, Hq, Hkv, Sq, Skv, D, m, ttt_step, float(scale))
+    return Problem(B, Hq, Hkv, Sq, Skv, D, m, ttt_step, float(scale), OUT_DTYPES[out])
 
 
-def problem_for(q, k, mask="causal", ttt_step=0, scale=None) -> Problem:
+def problem_for(q, k, mask="causal", ttt_step=0, scale=None, out="bf16") -> Problem:
     B, Hq, Sq, D = q.shape
     _, Hkv, Skv, _ = k.shape
-    return problem(B, Hq, Hkv, Sq, Skv, D, mask, ttt_step, 0.0 if scale is None else scale)
+    return problem(B, Hq, Hkv, Sq, Skv, D, mask, ttt_step, 0.0 if scale is None else scale, out)
+
+
+def _torch_out_dtype(out):
+    import torch
+    return torch.float32 if out == "fp32" else torch.bfloat16
 
 
 def view(t) -> Tensor:
@@ -142,6 +153,19 @@ def bwd_raw(p: Problem, q, k, v, o, dout, lse, dq, dk, dv, workspace, stream=Non
                                  _stream(stream)))
 
 
+BWD_PREP, BWD_DKDV, BWD_DQ, BWD_TTT, BWD_ALL = 1, 2, 4, 8, 15
+
+
+def bwd_passes_raw(p: Problem, passes: int, q, k, v, o, dout, lse, dq, dk, dv, workspace,
+                   stream=None):
+    """attn_train_bwd_passes: enqueue only the backward passes in `passes`."""
+    _check(load().attn_train_bwd_passes(ctypes.byref(p), passes, view(q), view(k), view(v),
+                                        view(o), view(dout), ctypes.c_void_p(lse.data_ptr()),
+                                        view(dq), view(dk), view(dv),
+                                        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                                        _stream(stream)))
+
+
 def device_status(stream=None):
     _check(load().attn_train_device_status(_stream(stream)))
 
@@ -151,23 +175,26 @@ def set_wait_budget_ns(ns: int):
 
 
 # ------------------------------------------------------------ conveniences
-def fwd(q, k, v, mask="causal", ttt_step=0, scale=None, stream=None):
-    """Allocates O and LSE with torch, runs the forward; returns (o, lse)."""
+def fwd(q, k, v, mask="causal", ttt_step=0, scale=None, stream=None, out="bf16"):
+    """Allocates O (bf16 or fp32) and LSE with torch, runs the forward;
+    returns (o, lse)."""
     import torch
-    p = problem_for(q, k, mask, ttt_step, scale)
-    o = torch.empty_like(q)
+    p = problem_for(q, k, mask, ttt_step, scale, out)
+    o = torch.empty(q.shape, dtype=_torch_out_dtype(out), device=q.device)
     lse = torch.empty(q.shape[0], q.shape[1], q.shape[2], dtype=torch.float32, device=q.device)
     fwd_raw(p, q, k, v, o, lse, stream)
     return o, lse
 
 
 def bwd(q, k, v, o, lse, dout, mask="causal", ttt_step=0, scale=None, stream=None, workspace=None):
-    """Allocates dQ, dK, dV (and workspace unless given); returns (dq, dk, dv)."""
+    """Allocates dQ, dK, dV (same dtype as o: bf16 or fp32) and the workspace
+    unless given; returns (dq, dk, dv)."""
     import torch
-    p = problem_for(q, k, mask, ttt_step, scale)
-    dq = torch.empty_like(q)
-    dk = torch.empty_like(k)
-    dv = torch.empty_like(v)
+    out = "fp32" if o.dtype == torch.float32 else "bf16"
+    p = problem_for(q, k, mask, ttt_step, scale, out)
+    dq = torch.empty(q.shape, dtype=o.dtype, device=q.device)
+    dk = torch.empty(k.shape, dtype=o.dtype, device=q.device)
+    dv = torch.empty(v.shape, dtype=o.dtype, device=q.device)
     if workspace is None:
         workspace = torch.empty(workspace_size(p), dtype=torch.uint8, device=q.device)
     bwd_raw(p, q, k, v, o, dout, lse, dq, dk, dv, workspace, stream)

@@ -126,6 +126,8 @@ attn_status check_problem(const attn_problem* p) {
                   p->ttt_step, (long long)(p->ttt_step + 1) * p->Sq, p->Skv);
   }
   if (!std::isfinite(p->scale)) return fail(ATTN_ERR_INVALID, "scale is not finite");
+  if (p->out_dtype != ATTN_OUT_BF16 && p->out_dtype != ATTN_OUT_F32)
+    return fail(ATTN_ERR_UNSUPPORTED, "unknown out_dtype %d", p->out_dtype);
   const int64_t grid_q = (int64_t)((p->Sq + 127) / 128) * p->B * p->Hq;
   const int64_t grid_k = (int64_t)((p->Skv + 127) / 128) * p->B * p->Hkv;
   if (grid_q > 0x7fffffffLL || grid_k > 0x7fffffffLL)
@@ -133,7 +135,9 @@ attn_status check_problem(const attn_problem* p) {
   return ATTN_OK;
 }
 
-attn_status check_tensor(const attn_tensor& t, int B, int H, int S, int D, const char* name) {
+// esize: element size in bytes (2 for bf16 inputs and bf16 outputs, 4 for fp32 outputs)
+attn_status check_tensor(const attn_tensor& t, int B, int H, int S, int D, const char* name,
+                         int esize = 2) {
   if (t.ptr == nullptr) return fail(ATTN_ERR_INVALID, "%s is NULL", name);
   if (reinterpret_cast<uintptr_t>(t.ptr) % 16 != 0)
     return fail(ATTN_ERR_ALIGNMENT, "%s pointer is not 16-byte aligned", name);
@@ -143,9 +147,10 @@ attn_status check_tensor(const attn_tensor& t, int B, int H, int S, int D, const
   for (int i = 0; i < 3; ++i) {
     if (sizes[i] == 1 && i < 2) continue;  // stride of a size-1 dim is never used
     if (strides[i] <= 0) return fail(ATTN_ERR_INVALID, "%s.%s must be positive", name, names[i]);
-    if ((strides[i] * 2) % 16 != 0)
-      return fail(ATTN_ERR_ALIGNMENT, "%s.%s * 2 bytes is not a multiple of 16", name, names[i]);
-    if (strides[i] * 2 >= (int64_t)1 << 40)
+    if ((strides[i] * esize) % 16 != 0)
+      return fail(ATTN_ERR_ALIGNMENT, "%s.%s * %d bytes is not a multiple of 16", name, names[i],
+                  esize);
+    if (strides[i] * esize >= (int64_t)1 << 40)
       return fail(ATTN_ERR_UNSUPPORTED, "%s.%s too large", name, names[i]);
   }
   if (t.stride_s < D) return fail(ATTN_ERR_INVALID, "%s rows overlap (stride_s < D)", name);
@@ -164,6 +169,7 @@ Dims make_dims(const attn_problem* p) {
   d.geom = attn::make_geom(p->mask, p->mask == ATTN_MASK_TTT ? p->ttt_step : 0, p->Sq, p->Skv);
   d.scale = p->scale > 0.f ? p->scale : 1.0f / std::sqrt((float)p->D);
   d.scale_log2 = d.scale * 1.4426950408889634f;
+  d.out_f32 = p->out_dtype == ATTN_OUT_F32 ? 1 : 0;
   return d;
 }
 
@@ -206,7 +212,8 @@ attn_status attn_train_fwd(const attn_problem* p, attn_tensor q, attn_tensor k, 
   if ((st = check_tensor(q, p->B, p->Hq, p->Sq, p->D, "q")) != ATTN_OK) return st;
   if ((st = check_tensor(k, p->B, p->Hkv, p->Skv, p->D, "k")) != ATTN_OK) return st;
   if ((st = check_tensor(v, p->B, p->Hkv, p->Skv, p->D, "v")) != ATTN_OK) return st;
-  if ((st = check_tensor(o, p->B, p->Hq, p->Sq, p->D, "o")) != ATTN_OK) return st;
+  const int oes = p->out_dtype == ATTN_OUT_F32 ? 4 : 2;
+  if ((st = check_tensor(o, p->B, p->Hq, p->Sq, p->D, "o", oes)) != ATTN_OK) return st;
   if (lse == nullptr) return fail(ATTN_ERR_INVALID, "lse is NULL");
   if (reinterpret_cast<uintptr_t>(lse) % 4 != 0)
     return fail(ATTN_ERR_ALIGNMENT, "lse is not 4-byte aligned");
@@ -234,16 +241,27 @@ attn_status attn_train_bwd(const attn_problem* p, attn_tensor q, attn_tensor k, 
                            attn_tensor o, attn_tensor dout, const float* lse, attn_tensor dq,
                            attn_tensor dk, attn_tensor dv, void* workspace, size_t ws_bytes,
                            void* stream) {
+  return attn_train_bwd_passes(p, ATTN_BWD_ALL, q, k, v, o, dout, lse, dq, dk, dv, workspace,
+                               ws_bytes, stream);
+}
+
+attn_status attn_train_bwd_passes(const attn_problem* p, unsigned passes, attn_tensor q,
+                                  attn_tensor k, attn_tensor v, attn_tensor o, attn_tensor dout,
+                                  const float* lse, attn_tensor dq, attn_tensor dk, attn_tensor dv,
+                                  void* workspace, size_t ws_bytes, void* stream) {
   attn_status st = check_problem(p);
   if (st != ATTN_OK) return st;
+  if (passes == 0 || (passes & ~(unsigned)ATTN_BWD_ALL) != 0)
+    return fail(ATTN_ERR_INVALID, "passes mask 0x%x is empty or has unknown bits", passes);
   if ((st = check_tensor(q, p->B, p->Hq, p->Sq, p->D, "q")) != ATTN_OK) return st;
   if ((st = check_tensor(k, p->B, p->Hkv, p->Skv, p->D, "k")) != ATTN_OK) return st;
   if ((st = check_tensor(v, p->B, p->Hkv, p->Skv, p->D, "v")) != ATTN_OK) return st;
-  if ((st = check_tensor(o, p->B, p->Hq, p->Sq, p->D, "o")) != ATTN_OK) return st;
+  const int oes = p->out_dtype == ATTN_OUT_F32 ? 4 : 2;
+  if ((st = check_tensor(o, p->B, p->Hq, p->Sq, p->D, "o", oes)) != ATTN_OK) return st;
   if ((st = check_tensor(dout, p->B, p->Hq, p->Sq, p->D, "dout")) != ATTN_OK) return st;
-  if ((st = check_tensor(dq, p->B, p->Hq, p->Sq, p->D, "dq")) != ATTN_OK) return st;
-  if ((st = check_tensor(dk, p->B, p->Hkv, p->Skv, p->D, "dk")) != ATTN_OK) return st;
-  if ((st = check_tensor(dv, p->B, p->Hkv, p->Skv, p->D, "dv")) != ATTN_OK) return st;
+  if ((st = check_tensor(dq, p->B, p->Hq, p->Sq, p->D, "dq", oes)) != ATTN_OK) return st;
+  if ((st = check_tensor(dk, p->B, p->Hkv, p->Skv, p->D, "dk", oes)) != ATTN_OK) return st;
+  if ((st = check_tensor(dv, p->B, p->Hkv, p->Skv, p->D, "dv", oes)) != ATTN_OK) return st;
   if (lse == nullptr) return fail(ATTN_ERR_INVALID, "lse is NULL");
   if (reinterpret_cast<uintptr_t>(lse) % 4 != 0)
     return fail(ATTN_ERR_ALIGNMENT, "lse is not 4-byte aligned");
@@ -273,7 +291,7 @@ attn_status attn_train_bwd(const attn_problem* p, attn_tensor q, attn_tensor k, 
   if ((st = make_map(&m.k, a.k, p->B, p->Hkv, p->Skv, p->D, "k")) != ATTN_OK) return st;
   if ((st = make_map(&m.v, a.v, p->B, p->Hkv, p->Skv, p->D, "v")) != ATTN_OK) return st;
   if ((st = make_map(&m.dout, a.dout, p->B, p->Hq, p->Sq, p->D, "dout")) != ATTN_OK) return st;
-  cudaError_t e = attn::launch_bwd(a, m, static_cast<cudaStream_t>(stream));
+  cudaError_t e = attn::launch_bwd(a, m, passes, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   return ATTN_OK;
 }

@@ -80,16 +80,28 @@ __device__ __forceinline__ float dot_rows(const __nv_bfloat16* x, const __nv_bfl
   return acc;
 }
 
-// Store 16 fp32 values (times mul) as bf16 at row + c0.
-__device__ __forceinline__ void store16_bf16(__nv_bfloat16* row, const float* v, float mul) {
+// Store 16 fp32 values (times mul) at columns c0 .. c0+15 of an output row,
+// as fp32 or bf16.
+__device__ __forceinline__ void store16(const View& v, int b, int h, int64_t s, int c0,
+                                        const float* x, float mul, bool f32) {
+  const int64_t off = b * v.sb + h * v.sh + s * v.ss + c0;
+  if (f32) {
+    float* row = reinterpret_cast<float*>(v.ptr) + off;
 #pragma unroll
-  for (int e = 0; e < 16; e += 8) {
-    uint4 pkt;
-    pkt.x = pack_bf16x2(v[e + 0] * mul, v[e + 1] * mul);
-    pkt.y = pack_bf16x2(v[e + 2] * mul, v[e + 3] * mul);
-    pkt.z = pack_bf16x2(v[e + 4] * mul, v[e + 5] * mul);
-    pkt.w = pack_bf16x2(v[e + 6] * mul, v[e + 7] * mul);
-    *reinterpret_cast<uint4*>(row + e) = pkt;
+    for (int e = 0; e < 16; e += 4)
+      *reinterpret_cast<float4*>(row + e) =
+          make_float4(x[e] * mul, x[e + 1] * mul, x[e + 2] * mul, x[e + 3] * mul);
+  } else {
+    __nv_bfloat16* row = reinterpret_cast<__nv_bfloat16*>(v.ptr) + off;
+#pragma unroll
+    for (int e = 0; e < 16; e += 8) {
+      uint4 pkt;
+      pkt.x = pack_bf16x2(x[e + 0] * mul, x[e + 1] * mul);
+      pkt.y = pack_bf16x2(x[e + 2] * mul, x[e + 3] * mul);
+      pkt.z = pack_bf16x2(x[e + 4] * mul, x[e + 5] * mul);
+      pkt.w = pack_bf16x2(x[e + 6] * mul, x[e + 7] * mul);
+      *reinterpret_cast<uint4*>(row + e) = pkt;
+    }
   }
 }
 
@@ -107,18 +119,32 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdArgs a) {
     const int q = (int)(row % a.d.Sq);
     const int bh = (int)(row / a.d.Sq);
     const int h = bh % a.d.Hq, b = bh / a.d.Hq;
-    const __nv_bfloat16* o = row_ptr(a.o, b, h, q) + sub * 8;
     const __nv_bfloat16* g = row_ptr(a.dout, b, h, q) + sub * 8;
-    const uint4 oa = *reinterpret_cast<const uint4*>(o);
     const uint4 ga = *reinterpret_cast<const uint4*>(g);
-    const __nv_bfloat162* ov = reinterpret_cast<const __nv_bfloat162*>(&oa);
     const __nv_bfloat162* gv = reinterpret_cast<const __nv_bfloat162*>(&ga);
+    float of[8];
+    if (a.d.out_f32) {
+      const float* o = reinterpret_cast<const float*>(a.o.ptr) + b * a.o.sb + h * a.o.sh +
+                       (int64_t)q * a.o.ss + sub * 8;
+      const float4 o0 = *reinterpret_cast<const float4*>(o);
+      const float4 o1 = *reinterpret_cast<const float4*>(o + 4);
+      of[0] = o0.x; of[1] = o0.y; of[2] = o0.z; of[3] = o0.w;
+      of[4] = o1.x; of[5] = o1.y; of[6] = o1.z; of[7] = o1.w;
+    } else {
+      const uint4 oa = *reinterpret_cast<const uint4*>(row_ptr(a.o, b, h, q) + sub * 8);
+      const __nv_bfloat162* ov = reinterpret_cast<const __nv_bfloat162*>(&oa);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(ov[e]);
+        of[2 * e] = f.x;
+        of[2 * e + 1] = f.y;
+      }
+    }
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float2 of = __bfloat1622float2(ov[e]);
       const float2 gf = __bfloat1622float2(gv[e]);
-      acc = fmaf(of.x, gf.x, acc);
-      acc = fmaf(of.y, gf.y, acc);
+      acc = fmaf(of[2 * e], gf.x, acc);
+      acc = fmaf(of[2 * e + 1], gf.y, acc);
     }
   }
 #pragma unroll
@@ -387,8 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && N > 0) ok = mbar_wait_warp(done, 0, ctl);
     if (ok) {
       const bool store = kv < g.kv_main;
-      __nv_bfloat16* dvrow = row_ptr_w(a.dv, b, hk, kv);
-      __nv_bfloat16* dkrow = row_ptr_w(a.dk, b, hk, kv);
+      const bool f32 = d.out_f32 != 0;
       if (N > 0) tc_fence_after();
       for (int c0 = 16 * wg; c0 < D; c0 += 32) {
         float vals[16];
@@ -401,13 +426,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e) vals[e] = 0.f;
         }
-        if (store) store16_bf16(dvrow + c0, vals, 1.f);
+        if (store) store16(a.dv, b, hk, kv, c0, vals, 1.f, f32);
         if (N > 0) {
           tmem_ld16(tmem + lane_base + 256 + D + c0, raw);
 #pragma unroll
           for (int e = 0; e < 16; ++e) vals[e] = __uint_as_float(raw[e]);
         }
-        if (store) store16_bf16(dkrow + c0, vals, d.scale);
+        if (store) store16(a.dk, b, hk, kv, c0, vals, d.scale, f32);
       }
     }
   }
@@ -688,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (qin) store16_bf16(row_ptr_w(a.dq, b, h, q) + c0, acc, d.scale);
+        if (qin) store16(a.dq, b, h, q, c0, acc, d.scale, d.out_f32 != 0);
       }
     }
   }
@@ -760,28 +785,33 @@ __global__ void __launch_bounds__(256) ttt_diag_bwd_kernel(const BwdArgs a) {
       dk[e] = fmaf(ds, qf[e], dk[e]);
     }
   }
-  __nv_bfloat16* dkrow = row_ptr_w(a.dk, b, hk, kr);
-  __nv_bfloat16* dvrow = row_ptr_w(a.dv, b, hk, kr);
+  const int64_t koff = b * a.dk.sb + hk * a.dk.sh + kr * a.dk.ss;
+  const int64_t voff = b * a.dv.sb + hk * a.dv.sh + kr * a.dv.ss;
 #pragma unroll
   for (int e = 0; e < EPL; ++e) {
     const int c = lane + 32 * e;
     if (c < D) {
-      dkrow[c] = __float2bfloat16_rn(dk[e] * d.scale);
-      dvrow[c] = __float2bfloat16_rn(dv[e]);
+      if (d.out_f32) {
+        reinterpret_cast<float*>(a.dk.ptr)[koff + c] = dk[e] * d.scale;
+        reinterpret_cast<float*>(a.dv.ptr)[voff + c] = dv[e];
+      } else {
+        reinterpret_cast<__nv_bfloat16*>(a.dk.ptr)[koff + c] = __float2bfloat16_rn(dk[e] * d.scale);
+        reinterpret_cast<__nv_bfloat16*>(a.dv.ptr)[voff + c] = __float2bfloat16_rn(dv[e]);
+      }
     }
   }
 }
 
 template <int D>
-cudaError_t launch_bwd_d(const BwdArgs& a, const Maps& m, cudaStream_t s) {
+cudaError_t launch_bwd_d(const BwdArgs& a, const Maps& m, unsigned passes, cudaStream_t s) {
   cudaError_t e;
-  {
+  if (passes & 1u) {
     constexpr int RPB = 256 / (D / 8);
     const int64_t rows = (int64_t)a.d.B * a.d.Hq * a.d.Sq;
     bwd_prep_kernel<D><<<(unsigned)((rows + RPB - 1) / RPB), 256, 0, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  {
+  if (passes & 2u) {
     using L = DkdvLayout<D>;
     auto kern = bwd_dkdv_kernel<D>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC)) !=
@@ -791,7 +821,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const Maps& m, cudaStream_t s) {
     kern<<<grid, kThreads, L::ALLOC, s>>>(m.q, m.k, m.v, m.dout, a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  {
+  if (passes & 4u) {
     using L = DqLayout<D>;
     auto kern = bwd_dq_kernel<D>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC)) !=
@@ -801,7 +831,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const Maps& m, cudaStream_t s) {
     kern<<<grid, kThreads, L::ALLOC, s>>>(m.q, m.k, m.v, m.dout, a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if (a.d.geom.ttt > 0) {
+  if ((passes & 8u) && a.d.geom.ttt > 0) {
     const int64_t rows = (int64_t)a.d.B * a.d.Hkv * a.d.geom.ttt * a.d.Sq;
     ttt_diag_bwd_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -811,12 +841,12 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const Maps& m, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_bwd(const BwdArgs& a, const Maps& m, cudaStream_t s) {
+cudaError_t launch_bwd(const BwdArgs& a, const Maps& m, unsigned passes, cudaStream_t s) {
   switch (a.d.D) {
-    case 16: return launch_bwd_d<16>(a, m, s);
-    case 32: return launch_bwd_d<32>(a, m, s);
-    case 64: return launch_bwd_d<64>(a, m, s);
-    case 128: return launch_bwd_d<128>(a, m, s);
+    case 16: return launch_bwd_d<16>(a, m, passes, s);
+    case 32: return launch_bwd_d<32>(a, m, passes, s);
+    case 64: return launch_bwd_d<64>(a, m, passes, s);
+    case 128: return launch_bwd_d<128>(a, m, passes, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -392,16 +392,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
         }
         const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
-        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o.ptr) + b * a.o.sb +
-                              h * a.o.sh + (int64_t)q * a.o.ss;
+        const int64_t ooff = b * a.o.sb + h * a.o.sh + (int64_t)q * a.o.ss;
+        if (d.out_f32) {
+          float* orow = reinterpret_cast<float*>(a.o.ptr) + ooff;
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 8) {
-          uint4 pkt;
-          pkt.x = pack_bf16x2(o[c0 + 0] * inv, o[c0 + 1] * inv);
-          pkt.y = pack_bf16x2(o[c0 + 2] * inv, o[c0 + 3] * inv);
-          pkt.z = pack_bf16x2(o[c0 + 4] * inv, o[c0 + 5] * inv);
-          pkt.w = pack_bf16x2(o[c0 + 6] * inv, o[c0 + 7] * inv);
-          *reinterpret_cast<uint4*>(orow + c0) = pkt;
+          for (int c0 = 0; c0 < D; c0 += 4)
+            *reinterpret_cast<float4*>(orow + c0) =
+                make_float4(o[c0] * inv, o[c0 + 1] * inv, o[c0 + 2] * inv, o[c0 + 3] * inv);
+        } else {
+          __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o.ptr) + ooff;
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 8) {
+            uint4 pkt;
+            pkt.x = pack_bf16x2(o[c0 + 0] * inv, o[c0 + 1] * inv);
+            pkt.y = pack_bf16x2(o[c0 + 2] * inv, o[c0 + 3] * inv);
+            pkt.z = pack_bf16x2(o[c0 + 4] * inv, o[c0 + 5] * inv);
+            pkt.w = pack_bf16x2(o[c0 + 6] * inv, o[c0 + 7] * inv);
+            *reinterpret_cast<uint4*>(orow + c0) = pkt;
+          }
         }
         const float lse = (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * 0.69314718055994531f : 0.f;
         a.lse[((int64_t)b * d.Hq + h) * d.Sq + q] = lse;

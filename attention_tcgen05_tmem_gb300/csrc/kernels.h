@@ -21,6 +21,7 @@ struct Dims {
   MaskGeom geom;
   float scale;       // softmax scale c
   float scale_log2;  // c * log2(e)
+  int out_f32;       // O, dQ, dK, dV are fp32 (else bf16)
 };
 
 struct Ctl {
@@ -48,7 +49,8 @@ struct Maps {
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, const Maps& m, cudaStream_t s);
-cudaError_t launch_bwd(const BwdArgs& a, const Maps& m, cudaStream_t s);
+// passes: mask of 1 = Delta prep, 2 = dK/dV, 4 = dQ, 8 = TTT suffix keys
+cudaError_t launch_bwd(const BwdArgs& a, const Maps& m, unsigned passes, cudaStream_t s);
 cudaError_t launch_mask_pattern(const Dims& d, uint8_t* bits, uint8_t* tiles, cudaStream_t s);
 // One-tile descriptor probe (test only).  mode 0: C[128x128] = A[128xD] B[128xD]^T with
 // both operands K-major in shared memory; mode 1: C[128xD] = A[128x128] B[128xD] with A in

@@ -30,11 +30,13 @@
  *
  * Layout and types
  * ----------------
- * Every Q/K/V/O/dO/dQ/dK/dV tensor is bf16 [B, H, S, D] with D contiguous
+ * Every Q/K/V/O/dO/dQ/dK/dV tensor is [B, H, S, D] with D contiguous
  * (stride 1) and arbitrary element strides for B, H and S (so BHSD and BSHD
- * both work).  Pointers must be 16-byte aligned and every stride times 2 bytes
- * a multiple of 16.  D is 16, 32, 64 or 128.  LSE is fp32 contiguous
- * [B, Hq, Sq].  Arithmetic: bf16 MMA operands, fp32 accumulation and softmax.
+ * both work).  Q, K, V and dO are bf16; O, dQ, dK and dV are bf16 or fp32 as
+ * attn_problem.out_dtype says.  Pointers must be 16-byte aligned and every
+ * stride times the element size a multiple of 16 bytes.  D is 16, 32, 64 or
+ * 128.  LSE is fp32 contiguous [B, Hq, Sq].  Arithmetic: bf16 MMA operands,
+ * fp32 accumulation and softmax.
  *
  * Ownership and streams
  * ---------------------
@@ -81,20 +83,27 @@ typedef enum {
   ATTN_ERR_DEVICE_TIMEOUT = 6  /* a device-side wait ran out of budget */
 } attn_status;
 
-/* A bf16 [B, H, S, D] tensor view: D has stride 1, the other strides are in
- * elements. */
+/* A [B, H, S, D] tensor view: D has stride 1, the other strides are in
+ * elements of the tensor's type. */
 typedef struct {
   const void* ptr;
   int64_t stride_b, stride_h, stride_s;
 } attn_tensor;
 
+/* Element type of the outputs O, dQ, dK and dV (inputs are always bf16). */
+typedef enum { ATTN_OUT_BF16 = 0, ATTN_OUT_F32 = 1 } attn_out_dtype;
+
 /* Problem shape.  mask is an attn_mask_kind; ttt_step is t for ATTN_MASK_TTT
- * (ignored otherwise); scale <= 0 selects 1/sqrt(D). */
+ * (ignored otherwise); scale <= 0 selects 1/sqrt(D); out_dtype is an
+ * attn_out_dtype for O (forward output and backward input), dQ, dK and dV.
+ * fp32 outputs avoid the bf16 rounding of large GQA gradient sums (a bf16
+ * value of magnitude 8 is only good to 2^-5). */
 typedef struct {
   int B, Hq, Hkv, Sq, Skv, D;
   int mask;
   int ttt_step;
   float scale;
+  int out_dtype;
 } attn_problem;
 
 /* Whether the problem is supported.  Pure host check, no side effects.
@@ -122,6 +131,26 @@ attn_status attn_train_bwd(const attn_problem* p, attn_tensor q, attn_tensor k, 
                            attn_tensor o, attn_tensor dout, const float* lse, attn_tensor dq,
                            attn_tensor dk, attn_tensor dv, void* workspace, size_t ws_bytes,
                            void* stream);
+
+/* The backward's passes, for attn_train_bwd_passes. */
+typedef enum {
+  ATTN_BWD_PREP = 1,  /* Delta = rowsum(dO * O) into the workspace */
+  ATTN_BWD_DKDV = 2,  /* dK, dV of the tiled keys (needs PREP's Delta) */
+  ATTN_BWD_DQ = 4,    /* dQ incl. TTT suffix-diagonal terms (needs PREP's Delta) */
+  ATTN_BWD_TTT = 8,   /* dK, dV of the TTT suffix keys (needs PREP's Delta) */
+  ATTN_BWD_ALL = 15
+} attn_bwd_pass;
+
+/* Same arguments and checks as attn_train_bwd, but enqueues only the passes
+ * set in `passes` (a mask of attn_bwd_pass), in the order PREP, DKDV, DQ,
+ * TTT.  DKDV, DQ and TTT read the Delta that PREP wrote into the workspace
+ * and are independent of each other, so a caller may run them on different
+ * streams once PREP is done, or time them one by one.  ATTN_BWD_TTT is a
+ * no-op unless the mask is TTT with ttt_step > 0. */
+attn_status attn_train_bwd_passes(const attn_problem* p, unsigned passes, attn_tensor q,
+                                  attn_tensor k, attn_tensor v, attn_tensor o, attn_tensor dout,
+                                  const float* lse, attn_tensor dq, attn_tensor dk, attn_tensor dv,
+                                  void* workspace, size_t ws_bytes, void* stream);
 
 /* Message for the calling thread's last non-OK status ("" if none). */
 const char* attn_train_last_error(void);

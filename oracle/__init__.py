@@ -70,6 +70,10 @@ def _load():
             lib.oracle_bwd.restype = ctypes.c_int
             lib.oracle_bwd.argtypes = [ctypes.c_int] * 3 + [L, L] + [ctypes.c_int] * 3 + [
                 ctypes.c_double] + [dp] * 7
+            lib.oracle_fwd_rows.restype = ctypes.c_int
+            lib.oracle_fwd_rows.argtypes = lib.oracle_fwd.argtypes + [L, L]
+            lib.oracle_bwd_rows.restype = ctypes.c_int
+            lib.oracle_bwd_rows.argtypes = lib.oracle_bwd.argtypes + [L, L]
             lib.oracle_count_visible.restype = ctypes.c_longlong
             lib.oracle_count_visible.argtypes = [ctypes.c_int, ctypes.c_int, L, L]
             lib.oracle_num_threads.restype = ctypes.c_int
@@ -124,30 +128,35 @@ def _dims(q, k):
     return B, Hq, Hkv, Sq, Skv, D
 
 
-def fwd(q, k, v, mask="causal", t: int = 0, scale: float | None = None):
-    """Returns (O [B,Hq,Sq,D], LSE [B,Hq,Sq]) in fp64."""
+def fwd(q, k, v, mask="causal", t: int = 0, scale: float | None = None, rows=None):
+    """Returns (O [B,Hq,Sq,D], LSE [B,Hq,Sq]) in fp64.  rows=(begin, end)
+    restricts the work to those query rows (others stay zero)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Hq, Hkv, Sq, Skv, D = _dims(q, k)
     scale = default_scale(D) if scale is None else float(scale)
+    r0, r1 = (0, Sq) if rows is None else rows
     o = np.zeros((B, Hq, Sq, D))
     lse = np.zeros((B, Hq, Sq))
-    rc = _load().oracle_fwd(B, Hq, Hkv, Sq, Skv, D, _mask_id(mask), t, scale, _ptr(q), _ptr(k),
-                            _ptr(v), _ptr(o), _ptr(lse))
+    rc = _load().oracle_fwd_rows(B, Hq, Hkv, Sq, Skv, D, _mask_id(mask), t, scale, _ptr(q),
+                                 _ptr(k), _ptr(v), _ptr(o), _ptr(lse), r0, r1)
     if rc != 0:
         raise ValueError(f"oracle_fwd rejected the problem (code {rc})")
     return o, lse
 
 
-def bwd(q, k, v, do, mask="causal", t: int = 0, scale: float | None = None):
-    """Returns (dQ, dK, dV) in fp64; dK/dV summed over each kv head's q heads."""
+def bwd(q, k, v, do, mask="causal", t: int = 0, scale: float | None = None, rows=None):
+    """Returns (dQ, dK, dV) in fp64; dK/dV summed over each kv head's q heads.
+    rows=(begin, end) restricts the work to those query rows: dQ of those
+    rows and their contributions to dK/dV."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     B, Hq, Hkv, Sq, Skv, D = _dims(q, k)
     scale = default_scale(D) if scale is None else float(scale)
+    r0, r1 = (0, Sq) if rows is None else rows
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
-    rc = _load().oracle_bwd(B, Hq, Hkv, Sq, Skv, D, _mask_id(mask), t, scale, _ptr(q), _ptr(k),
-                            _ptr(v), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv))
+    rc = _load().oracle_bwd_rows(B, Hq, Hkv, Sq, Skv, D, _mask_id(mask), t, scale, _ptr(q),
+                                 _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), r0, r1)
     if rc != 0:
         raise ValueError(f"oracle_bwd rejected the problem (code {rc})")
     return dq, dk, dv

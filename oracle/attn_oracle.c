@@ -113,11 +113,14 @@ static int check_shape(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mas
     return 0;
 }
 
-/* Forward: O [B,Hq,Sq,D], LSE [B,Hq,Sq].  Returns 0 on success. */
-int oracle_fwd(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t, double scale,
-               const double *Q, const double *K, const double *V, double *O, double *LSE)
+/* Forward over query rows [q_begin, q_end) of every (b, h): O [B,Hq,Sq,D],
+ * LSE [B,Hq,Sq] (other rows untouched).  Returns 0 on success. */
+int oracle_fwd_rows(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t,
+                    double scale, const double *Q, const double *K, const double *V, double *O,
+                    double *LSE, long q_begin, long q_end)
 {
     if (check_shape(B, Hq, Hkv, Sq, Skv, D, mask, t)) return 1;
+    if (q_begin < 0 || q_end > Sq || q_begin > q_end) return 1;
     const int G = Hq / Hkv;
     int ok = 1;
 #pragma omp parallel
@@ -137,7 +140,7 @@ int oracle_fwd(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t
                 const double *Vh = V + ((long)b * Hkv + hk) * Skv * D;
                 double *Oh = O + ((long)b * Hq + h) * Sq * D;
                 double *Lh = LSE + ((long)b * Hq + h) * Sq;
-                for (long q = 0; q < Sq; ++q) {
+                for (long q = q_begin; q < q_end; ++q) {
                     double lse;
                     long nvis = row_scores(Qh + q * D, Kh, Skv, D, scale, mask, t, Sq, q, s, &lse);
                     double *orow = Oh + q * D;
@@ -157,14 +160,25 @@ int oracle_fwd(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t
     return ok ? 0 : 2;
 }
 
-/* Backward: dQ [B,Hq,Sq,D], dK and dV [B,Hkv,Skv,D].  Recomputes P and O
+/* Forward over every row. */
+int oracle_fwd(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t, double scale,
+               const double *Q, const double *K, const double *V, double *O, double *LSE)
+{
+    return oracle_fwd_rows(B, Hq, Hkv, Sq, Skv, D, mask, t, scale, Q, K, V, O, LSE, 0, Sq);
+}
+
+/* Backward over query rows [q_begin, q_end): dQ of those rows, and the dK /
+ * dV contributions of those rows (the full gradients when the range is
+ * [0, Sq)).  dQ [B,Hq,Sq,D], dK and dV [B,Hkv,Skv,D].  Recomputes P and O
  * itself.  dK/dV are accumulated per q head and then summed over the group in
  * ascending head order.  Returns 0 on success. */
-int oracle_bwd(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t, double scale,
-               const double *Q, const double *K, const double *V, const double *dO, double *dQ,
-               double *dK, double *dV)
+int oracle_bwd_rows(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t,
+                    double scale, const double *Q, const double *K, const double *V,
+                    const double *dO, double *dQ, double *dK, double *dV, long q_begin,
+                    long q_end)
 {
     if (check_shape(B, Hq, Hkv, Sq, Skv, D, mask, t)) return 1;
+    if (q_begin < 0 || q_end > Sq || q_begin > q_end) return 1;
     const int G = Hq / Hkv;
     const size_t head_kv = (size_t)Skv * D;
     double *dKh_all = (double *)calloc((size_t)B * Hq * head_kv, sizeof(double));
@@ -195,7 +209,7 @@ int oracle_bwd(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t
                 double *dQh = dQ + ((long)b * Hq + h) * Sq * D;
                 double *dKh = dKh_all + ((size_t)b * Hq + h) * head_kv;
                 double *dVh = dVh_all + ((size_t)b * Hq + h) * head_kv;
-                for (long q = 0; q < Sq; ++q) {
+                for (long q = q_begin; q < q_end; ++q) {
                     double lse;
                     const double *qrow = Qh + q * D;
                     const double *dorow = dOh + q * D;
@@ -256,6 +270,14 @@ int oracle_bwd(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t
     free(dKh_all);
     free(dVh_all);
     return ok ? 0 : 2;
+}
+
+/* Backward over every row. */
+int oracle_bwd(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t, double scale,
+               const double *Q, const double *K, const double *V, const double *dO, double *dQ,
+               double *dK, double *dV)
+{
+    return oracle_bwd_rows(B, Hq, Hkv, Sq, Skv, D, mask, t, scale, Q, K, V, dO, dQ, dK, dV, 0, Sq);
 }
 
 /* Exact count of visible (q, kv) pairs for one (b, h); used to pin the

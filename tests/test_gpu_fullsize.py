@@ -1,0 +1,68 @@
+"""Parity at the full workload sizes, in the launch configuration bench.py
+times (the whole problem in one forward call and one backward call, fp32
+outputs).  The oracle recomputes a sample of whole heads exactly: every q
+head of one or more kv-head groups (so dK and dV, which sum a group, are
+complete), over all rows."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_tcgen05_tmem_gb300 import binding, synth
+from tests.gpu_util import LSE_ATOL, compare, device
+
+
+def run_sampled(w, b_idx=(0,), groups=(0,), out="fp32"):
+    dev = device()
+    x = synth.make_inputs(w)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
+    o, lse = binding.fwd(q, k, v, w.mask, w.ttt_step, out=out)
+    dq, dk, dv = binding.bwd(q, k, v, o, lse, do, w.mask, w.ttt_step)
+    binding.device_status()
+    G = w.G
+    for b in b_idx:
+        for g in groups:
+            hs = slice(g * G, (g + 1) * G)
+            sub = {n: x[n][b:b + 1, hs] for n in ("q", "dout")}
+            sub.update({n: x[n][b:b + 1, g:g + 1] for n in ("k", "v")})
+            ro, rl = oracle.fwd(sub["q"], sub["k"], sub["v"], w.mask, w.ttt_step)
+            rdq, rdk, rdv = oracle.bwd(sub["q"], sub["k"], sub["v"], sub["dout"], w.mask,
+                                       w.ttt_step)
+            tag = f"{w.name}[b={b},kv={g}]"
+            compare(tag + " O", o[b:b + 1, hs], ro)
+            compare(tag + " LSE", lse[b:b + 1, hs], rl, atol=LSE_ATOL, rel_l2=1e-3)
+            compare(tag + " dQ", dq[b:b + 1, hs], rdq)
+            compare(tag + " dK", dk[b:b + 1, g:g + 1], rdk)
+            compare(tag + " dV", dv[b:b + 1, g:g + 1], rdv)
+
+
+@pytest.mark.gpu
+@pytest.mark.timeout(1800)
+def test_long_causal_gqa_full_size():
+    run_sampled(synth.LONG_GQA, groups=(0,))
+
+
+@pytest.mark.gpu
+@pytest.mark.timeout(1800)
+@pytest.mark.parametrize("t", [1, 6])
+def test_eagle3_ttt_full_size(t):
+    run_sampled(synth.TTT_STEPS[t], groups=(0,))
+
+
+@pytest.mark.gpu
+@pytest.mark.timeout(1800)
+def test_dit_cross_full_size():
+    run_sampled(synth.DIT_CROSS, b_idx=(0, 1), groups=(0, 15))
+
+
+@pytest.mark.gpu
+@pytest.mark.timeout(1800)
+def test_dit_self_full_size():
+    run_sampled(synth.DIT_SELF, b_idx=(1,), groups=(3,))
+
+
+@pytest.mark.gpu
+@pytest.mark.timeout(1800)
+@pytest.mark.parametrize("w", [w for w in synth.SWEEP if w.Sq == 4096], ids=lambda w: w.name)
+def test_sweep_s4096_full(w):
+    run_sampled(w, b_idx=tuple(range(w.B)), groups=(0,))

@@ -12,11 +12,11 @@ from attention_tcgen05_tmem_gb300 import binding, synth
 from tests.gpu_util import LSE_ATOL, compare, device
 
 
-def run_both(w: synth.Workload, check_bwd=True):
+def run_both(w: synth.Workload, check_bwd=True, out="fp32"):
     dev = device()
     x = synth.make_inputs(w)
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
-    o, lse = binding.fwd(q, k, v, w.mask, w.ttt_step)
+    o, lse = binding.fwd(q, k, v, w.mask, w.ttt_step, out=out)
     binding.device_status()
     ro, rl = oracle.fwd(x["q"], x["k"], x["v"], w.mask, w.ttt_step)
     compare("O", o, ro)
@@ -58,9 +58,10 @@ CASES = [
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("out", ["fp32", "bf16"])
 @pytest.mark.parametrize("w", CASES, ids=[c.name for c in CASES])
-def test_parity(w):
-    run_both(w)
+def test_parity(w, out):
+    run_both(w, out=out)
 
 
 SWEEP_SMALL = [w for w in synth.SWEEP if w.Sq <= 1024]
