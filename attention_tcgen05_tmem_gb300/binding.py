@@ -22,7 +22,7 @@ STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID", 2: "ATTN_ERR_UNSUPPORTED", 3: "AT
 
 # Entry points of include/attn_train.h (checked against the header by the tests).
 EXPORTS = ("attn_train_supports", "attn_train_workspace_size", "attn_train_fwd", "attn_train_bwd",
-           "attn_train_bwd_passes", "attn_train_last_error", "attn_train_device_status", "attn_train_set_wait_budget_ns",
+           "attn_train_bwd_passes", "attn_train_bwd_noalloc", "attn_train_last_error", "attn_train_device_status", "attn_train_set_wait_budget_ns",
            "attn_train_mask_pattern", "attn_train_probe_mma", "attn_train_selftest_wait_timeout")
 
 
@@ -72,6 +72,7 @@ def load(path: str = LIB_PATH):
             "attn_train_bwd": (st, [P, T, T, T, T, T, vp, T, T, T, vp, ctypes.c_size_t, vp]),
             "attn_train_bwd_passes": (st, [P, ctypes.c_uint, T, T, T, T, T, vp, T, T, T, vp,
                                            ctypes.c_size_t, vp]),
+            "attn_train_bwd_noalloc": (st, [P, T, T, T, T, T, vp, T, T, T, vp]),
             "attn_train_last_error": (ctypes.c_char_p, []),
             "attn_train_device_status": (st, [vp]),
             "attn_train_set_wait_budget_ns": (st, [ctypes.c_uint64]),
@@ -164,6 +165,14 @@ def bwd_passes_raw(p: Problem, passes: int, q, k, v, o, dout, lse, dq, dk, dv, w
                                         view(dq), view(dk), view(dv),
                                         ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
                                         _stream(stream)))
+
+
+def bwd_noalloc_raw(p: Problem, q, k, v, o, dout, lse, dq, dk, dv, stream=None):
+    """attn_train_bwd_noalloc: the backward using the library's built-in
+    scratch instead of a workspace (for callers that cannot allocate)."""
+    _check(load().attn_train_bwd_noalloc(ctypes.byref(p), view(q), view(k), view(v), view(o),
+                                         view(dout), ctypes.c_void_p(lse.data_ptr()), view(dq),
+                                         view(dk), view(dv), _stream(stream)))
 
 
 def device_status(stream=None):

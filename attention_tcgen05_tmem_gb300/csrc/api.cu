@@ -187,6 +187,36 @@ size_t ws_bytes_for(const attn_problem* p) {
   return (delta + 255) & ~(size_t)255;
 }
 
+// ------------------------------------------- built-in scratch (no-alloc bwd)
+// Scratch for attn_train_bwd_noalloc: the backward's only scratch is the
+// fp32 Delta row statistic, B * Hq * Sq floats.  4 MiB covers 1,048,576 rows
+// (the long GQA workload needs 524,288).  It lives in the module image, so
+// every GPU that loads this library holds it until the process exits.
+constexpr size_t kNoAllocScratchBytes = (size_t)4 << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+void* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+// Device address of the scratch array on the current device.  In host code
+// `g_noalloc_scratch` names a host-side shadow, not device memory, so the
+// address must come from cudaGetSymbolAddress, once per device.
+attn_status noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(built-in scratch)");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -294,6 +324,26 @@ attn_status attn_train_bwd_passes(const attn_problem* p, unsigned passes, attn_t
   cudaError_t e = attn::launch_bwd(a, m, passes, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   return ATTN_OK;
+}
+
+attn_status attn_train_bwd_noalloc(const attn_problem* p, attn_tensor q, attn_tensor k,
+                                   attn_tensor v, attn_tensor o, attn_tensor dout,
+                                   const float* lse, attn_tensor dq, attn_tensor dk,
+                                   attn_tensor dv, void* stream) {
+  size_t need = 0;
+  attn_status st = attn_train_workspace_size(p, &need);
+  if (st != ATTN_OK) return st;
+  if (need > kNoAllocScratchBytes)
+    return fail(ATTN_ERR_WORKSPACE,
+                "attn_train_bwd_noalloc: this problem needs %zu bytes of scratch (B*Hq*Sq = %lld "
+                "rows) but the built-in scratch holds %zu bytes (%zu rows); call attn_train_bwd "
+                "with a caller-provided workspace instead",
+                need, (long long)p->B * p->Hq * p->Sq, kNoAllocScratchBytes,
+                kNoAllocScratchBytes / sizeof(float));
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != ATTN_OK) return st;
+  return attn_train_bwd(p, q, k, v, o, dout, lse, dq, dk, dv, scratch, kNoAllocScratchBytes,
+                        stream);
 }
 
 const char* attn_train_last_error(void) { return g_msg; }

@@ -73,9 +73,14 @@ DIT_CROSS = Workload("dit_full_cross_B2_H16_Sq12288_Skv512_D64", 2, 16, 16, 1228
 
 ALL = (TINY,) + SWEEP + (LONG_GQA,) + TTT_STEPS + (DIT_SELF, DIT_CROSS)
 
+# Smaller cases of the same kernels for hardware-counter captures (inputs
+# still larger than the 129 MB L2 once outputs are counted).
+PROFILE = (Workload("profile_causal_gqa_B1_Hq32_Hkv4_S4096_D128", 1, 32, 4, 4096, 4096, 128,
+                    "causal", 0, 2),)
+
 
 def by_name(name: str) -> Workload:
-    for w in ALL:
+    for w in ALL + PROFILE:
         if w.name == name:
             return w
     raise KeyError(name)

@@ -152,6 +152,30 @@ attn_status attn_train_bwd_passes(const attn_problem* p, unsigned passes, attn_t
                                   const float* lse, attn_tensor dq, attn_tensor dk, attn_tensor dv,
                                   void* workspace, size_t ws_bytes, void* stream);
 
+/* Backward without a caller-provided workspace.  The pages have no
+ * counterpart for this entry point; it exists for callers that cannot
+ * allocate device memory: code plugged into a host framework that owns all
+ * device memory and hands an operator only its inputs and outputs (no
+ * workspace hook), and code on a path where cudaMalloc's implicit device
+ * synchronization is not acceptable.  Same arguments, checks, kernels and
+ * results as attn_train_bwd minus the workspace pair; it allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library call).
+ *
+ * Its scratch (the fp32 Delta row statistic) is a 4 MiB array compiled into
+ * the library as device memory, held by every GPU that loads the library
+ * until the process exits.  Limit: B * Hq * Sq <= 1,048,576; larger problems
+ * return ATTN_ERR_WORKSPACE with a message (use attn_train_bwd then).
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call on a device shares the one array and each call
+ * rewrites all the scratch it reads, so nothing needs clearing between
+ * calls; but calls whose work overlaps on the GPU (different streams, no
+ * ordering between them) race on it and must be serialized by the caller. */
+attn_status attn_train_bwd_noalloc(const attn_problem* p, attn_tensor q, attn_tensor k,
+                                   attn_tensor v, attn_tensor o, attn_tensor dout,
+                                   const float* lse, attn_tensor dq, attn_tensor dk,
+                                   attn_tensor dv, void* stream);
+
 /* Message for the calling thread's last non-OK status ("" if none). */
 const char* attn_train_last_error(void);
 
