@@ -15,7 +15,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/attn_train.h"
+#include "attn_train.h"
 #include "kernels.h"
 
 namespace {

@@ -31,13 +31,15 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "rows.cuh"
 #include "sched.cuh"
 #include "tile.cuh"
+#include "trace.cuh"
 
 namespace attn {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -52,58 +54,6 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-__device__ __forceinline__ const __nv_bfloat16* row_ptr(const View& v, int b, int h, int64_t s) {
-  return reinterpret_cast<const __nv_bfloat16*>(v.ptr) + b * v.sb + h * v.sh + s * v.ss;
-}
-__device__ __forceinline__ __nv_bfloat16* row_ptr_w(const View& v, int b, int h, int64_t s) {
-  return reinterpret_cast<__nv_bfloat16*>(v.ptr) + b * v.sb + h * v.sh + s * v.ss;
-}
-
-// Dot product of two bf16 rows of length D (fp32 accumulate).
-template <int D>
-__device__ __forceinline__ float dot_rows(const __nv_bfloat16* x, const __nv_bfloat16* y) {
-  float acc = 0.f;
-#pragma unroll
-  for (int c0 = 0; c0 < D; c0 += 8) {
-    const uint4 xa = *reinterpret_cast<const uint4*>(x + c0);
-    const uint4 ya = *reinterpret_cast<const uint4*>(y + c0);
-    const __nv_bfloat162* xv = reinterpret_cast<const __nv_bfloat162*>(&xa);
-    const __nv_bfloat162* yv = reinterpret_cast<const __nv_bfloat162*>(&ya);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 xf = __bfloat1622float2(xv[e]);
-      const float2 yf = __bfloat1622float2(yv[e]);
-      acc = fmaf(xf.x, yf.x, acc);
-      acc = fmaf(xf.y, yf.y, acc);
-    }
-  }
-  return acc;
-}
-
-// Store 16 fp32 values (times mul) at columns c0 .. c0+15 of an output row,
-// as fp32 or bf16.
-__device__ __forceinline__ void store16(const View& v, int b, int h, int64_t s, int c0,
-                                        const float* x, float mul, bool f32) {
-  const int64_t off = b * v.sb + h * v.sh + s * v.ss + c0;
-  if (f32) {
-    float* row = reinterpret_cast<float*>(v.ptr) + off;
-#pragma unroll
-    for (int e = 0; e < 16; e += 4)
-      *reinterpret_cast<float4*>(row + e) =
-          make_float4(x[e] * mul, x[e + 1] * mul, x[e + 2] * mul, x[e + 3] * mul);
-  } else {
-    __nv_bfloat16* row = reinterpret_cast<__nv_bfloat16*>(v.ptr) + off;
-#pragma unroll
-    for (int e = 0; e < 16; e += 8) {
-      uint4 pkt;
-      pkt.x = pack_bf16x2(x[e + 0] * mul, x[e + 1] * mul);
-      pkt.y = pack_bf16x2(x[e + 2] * mul, x[e + 3] * mul);
-      pkt.z = pack_bf16x2(x[e + 4] * mul, x[e + 5] * mul);
-      pkt.w = pack_bf16x2(x[e + 6] * mul, x[e + 7] * mul);
-      *reinterpret_cast<uint4*>(row + e) = pkt;
-    }
-  }
-}
 
 // ===================================================================== prep
 // Delta[b, h, q] = sum_d dO * O.  D/8 threads per row, 16-byte loads.
@@ -244,6 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto iter_head = [&](int it) { return hk * d.G + it / n_q; };
   auto iter_q0 = [&](int it) { return (qt_begin + it % n_q) * kBM; };
 
+  if (warp >= 8) {
+    regs_shrink();  // producer / MMA warpgroup (warps 10, 11 idle)
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (N > 0) {
@@ -291,27 +243,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && N > 0) {
       constexpr uint32_t idesc_s = make_idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_g = make_idesc_bf16(128, D, false, true);
-      const uint32_t sK = smem_u32(smem + L::K_OFF);
-      const uint32_t sV = smem_u32(smem + L::V_OFF);
-      const uint32_t sST = smem_u32(smem + L::ST_OFF);
-      auto sq = [&](int it) { return sST + (it % NST) * L::STAGE_BYTES; };
-      auto sdo = [&](int it) { return sST + (it % NST) * L::STAGE_BYTES + TG::TILE_BYTES; };
+      const uint64_t dK = TG::kmajor_base(smem_u32(smem + L::K_OFF));
+      const uint64_t dV = TG::kmajor_base(smem_u32(smem + L::V_OFF));
+      const uint64_t dSTk = TG::kmajor_base(smem_u32(smem + L::ST_OFF));   // stage 0, K-major
+      const uint64_t dSTm = TG::mnmajor_base(smem_u32(smem + L::ST_OFF));  // stage 0, MN-major
+      auto stage = [&](int it) { return TG::bytes((it % NST) * L::STAGE_BYTES); };
+      constexpr uint64_t kDo = TG::bytes(TG::TILE_BYTES);  // dO follows Q in a stage
       auto issue_st = [&](int it) {  // S^T = K Q^T
+        const uint64_t qd = dSTk + stage(it);
 #pragma unroll
         for (int kk = 0; kk < TG::KSTEPS; ++kk)
-          umma_ss(tmem + 0, TG::kmajor(sK, kk), TG::kmajor(sq(it), kk), idesc_s, kk > 0);
+          umma_ss(tmem + 0, dK + TG::kmajor_step(kk), qd + TG::kmajor_step(kk), idesc_s, kk > 0);
       };
       auto issue_dpt = [&](int it) {  // dP^T = V dO^T
+        const uint64_t od = dSTk + stage(it) + kDo;
 #pragma unroll
         for (int kk = 0; kk < TG::KSTEPS; ++kk)
-          umma_ss(tmem + 128, TG::kmajor(sV, kk), TG::kmajor(sdo(it), kk), idesc_s, kk > 0);
+          umma_ss(tmem + 128, dV + TG::kmajor_step(kk), od + TG::kmajor_step(kk), idesc_s, kk > 0);
       };
       // A operand in TMEM: q columns 16kk.. of warpgroup kk/4 live at 64*(kk/4) + 8*(kk%4)
-      auto issue_grad = [&](uint32_t acc_col, uint32_t a_col, uint32_t bt, bool acc) {
+      auto issue_grad = [&](uint32_t acc_col, uint32_t a_col, uint64_t bd, bool acc) {
 #pragma unroll
         for (int kk = 0; kk < kBM / 16; ++kk)
           umma_ts(tmem + acc_col, tmem + a_col + 64 * (kk / 4) + 8 * (kk % 4),
-                  TG::mnmajor(bt, kk), idesc_g, (acc || kk > 0) ? 1u : 0u);
+                  bd + TG::mnmajor_step(kk), idesc_g, (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(kv_full, 0, ctl) && mbar_wait(&qdo_full[0], 0, ctl);
       if (ok) {
@@ -322,25 +277,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(dp_full);
       }
       for (int it = 0; ok && it < N; ++it) {
+        ATTN_TR(1, 0, it);
         if (!(ok = mbar_wait(p_ready, (uint32_t)it & 1u, ctl))) break;
+        ATTN_TR(1, 1, it);
         tc_fence_after();
-        issue_grad(256, 0, sdo(it), it > 0);  // dV += P^T dO
+        issue_grad(256, 0, dSTm + stage(it) + kDo, it > 0);  // dV += P^T dO
         const bool more = it + 1 < N;
         if (more) {
           if (!(ok = mbar_wait(&qdo_full[(it + 1) % NST], (uint32_t)((it + 1) / NST) & 1u, ctl)))
             break;
+          ATTN_TR(1, 2, it);
           tc_fence_after();
           issue_st(it + 1);
           umma_commit(s_full);
         }
         if (!(ok = mbar_wait(ds_ready, (uint32_t)it & 1u, ctl))) break;
+        ATTN_TR(1, 3, it);
         tc_fence_after();
-        issue_grad(256 + D, 128, sq(it), it > 0);  // dK += dS^T Q
+        issue_grad(256 + D, 128, dSTm + stage(it), it > 0);  // dK += dS^T Q
         umma_commit(&qdo_empty[it % NST]);
         if (more) {
           issue_dpt(it + 1);
           umma_commit(dp_full);
         }
+        ATTN_TR(1, 4, it);
       }
       if (ok) {
         umma_commit(done);
@@ -349,7 +309,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         drain_wait(drain, 0);
       }
     }
+  }
   } else {
+    regs_grow();  // elementwise warpgroups
     // ------------------------------------------------------- elementwise
     const int wg = warp >> 2;
     const int quad = warp & 3;
@@ -365,7 +327,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q0 = iter_q0(it);
       const float* lse2 = stats + s * 256 + 64 * wg;
       const float* dl = stats + s * 256 + 128 + 64 * wg;
+      const bool tr = lane == 0 && quad == 0;
+      if (tr) ATTN_TR(2 + wg, 0, it);
       if (!(ok = mbar_wait_warp(s_full, (uint32_t)it & 1u, ctl))) break;
+      if (tr) ATTN_TR(2 + wg, 1, it);
       tc_fence_after();
       uint32_t raw[64];
       tmem_ld32x2(tS, tS + 32, raw);
@@ -391,8 +356,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_ready);
+      if (tr) ATTN_TR(2 + wg, 2, it);
 
       if (!(ok = mbar_wait_warp(dp_full, (uint32_t)it & 1u, ctl))) break;
+      if (tr) ATTN_TR(2 + wg, 3, it);
       tc_fence_after();
       tmem_ld32x2(tdP, tdP + 32, raw);
 #pragma unroll
@@ -408,6 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(ds_ready);
+      if (tr) ATTN_TR(2 + wg, 4, it);
     }
     // ------------------------------------------------------------ epilogue
     if (ok && N > 0) ok = mbar_wait_warp(done, 0, ctl);
@@ -449,13 +417,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 struct DqLayout {
   using TG = TileGeom<D>;
-  static constexpr int NSLOT = (D == 128) ? 4 : (D == 64 ? 8 : 10);
+  // K and V have their own rings: a K tile is held until dQ += dS K of its
+  // iteration retires, a V tile only until dP = dO V^T does, so K needs the
+  // deeper ring to keep the copies a full iteration ahead
+  static constexpr int NK = (D == 128) ? 3 : (D == 64 ? 5 : 8);
+  static constexpr int NV = (D == 128) ? 2 : (D == 64 ? 4 : (D == 32 ? 6 : 8));
   static constexpr int Q_OFF = 0;
   static constexpr int DO_OFF = TG::TILE_BYTES;
-  static constexpr int KV_OFF = 2 * TG::TILE_BYTES;
-  static constexpr int BAR_OFF = KV_OFF + NSLOT * TG::TILE_BYTES;
-  // qdo_full, kv_full[NSLOT], kv_empty[NSLOT], sdp_full, sdp_used, ds_ready, ds_free, done, drain
-  static constexpr int NBAR = 1 + 2 * NSLOT + 6;
+  static constexpr int K_OFF = 2 * TG::TILE_BYTES;
+  static constexpr int V_OFF = K_OFF + NK * TG::TILE_BYTES;
+  static constexpr int BAR_OFF = V_OFF + NV * TG::TILE_BYTES;
+  // qdo_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full, dp_full, sdp_used,
+  // ds_ready, ds_free, done, drain
+  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 7;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int BYTES = MISC_OFF + 16;
   // at least 116 KB so that only one CTA fits per SM: each holds all 512 TMEM columns
@@ -470,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const BwdArgs a) {
   using TG = TileGeom<D>;
   using L = DqLayout<D>;
-  constexpr int NSLOT = L::NSLOT;
+  constexpr int NK = L::NK, NV = L::NV;
   constexpr int T_S = 0, T_DP = 128, T_DQ = 256, T_DS = 384;
   extern __shared__ uint8_t smem_raw[];
   if (*reinterpret_cast<volatile uint32_t*>(a.ctl.err) != 0) return;
@@ -478,10 +452,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* qdo_full = bars;
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = kv_full + NSLOT;
-  uint64_t* sdp_full = kv_empty + NSLOT;
-  uint64_t* sdp_used = sdp_full + 1;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + NK;
+  uint64_t* v_full = k_empty + NK;
+  uint64_t* v_empty = v_full + NV;
+  uint64_t* s_full = v_empty + NV;
+  uint64_t* dp_full = s_full + 1;
+  uint64_t* sdp_used = dp_full + 1;
   uint64_t* ds_ready = sdp_used + 1;
   uint64_t* ds_free = ds_ready + 1;
   uint64_t* done = ds_free + 1;
@@ -511,11 +488,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = lane_id();
   if (threadIdx.x == 0) {
     mbar_init(qdo_full, 1);
-    for (int s = 0; s < NSLOT; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
     }
-    mbar_init(sdp_full, 1);
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
     mbar_init(sdp_used, 256);
     mbar_init(ds_ready, 256);
     mbar_init(ds_free, 1);
@@ -534,6 +516,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{a.ctl.err, abort_flag, a.ctl.budget_ns};
 
+  if (warp >= 8) {
+    regs_shrink();  // producer / MMA warpgroup (warps 10, 11 idle)
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && n_kv > 0) {
@@ -542,28 +526,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(qdo_full, 2 * TG::TILE_BYTES);
       TG::load(smem + L::Q_OFF, &tq, qdo_full, q0, h, b);
       TG::load(smem + L::DO_OFF, &tdo, qdo_full, q0, h, b);
-      int issued = 0;
+      int k_issued = 0, v_issued = 0;
       for (int j = 0; j < n_kv; ++j) {
-        bool ok = true;
-        for (int w = 0; w < 2; ++w) {
-          const int idx = 2 * j + w;
-          const int s = idx % NSLOT;
-          const uint32_t ph = (uint32_t)(idx / NSLOT) & 1u;
-          if (!mbar_wait(&kv_empty[s], ph ^ 1u, ctl)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&kv_full[s], TG::TILE_BYTES);
-          TG::load(smem + L::KV_OFF + s * TG::TILE_BYTES, w == 0 ? &tk : &tv, &kv_full[s],
-                   j * kBN, hk, b);
-          issued = idx + 1;
-        }
-        if (!ok) break;
+        if (!mbar_wait(&k_empty[j % NK], ((uint32_t)(j / NK) & 1u) ^ 1u, ctl)) break;
+        mbar_arrive_expect_tx(&k_full[j % NK], TG::TILE_BYTES);
+        TG::load(smem + L::K_OFF + (j % NK) * TG::TILE_BYTES, &tk, &k_full[j % NK], j * kBN, hk, b);
+        k_issued = j + 1;
+        if (!mbar_wait(&v_empty[j % NV], ((uint32_t)(j / NV) & 1u) ^ 1u, ctl)) break;
+        mbar_arrive_expect_tx(&v_full[j % NV], TG::TILE_BYTES);
+        TG::load(smem + L::V_OFF + (j % NV) * TG::TILE_BYTES, &tv, &v_full[j % NV], j * kBN, hk, b);
+        v_issued = j + 1;
       }
       if (*abort_flag) {
         drain_wait(qdo_full, 0);
-        for (int idx = issued - NSLOT < 0 ? 0 : issued - NSLOT; idx < issued; ++idx)
-          drain_wait(&kv_full[idx % NSLOT], (uint32_t)(idx / NSLOT) & 1u);
+        for (int j = k_issued - NK < 0 ? 0 : k_issued - NK; j < k_issued; ++j)
+          drain_wait(&k_full[j % NK], (uint32_t)(j / NK) & 1u);
+        for (int j = v_issued - NV < 0 ? 0 : v_issued - NV; j < v_issued; ++j)
+          drain_wait(&v_full[j % NV], (uint32_t)(j / NV) & 1u);
       }
     }
   } else if (warp == 9) {
@@ -571,55 +550,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_kv > 0) {
       constexpr uint32_t idesc_s = make_idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_g = make_idesc_bf16(128, D, false, true);
-      const uint32_t sQ = smem_u32(smem + L::Q_OFF);
-      const uint32_t sDO = smem_u32(smem + L::DO_OFF);
-      const uint32_t sKV = smem_u32(smem + L::KV_OFF);
-      auto slot = [&](int idx) { return sKV + (idx % NSLOT) * TG::TILE_BYTES; };
-      auto phase = [](int idx) { return (uint32_t)(idx / NSLOT) & 1u; };
+      const uint64_t dQd = TG::kmajor_base(smem_u32(smem + L::Q_OFF));
+      const uint64_t dDO = TG::kmajor_base(smem_u32(smem + L::DO_OFF));
+      const uint64_t dKk = TG::kmajor_base(smem_u32(smem + L::K_OFF));   // K slot 0, K-major
+      const uint64_t dKm = TG::mnmajor_base(smem_u32(smem + L::K_OFF));  // K slot 0, MN-major
+      const uint64_t dVk = TG::kmajor_base(smem_u32(smem + L::V_OFF));   // V slot 0, K-major
+      auto kslot = [](int j) { return TG::bytes((j % NK) * TG::TILE_BYTES); };
+      auto vslot = [](int j) { return TG::bytes((j % NV) * TG::TILE_BYTES); };
+      auto issue_dq = [&](int jp, bool acc) {  // dQ += dS K
+        const uint64_t kd = dKm + kslot(jp);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          umma_ts(tmem + T_DQ, tmem + T_DS + 8 * kk, kd + TG::mnmajor_step(kk), idesc_g,
+                  (acc || kk > 0) ? 1u : 0u);
+      };
       bool ok = mbar_wait(qdo_full, 0, ctl);
       for (int j = 0; ok && j < n_kv; ++j) {
-        const int ki = 2 * j, vi = 2 * j + 1;
-        ok = mbar_wait(&kv_full[ki % NSLOT], phase(ki), ctl) &&
-             mbar_wait(&kv_full[vi % NSLOT], phase(vi), ctl);
+        ATTN_TR(1, 0, j);
+        ok = mbar_wait(&k_full[j % NK], (uint32_t)(j / NK) & 1u, ctl) &&
+             mbar_wait(&v_full[j % NV], (uint32_t)(j / NV) & 1u, ctl);
+        ATTN_TR(1, 1, j);
         if (ok && j > 0) ok = mbar_wait(sdp_used, (uint32_t)(j - 1) & 1u, ctl);
         if (!ok) break;
+        ATTN_TR(1, 2, j);
         tc_fence_after();
+        const uint64_t kd = dKk + kslot(j), vd = dVk + vslot(j);
 #pragma unroll
         for (int kk = 0; kk < TG::KSTEPS; ++kk)
-          umma_ss(tmem + T_S, TG::kmajor(sQ, kk), TG::kmajor(slot(ki), kk), idesc_s, kk > 0);
+          umma_ss(tmem + T_S, dQd + TG::kmajor_step(kk), kd + TG::kmajor_step(kk), idesc_s, kk > 0);
+        umma_commit(s_full);
 #pragma unroll
         for (int kk = 0; kk < TG::KSTEPS; ++kk)
-          umma_ss(tmem + T_DP, TG::kmajor(sDO, kk), TG::kmajor(slot(vi), kk), idesc_s, kk > 0);
-        umma_commit(sdp_full);
-        umma_commit(&kv_empty[vi % NSLOT]);
+          umma_ss(tmem + T_DP, dDO + TG::kmajor_step(kk), vd + TG::kmajor_step(kk), idesc_s,
+                  kk > 0);
+        umma_commit(dp_full);
+        umma_commit(&v_empty[j % NV]);
+        ATTN_TR(1, 3, j);
         if (j > 0) {
           if (!(ok = mbar_wait(ds_ready, (uint32_t)(j - 1) & 1u, ctl))) break;
+          ATTN_TR(1, 4, j);
           tc_fence_after();
-          const int kp = 2 * (j - 1);
-#pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
-            umma_ts(tmem + T_DQ, tmem + T_DS + 8 * kk, TG::mnmajor(slot(kp), kk), idesc_g,
-                    (j - 1 > 0 || kk > 0) ? 1u : 0u);
+          issue_dq(j - 1, j - 1 > 0);
           umma_commit(ds_free);
-          umma_commit(&kv_empty[kp % NSLOT]);
+          umma_commit(&k_empty[(j - 1) % NK]);
+          ATTN_TR(1, 5, j);
         }
       }
       if (ok) ok = mbar_wait(ds_ready, (uint32_t)(n_kv - 1) & 1u, ctl);
       if (ok) {
         tc_fence_after();
-        const int kp = 2 * (n_kv - 1);
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          umma_ts(tmem + T_DQ, tmem + T_DS + 8 * kk, TG::mnmajor(slot(kp), kk), idesc_g,
-                  (n_kv - 1 > 0 || kk > 0) ? 1u : 0u);
+        issue_dq(n_kv - 1, n_kv - 1 > 0);
         umma_commit(done);
-        umma_commit(&kv_empty[kp % NSLOT]);
+        umma_commit(&k_empty[(n_kv - 1) % NK]);
       } else {
         umma_commit(drain);
         drain_wait(drain, 0);
       }
     }
+  }
   } else {
+    regs_grow();  // elementwise warpgroups
     // ------------------------------------------------------- elementwise
     const int wg = warp >> 2;
     const int quad = warp & 3;
@@ -633,85 +623,111 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float delta = qin ? a.delta[rrow] : 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      if (!(ok = mbar_wait_warp(sdp_full, (uint32_t)j & 1u, ctl))) break;
+      // P first (needs only S), while the dP MMAs are still running
+      const bool tr = lane == 0 && quad == 0;
+      if (tr) ATTN_TR(2 + wg, 0, j);
+      if (!(ok = mbar_wait_warp(s_full, (uint32_t)j & 1u, ctl))) break;
+      if (tr) ATTN_TR(2 + wg, 1, j);
       tc_fence_after();
-      uint32_t rs[64], rp[64];
+      uint32_t rs[64];
       tmem_ld32x2(tmem + lane_base + T_S + 64 * wg, tmem + lane_base + T_S + 64 * wg + 32, rs);
-      tmem_ld32x2(tmem + lane_base + T_DP + 64 * wg, tmem + lane_base + T_DP + 64 * wg + 32, rp);
-      tc_fence_before();
-      mbar_arrive(sdp_used);
       const int k0 = j * kBN;
       const bool full = tile_is_full(g, q0, k0);
       const int lim = col_limit(g, q, k0) - 64 * wg;
+      float p[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        p[c] = ex2_approx(fmaf(__uint_as_float(rs[c]), sl2, -lse2));
+        if (!full && c > lim) p[c] = 0.f;
+      }
+      if (tr) ATTN_TR(2 + wg, 2, j);
+      if (!(ok = mbar_wait_warp(dp_full, (uint32_t)j & 1u, ctl))) break;
+      if (tr) ATTN_TR(2 + wg, 3, j);
+      tc_fence_after();
+      uint32_t rp[64];
+      tmem_ld32x2(tmem + lane_base + T_DP + 64 * wg, tmem + lane_base + T_DP + 64 * wg + 32, rp);
+      tc_fence_before();
+      mbar_arrive(sdp_used);
+      if (tr) ATTN_TR(2 + wg, 4, j);
       uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        float p0 = ex2_approx(fmaf(__uint_as_float(rs[c]), sl2, -lse2));
-        float p1 = ex2_approx(fmaf(__uint_as_float(rs[c + 1]), sl2, -lse2));
-        if (!full && c > lim) p0 = 0.f;
-        if (!full && c + 1 > lim) p1 = 0.f;
-        const float ds0 = p0 * (__uint_as_float(rp[c]) - delta);
-        const float ds1 = p1 * (__uint_as_float(rp[c + 1]) - delta);
-        pk[c / 2] = pack_bf16x2(ds0, ds1);
-      }
+      for (int c = 0; c < 64; c += 2)
+        pk[c / 2] = pack_bf16x2(p[c] * (__uint_as_float(rp[c]) - delta),
+                                p[c + 1] * (__uint_as_float(rp[c + 1]) - delta));
       if (j > 0) {
         if (!(ok = mbar_wait_warp(ds_free, (uint32_t)(j - 1) & 1u, ctl))) break;
         tc_fence_after();
       }
+      if (tr) ATTN_TR(2 + wg, 5, j);
       tmem_st32(tmem + lane_base + T_DS + 32 * wg, pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(ds_ready);
+      if (tr) ATTN_TR(2 + wg, 6, j);
     }
     // ------------------------------------------------------------ epilogue
     if (ok && n_kv > 0) ok = mbar_wait_warp(done, 0, ctl);
     if (ok) {
       if (n_kv > 0) tc_fence_after();
-      // TTT suffix diagonals: ds_i = p_i (dO . v_i - Delta), dQ += ds_i k_i
-      float ds_i[8];
-      int n_diag = 0;
+      // this warpgroup's dQ columns: 16-wide chunks c0 = 16 wg, 16 wg + 32, ...
+      const uint32_t tq = tmem + lane_base + T_DQ;
+      if (n_kv == 0 && g.ttt > 0) {  // accumulator never written by an MMA: start at zero
+        uint32_t z[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) z[e] = 0u;
+        for (int c0 = 16 * wg; c0 < D; c0 += 32) tmem_st16(tq + c0, z);
+        tmem_st_wait();
+      }
+      // TTT suffix diagonals: ds_i = p_i (dO . v_i - Delta), dQ += ds_i k_i, folded into
+      // the TMEM accumulator kDiagBatch diagonals at a time
       const __nv_bfloat16* qrow = row_ptr(a.q, b, h, q);
       const __nv_bfloat16* dorow = row_ptr(a.dout, b, h, q);
+      for (int i0 = 1; i0 <= g.ttt; i0 += kDiagBatch) {
+        float dsv[kDiagBatch];
+#pragma unroll
+        for (int u = 0; u < kDiagBatch; ++u) {
+          dsv[u] = 0.f;
+          if (qin && i0 + u <= g.ttt) {
+            const int64_t kr = (int64_t)(i0 + u) * d.Sq + q;
+            const float sv = dot_rows<D>(qrow, row_ptr(a.k, b, hk, kr));
+            const float dp = dot_rows<D>(dorow, row_ptr(a.v, b, hk, kr));
+            dsv[u] = ex2_approx(fmaf(sv, sl2, -lse2)) * (dp - delta);
+          }
+        }
+        for (int c0 = 16 * wg; c0 < D; c0 += 32) {
+          uint32_t raw[16];
+          tmem_ld16(tq + c0, raw);
+#pragma unroll
+          for (int u = 0; u < kDiagBatch; ++u) {
+            if (!(qin && i0 + u <= g.ttt)) continue;
+            const __nv_bfloat16* krow = row_ptr(a.k, b, hk, (int64_t)(i0 + u) * d.Sq + q) + c0;
+#pragma unroll
+            for (int e = 0; e < 16; e += 8) {
+              const uint4 ka = *reinterpret_cast<const uint4*>(krow + e);
+              const __nv_bfloat162* kv2 = reinterpret_cast<const __nv_bfloat162*>(&ka);
+#pragma unroll
+              for (int f = 0; f < 4; ++f) {
+                const float2 kf = __bfloat1622float2(kv2[f]);
+                raw[e + 2 * f] = __float_as_uint(fmaf(dsv[u], kf.x, __uint_as_float(raw[e + 2 * f])));
+                raw[e + 2 * f + 1] =
+                    __float_as_uint(fmaf(dsv[u], kf.y, __uint_as_float(raw[e + 2 * f + 1])));
+              }
+            }
+          }
+          tmem_st16(tq + c0, raw);
+        }
+        tmem_st_wait();
+      }
       for (int c0 = 16 * wg; c0 < D; c0 += 32) {
         float acc[16];
-        if (n_kv > 0) {
+        if (n_kv > 0 || g.ttt > 0) {
           uint32_t raw[16];
-          tmem_ld16(tmem + lane_base + T_DQ + c0, raw);
+          tmem_ld16(tq + c0, raw);
 #pragma unroll
           for (int e = 0; e < 16; ++e) acc[e] = __uint_as_float(raw[e]);
         } else {
 #pragma unroll
           for (int e = 0; e < 16; ++e) acc[e] = 0.f;
-        }
-        if (qin && g.ttt > 0) {
-          for (int i0 = 1; i0 <= g.ttt; i0 += 8) {
-            const int cnt = min(8, g.ttt - i0 + 1);
-            if (c0 == 16 * wg || n_diag != i0) {
-              // (re)compute this batch of diagonal weights
-              for (int u = 0; u < cnt; ++u) {
-                const int64_t kr = (int64_t)(i0 + u) * d.Sq + q;
-                const float sv = dot_rows<D>(qrow, row_ptr(a.k, b, hk, kr));
-                const float dp = dot_rows<D>(dorow, row_ptr(a.v, b, hk, kr));
-                const float pv = ex2_approx(fmaf(sv, sl2, -lse2));
-                ds_i[u] = pv * (dp - delta);
-              }
-              n_diag = i0;
-            }
-            for (int u = 0; u < cnt; ++u) {
-              const __nv_bfloat16* krow = row_ptr(a.k, b, hk, (int64_t)(i0 + u) * d.Sq + q) + c0;
-#pragma unroll
-              for (int e = 0; e < 16; e += 8) {
-                const uint4 ka = *reinterpret_cast<const uint4*>(krow + e);
-                const __nv_bfloat162* kv2 = reinterpret_cast<const __nv_bfloat162*>(&ka);
-#pragma unroll
-                for (int f = 0; f < 4; ++f) {
-                  const float2 kf = __bfloat1622float2(kv2[f]);
-                  acc[e + 2 * f] = fmaf(ds_i[u], kf.x, acc[e + 2 * f]);
-                  acc[e + 2 * f + 1] = fmaf(ds_i[u], kf.y, acc[e + 2 * f + 1]);
-                }
-              }
-            }
-          }
         }
         if (qin) store16(a.dq, b, h, q, c0, acc, d.scale, d.out_f32 != 0);
       }
@@ -814,6 +830,8 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const Maps& m, unsigned passes, cudaS
   if (passes & 2u) {
     using L = DkdvLayout<D>;
     auto kern = bwd_dkdv_kernel<D>;
+    static const cudaError_t regs_ok = check_launch_regs(reinterpret_cast<const void*>(kern));
+    if (regs_ok != cudaSuccess) return regs_ok;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC)) !=
         cudaSuccess)
       return e;
@@ -824,6 +842,8 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const Maps& m, unsigned passes, cudaS
   if (passes & 4u) {
     using L = DqLayout<D>;
     auto kern = bwd_dq_kernel<D>;
+    static const cudaError_t regs_ok = check_launch_regs(reinterpret_cast<const void*>(kern));
+    if (regs_ok != cudaSuccess) return regs_ok;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC)) !=
         cudaSuccess)
       return e;
@@ -852,3 +872,5 @@ cudaError_t launch_bwd(const BwdArgs& a, const Maps& m, unsigned passes, cudaStr
 }
 
 }  // namespace attn
+
+ATTN_TRACE_READER(attn_trace_read_bwd)

@@ -33,13 +33,15 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "rows.cuh"
 #include "sched.cuh"
 #include "tile.cuh"
+#include "trace.cuh"
 
 namespace attn {
 namespace {
 
-constexpr int kFwdThreads = 320;
+constexpr int kFwdThreads = 384;
 constexpr float kRescaleThreshold = 8.0f;
 
 template <int D>
@@ -144,6 +146,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{a.ctl.err, abort_flag, a.ctl.budget_ns};
 
+  if (warp >= 8) {
+    regs_shrink();  // producer / MMA warpgroup (warps 10, 11 idle)
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && n_kv > 0) {
@@ -183,22 +187,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (lane == 0 && n_kv > 0) {
       constexpr uint32_t idesc_s = make_idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_o = make_idesc_bf16(128, D, false, true);
-      const uint32_t sQ = smem_u32(smem + L::Q_OFF);
-      const uint32_t sKV = smem_u32(smem + L::KV_OFF);
+      // descriptors of Q tile 0 and of ring slot 0; tiles and slots are offsets
+      const uint64_t dQ0 = TG::kmajor_base(smem_u32(smem + L::Q_OFF));
+      const uint64_t dK0 = TG::kmajor_base(smem_u32(smem + L::KV_OFF));
+      const uint64_t dV0 = TG::mnmajor_base(smem_u32(smem + L::KV_OFF));
       auto slot_of = [](int idx) { return idx % NSLOT; };
       auto phase_of = [](int idx) { return (uint32_t)(idx / NSLOT) & 1u; };
       auto issue_s = [&](int x, int slot) {
-        const uint32_t qa = sQ + x * TG::TILE_BYTES;
-        const uint32_t ka = sKV + slot * TG::TILE_BYTES;
+        const uint64_t qd = dQ0 + TG::bytes(x * TG::TILE_BYTES);
+        const uint64_t kd = dK0 + TG::bytes(slot * TG::TILE_BYTES);
 #pragma unroll
         for (int kk = 0; kk < TG::KSTEPS; ++kk)
-          umma_ss(tmem + x * 128, TG::kmajor(qa, kk), TG::kmajor(ka, kk), idesc_s, kk > 0);
+          umma_ss(tmem + x * 128, qd + TG::kmajor_step(kk), kd + TG::kmajor_step(kk), idesc_s,
+                  kk > 0);
       };
       auto issue_pv = [&](int x, int slot, bool acc) {
-        const uint32_t va = sKV + slot * TG::TILE_BYTES;
+        const uint64_t vd = dV0 + TG::bytes(slot * TG::TILE_BYTES);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          umma_ts(tmem + 256 + x * D, tmem + x * 128 + kk * 8, TG::mnmajor(va, kk), idesc_o,
+          umma_ts(tmem + 256 + x * D, tmem + x * 128 + kk * 8, vd + TG::mnmajor_step(kk), idesc_o,
                   (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(q_full, 0, ctl);
@@ -213,16 +220,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       for (int j = 1; ok && j < n_kv; ++j) {
         const int vi = 2 * (j - 1) + 1, ki = 2 * j;
+        ATTN_TR(1, 0, j);
         ok = mbar_wait(&kv_full[slot_of(vi)], phase_of(vi), ctl) &&
-             mbar_wait(&kv_full[slot_of(ki)], phase_of(ki), ctl) &&
-             mbar_wait(&p_ready[0], (uint32_t)(j - 1) & 1u, ctl);
+             mbar_wait(&kv_full[slot_of(ki)], phase_of(ki), ctl);
+        ATTN_TR(1, 1, j);
+        ok = ok && mbar_wait(&p_ready[0], (uint32_t)(j - 1) & 1u, ctl);
         if (!ok) break;
+        ATTN_TR(1, 2, j);
         tc_fence_after();
         issue_pv(0, slot_of(vi), j - 1 > 0);
         umma_commit(&o_done[0]);
         issue_s(0, slot_of(ki));
         umma_commit(&s_full[0]);
+        ATTN_TR(1, 3, j);
         if (!(ok = mbar_wait(&p_ready[1], (uint32_t)(j - 1) & 1u, ctl))) break;
+        ATTN_TR(1, 4, j);
         tc_fence_after();
         issue_pv(1, slot_of(vi), j - 1 > 0);
         umma_commit(&o_done[1]);
@@ -254,7 +266,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         drain_wait(drain, 0);
       }
     }
+  }
   } else {
+    regs_grow();  // elementwise warpgroups
     // ---------------------------------------------------------- softmax
     const int x = warp >> 2;    // query tile of this warpgroup
     const int quad = warp & 3;  // TMEM lane quadrant
@@ -269,8 +283,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     float m_run = neg_inf();  // running max of c*log2(e)*s
     float l_run = 0.f;
     bool ok = true;
+    const bool tr = lane == 0 && quad == 0;
     for (int j = 0; j < n_kv; ++j) {
+      if (tr) ATTN_TR(2 + x, 0, j);
       if (!(ok = mbar_wait_warp(&s_full[x], (uint32_t)j & 1u, ctl))) break;
+      if (tr) ATTN_TR(2 + x, 1, j);
       tc_fence_after();
       uint32_t sr[128];  // S row as raw fp32 bits; columns k0 .. k0+127
       tmem_ld32x2(tS + 0, tS + 32, *reinterpret_cast<uint32_t(*)[64]>(&sr[0]));
@@ -295,6 +312,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         l_run *= alpha;
       }
       const float mu = (m_run == neg_inf()) ? 0.f : m_run;
+      if (tr) ATTN_TR(2 + x, 2, j);
       float rs = 0.f;
 #pragma unroll
       for (int qtr = 0; qtr < 4; ++qtr) {
@@ -309,6 +327,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tmem_st16(tS + qtr * 16, pk);
       }
       l_run += rs;
+      if (tr) ATTN_TR(2 + x, 3, j);
       if (j > 0) {
         // PV(j-1) finished before S(j) (in-order MMA); consume its phase
         if (!(ok = mbar_wait_warp(&o_done[x], (uint32_t)(j - 1) & 1u, ctl))) break;
@@ -327,90 +346,81 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&p_ready[x]);
+      if (tr) ATTN_TR(2 + x, 4, j);
     }
 
     // ------------------------------------------------------------ epilogue
     if (ok && n_kv > 0) ok = mbar_wait_warp(&o_done[x], (uint32_t)(n_kv - 1) & 1u, ctl);
     if (ok) {
-      float o[D];
-      if (n_kv > 0) {
-        tc_fence_after();
+      if (n_kv > 0) tc_fence_after();
+      const bool qin = q < d.Sq;
+      if (g.ttt > 0) {
+        // TTT suffix diagonals (key/value row i*Sq + q of segment i = 1..t), merged into
+        // the unnormalised O accumulator in TMEM by log-sum-exp
+        if (n_kv == 0) {  // accumulator never written by an MMA: start at zero
+          uint32_t z[16];
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 16) {
-          uint32_t ov[16];
-          tmem_ld16(tO + c0, ov);
+          for (int e = 0; e < 16; ++e) z[e] = 0u;
 #pragma unroll
-          for (int c = 0; c < 16; ++c) o[c0 + c] = __uint_as_float(ov[c]);
+          for (int c0 = 0; c0 < D; c0 += 16) tmem_st16(tO + c0, z);
+          tmem_st_wait();
         }
-      } else {
+        const __nv_bfloat16* qrow = row_ptr(a.q, b, h, q);
+        float m_star = m_run;  // pass 1: the merged running max
+        if (qin)
+          for (int i = 1; i <= g.ttt; ++i)
+            m_star = fmaxf(m_star, dot_rows<D>(qrow, row_ptr(a.k, b, hk, (int64_t)i * d.Sq + q)) * sl2);
+        const float alpha = (m_run == neg_inf()) ? 0.f : ex2_approx(m_run - m_star);
+        l_run *= alpha;
+        // pass 2: O = alpha O + sum_i w_i v_i, kDiagBatch diagonals per TMEM round trip
+        for (int i0 = 1; i0 <= g.ttt; i0 += kDiagBatch) {
+          float w[kDiagBatch];
 #pragma unroll
-        for (int c = 0; c < D; ++c) o[c] = 0.f;
+          for (int u = 0; u < kDiagBatch; ++u) {
+            w[u] = 0.f;
+            if (qin && i0 + u <= g.ttt) {
+              const int64_t kr = (int64_t)(i0 + u) * d.Sq + q;
+              w[u] = ex2_approx(fmaf(dot_rows<D>(qrow, row_ptr(a.k, b, hk, kr)), sl2, -m_star));
+              l_run += w[u];
+            }
+          }
+          const float scale0 = (i0 == 1) ? alpha : 1.f;
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 16) {
+            uint32_t raw[16];
+            float vals[16];
+            tmem_ld16(tO + c0, raw);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) vals[e] = __uint_as_float(raw[e]) * scale0;
+#pragma unroll
+            for (int u = 0; u < kDiagBatch; ++u)
+              if (qin && i0 + u <= g.ttt)
+                axpy16(vals, w[u], row_ptr(a.v, b, hk, (int64_t)(i0 + u) * d.Sq + q) + c0);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) raw[e] = __float_as_uint(vals[e]);
+            tmem_st16(tO + c0, raw);
+          }
+          tmem_st_wait();
+        }
+        m_run = m_star;
       }
-      if (q < d.Sq) {
-        // TTT suffix diagonals: key/value row i*Sq + q of each appended segment
-        if (g.ttt > 0) {
-          const __nv_bfloat16* qrow = reinterpret_cast<const __nv_bfloat16*>(a.q.ptr) +
-                                      b * a.q.sb + h * a.q.sh + (int64_t)q * a.q.ss;
-          for (int i = 1; i <= g.ttt; ++i) {
-            const int64_t kr = (int64_t)i * d.Sq + q;
-            const __nv_bfloat16* krow = reinterpret_cast<const __nv_bfloat16*>(a.k.ptr) +
-                                        b * a.k.sb + hk * a.k.sh + kr * a.k.ss;
-            const __nv_bfloat16* vrow = reinterpret_cast<const __nv_bfloat16*>(a.v.ptr) +
-                                        b * a.v.sb + hk * a.v.sh + kr * a.v.ss;
-            float dot = 0.f;
+      const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+      const bool have_acc = n_kv > 0 || g.ttt > 0;
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 8) {
-              const uint4 qa = *reinterpret_cast<const uint4*>(qrow + c0);
-              const uint4 ka = *reinterpret_cast<const uint4*>(krow + c0);
-              const __nv_bfloat162* qv = reinterpret_cast<const __nv_bfloat162*>(&qa);
-              const __nv_bfloat162* kv = reinterpret_cast<const __nv_bfloat162*>(&ka);
+      for (int c0 = 0; c0 < D; c0 += 16) {
+        float vals[16];
+        if (have_acc) {
+          uint32_t raw[16];
+          tmem_ld16(tO + c0, raw);
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float2 qf = __bfloat1622float2(qv[e]);
-                const float2 kf = __bfloat1622float2(kv[e]);
-                dot = fmaf(qf.x, kf.x, dot);
-                dot = fmaf(qf.y, kf.y, dot);
-              }
-            }
-            const float xs = dot * sl2;
-            const float m_new = fmaxf(m_run, xs);
-            const float al = (m_run == neg_inf()) ? 0.f : ex2_approx(m_run - m_new);
-            const float w = ex2_approx(xs - m_new);
-            l_run = l_run * al + w;
-#pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 8) {
-              const uint4 va = *reinterpret_cast<const uint4*>(vrow + c0);
-              const __nv_bfloat162* vv = reinterpret_cast<const __nv_bfloat162*>(&va);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float2 vf = __bfloat1622float2(vv[e]);
-                o[c0 + 2 * e] = fmaf(o[c0 + 2 * e], al, w * vf.x);
-                o[c0 + 2 * e + 1] = fmaf(o[c0 + 2 * e + 1], al, w * vf.y);
-              }
-            }
-            m_run = m_new;
-          }
-        }
-        const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
-        const int64_t ooff = b * a.o.sb + h * a.o.sh + (int64_t)q * a.o.ss;
-        if (d.out_f32) {
-          float* orow = reinterpret_cast<float*>(a.o.ptr) + ooff;
-#pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 4)
-            *reinterpret_cast<float4*>(orow + c0) =
-                make_float4(o[c0] * inv, o[c0 + 1] * inv, o[c0 + 2] * inv, o[c0 + 3] * inv);
+          for (int e = 0; e < 16; ++e) vals[e] = __uint_as_float(raw[e]);
         } else {
-          __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o.ptr) + ooff;
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 8) {
-            uint4 pkt;
-            pkt.x = pack_bf16x2(o[c0 + 0] * inv, o[c0 + 1] * inv);
-            pkt.y = pack_bf16x2(o[c0 + 2] * inv, o[c0 + 3] * inv);
-            pkt.z = pack_bf16x2(o[c0 + 4] * inv, o[c0 + 5] * inv);
-            pkt.w = pack_bf16x2(o[c0 + 6] * inv, o[c0 + 7] * inv);
-            *reinterpret_cast<uint4*>(orow + c0) = pkt;
-          }
+          for (int e = 0; e < 16; ++e) vals[e] = 0.f;
         }
+        if (qin) store16(a.o, b, h, q, c0, vals, inv, d.out_f32 != 0);
+      }
+      if (qin) {
         const float lse = (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * 0.69314718055994531f : 0.f;
         a.lse[((int64_t)b * d.Hq + h) * d.Sq + q] = lse;
       }
@@ -429,6 +439,8 @@ template <int D>
 cudaError_t launch_fwd_d(const FwdArgs& a, const Maps& m, cudaStream_t s) {
   using L = FwdLayout<D>;
   auto kern = fwd_kernel<D>;
+  static const cudaError_t regs_ok = check_launch_regs(reinterpret_cast<const void*>(kern));
+  if (regs_ok != cudaSuccess) return regs_ok;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   const int n_qp = cdiv(a.d.Sq, 2 * kBM);
@@ -450,3 +462,5 @@ cudaError_t launch_fwd(const FwdArgs& a, const Maps& m, cudaStream_t s) {
 }
 
 }  // namespace attn
+
+ATTN_TRACE_READER(attn_trace_read_fwd)

@@ -11,6 +11,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_runtime.h>
 
 namespace attn {
 
@@ -68,8 +69,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait by one thread.  Returns false if the budget ran out or another
-// role of this CTA already aborted.
-static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const WaitCtl& c) {
+// role of this CTA already aborted.  (Inlined: a real call inside a
+// setmaxnreg region defeats ptxas's per-region register allocation.)
+__device__ __forceinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const WaitCtl& c) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
@@ -241,6 +243,31 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 #undef ATTN_W8
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ------------------------------------------------- register reallocation
+// The tensor-core kernels run 3 warpgroups (384 threads, launched with 168
+// registers per thread = 64,512 in total).  The producer/MMA warpgroup gives
+// registers back and the two elementwise warpgroups take them:
+// 128 * kRegsLow + 256 * kRegsHigh == 384 * 168.  The host refuses to launch
+// a kernel compiled with fewer than kRegsLaunch registers, so an inc can
+// never wait for registers that do not exist.
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsLow = 88;
+constexpr int kRegsHigh = 208;
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= 384 * kRegsLaunch, "register split");
+// Host side: 0 if `kern` was compiled with the registers the split assumes.
+inline cudaError_t check_launch_regs(const void* kern) {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  return fa.numRegs >= kRegsLaunch ? cudaSuccess : cudaErrorLaunchOutOfResources;
+}
+__device__ __forceinline__ void regs_shrink() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+}
+__device__ __forceinline__ void regs_grow() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
 }
 
 // ------------------------------------------------------------- math

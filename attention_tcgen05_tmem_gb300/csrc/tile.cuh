@@ -44,6 +44,22 @@ struct TileGeom {
     const uint32_t a = tile + (uint32_t)kk * 16u * ROWB;
     return make_sdesc(a, (uint32_t)BOX_BYTES, SBO, LAYOUT);
   }
+  // Same descriptors built once per buffer: the start address is the only
+  // field that changes between k-steps and ring slots, and it sits in the low
+  // 14 bits (address >> 4; shared memory addresses stay below 2^18), so a
+  // k-step or slot is one 64-bit add on a precomputed base.
+  __device__ static uint64_t kmajor_base(uint32_t tile) { return make_sdesc(tile, 16u, SBO, LAYOUT); }
+  __device__ static uint64_t mnmajor_base(uint32_t tile) {
+    return make_sdesc(tile, (uint32_t)BOX_BYTES, SBO, LAYOUT);
+  }
+  __host__ __device__ static constexpr uint64_t kmajor_step(int kk) {
+    return (uint64_t)(((kk / (BOXC / 16)) * BOX_BYTES + (kk % (BOXC / 16)) * 32) >> 4);
+  }
+  __host__ __device__ static constexpr uint64_t mnmajor_step(int kk) {
+    return (uint64_t)((kk * 16 * ROWB) >> 4);
+  }
+  __host__ __device__ static constexpr uint64_t bytes(int n) { return (uint64_t)(n >> 4); }
+
   // Issue the TMA boxes of one tile (rows r0 .. r0+127 of head h, batch b).
   __device__ static void load(void* dst, const CUtensorMap* m, uint64_t* bar, int r0, int h,
                               int b) {
