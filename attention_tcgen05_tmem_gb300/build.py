@@ -44,15 +44,30 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD_DIR, exist_ok=True)
+TRACE_LIB = os.path.join(HERE, "libattn_train_trace.so")
+
+
+def build_trace(force: bool = False) -> str:
+    """Same library built with -DATTN_TRACE (pipeline timeline probes on), as
+    libattn_train_trace.so; used by pipeline_trace.py, never by the product."""
+    return build(force=force, trace=True)
+
+
+def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False,
+          trace: bool = False) -> str:
+    lib = TRACE_LIB if trace else LIB
+    if not force and os.path.exists(lib) and all(
+            os.path.getmtime(f) <= os.path.getmtime(lib) for f in _deps()):
+        return lib
+    bdir = BUILD_DIR + ("_trace" if trace else "")
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_v else []
+    if trace:
+        extra.append("-DATTN_TRACE")
 
     def compile_one(src: str) -> tuple[str, str]:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(bdir, src.replace(".cu", ".o"))
         cmd = [cc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -65,13 +80,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> 
         for _, log in results:
             if log:
                 sys.stderr.write(log)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-lcudart"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -3,17 +3,20 @@
 
 One step = one pass of the whole hot path over one batch of synthetic input:
 attn_train_fwd (O, LSE) then the backward passes (Delta prep, dK/dV, dQ, and
-the TTT suffix pass when the mask has one), all through the C ABI.
+the TTT suffix pass when the mask has one), all through the C ABI.  The
+EAGLE3 TTT workload's step is the forward + backward of all seven TTT steps
+(t = 0..6, K/V growing by one segment per step).
 
 Throughput is mask-aware: F = 3.5 * 4 * D * N_vis FLOPs per step, N_vis the
 exact number of visible (q, kv) pairs (forward 2 GEMMs, backward 5).  Inputs
 are seeded N(0,1) draws rounded to bf16 (attention_tcgen05_tmem_gb300.synth).
 
-Prints ONE JSON line on rank 0.  Under torchrun (N > 1) every rank runs the
-same workload on its own GPU (independent replicas; attention needs no
-collective), the timed region is bracketed by barriers and the max over
-ranks is taken.  ``--impl reference`` times the fp64 CPU oracle on the
-host cores on a bounded sample of the same workload instead.
+Prints ONE JSON line on rank 0 (``--all``: one line per workload).  Under
+torchrun (N > 1) every rank runs the same workload on its own GPU
+(independent replicas; attention needs no collective), the timed region is
+bracketed by barriers and the max over ranks is taken.  ``--impl reference``
+times the fp64 CPU oracle on the host cores on a bounded sample of the same
+workload instead.
 """
 from __future__ import annotations
 
@@ -33,20 +36,37 @@ if ROOT not in sys.path:
 METRIC = "attention fwd+bwd TFLOPS (mask-aware, bf16) and % of GB300 tensor peak"
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TTT_ALL = "eagle3_ttt_steps0-6"
+
+
+def bench_workloads():
+    """name -> list of synth.Workload run back to back in one step."""
+    from attention_tcgen05_tmem_gb300 import synth
+    d = {w.name: [w] for w in synth.ALL + synth.PROFILE}
+    d[TTT_ALL] = list(synth.TTT_STEPS)
+    return d
+
+
+def headline_names():
+    from attention_tcgen05_tmem_gb300 import synth
+    return ([synth.TINY.name] + [w.name for w in synth.SWEEP] +
+            [synth.LONG_GQA.name, TTT_ALL, synth.DIT_SELF.name, synth.DIT_CROSS.name])
 
 
 def parse_args():
     from attention_tcgen05_tmem_gb300 import synth
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=synth.LONG_GQA.name,
-                    help="one of: " + ", ".join(w.name for w in synth.ALL))
+                    help="one of: " + ", ".join(bench_workloads()))
+    ap.add_argument("--all", action="store_true", help="one line per workload of the pages")
     ap.add_argument("--out", choices=["fp32", "bf16"], default="fp32",
                     help="dtype of O, dQ, dK, dV (fp32 is the parity-gated configuration)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     return ap.parse_args()
@@ -64,7 +84,7 @@ def load_peaks():
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+    """nvidia-smi samples (every 100 ms) while the timed region runs."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -81,7 +101,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200", "-i", str(self.gpu_index)],
+                 "-lms", "100", "-i", str(self.gpu_index)],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -97,7 +117,7 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         try:
             lines = open(self.path).read().strip().splitlines()
@@ -110,6 +130,7 @@ class ClockSampler:
             try:
                 sm.append(float(parts[1]))
                 mx.append(float(parts[2]))
+                pw.append(float(parts[3]))
             except ValueError:
                 continue
             for n, v in zip(names, parts[5:9]):
@@ -123,46 +144,42 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "power_w_max": max(pw) if pw else None, "samples": len(sm)}
 
 
 # ------------------------------------------------------------- CPU oracle
-def cpu_sample(w, target_s: float, seed_inputs=None):
+def cpu_sample(ws, target_s: float, inputs=None):
     """Time the fp64 oracle (forward + backward) on a bounded sample of the
-    workload: the q heads of the first kv-head groups (at least as many q
-    heads as host threads, so every core has a head) and the last R query rows
-    (the rows with the most visible keys), R sized to ~target_s seconds.
-    Returns (TFLOP/s, description, threads)."""
-    import numpy as np
-
+    workload's first (or only) shape: the q heads of the first kv-head
+    groups (at least as many q heads as host threads) and the last R query
+    rows (those with the most visible keys), R grown until the run takes
+    about target_s seconds.  Returns (TFLOP/s, description, threads)."""
     import oracle
     from attention_tcgen05_tmem_gb300 import flops, synth
 
+    w = ws[-1]  # for TTT: the largest step (most keys per row)
     threads = oracle.num_threads()
     groups = min(w.Hkv, max(1, -(-threads // w.G)))
     hq = groups * w.G
-    x = seed_inputs or synth.make_inputs(w)
+    x = inputs or synth.make_inputs(w)
     q = x["q"][:, :hq].double().numpy()
     k = x["k"][:, :groups].double().numpy()
     v = x["v"][:, :groups].double().numpy()
     do = x["dout"][:, :hq].double().numpy()
     t = w.ttt_step
 
-    def vis_rows(r0, r1):
-        full = flops.visible_pairs_per_head(w.mask, w.Sq, w.Skv, t)
+    def pref(n):  # visible pairs of query rows [0, n) of one head
+        if n <= 0:
+            return 0
         if w.mask == "full":
-            return (r1 - r0) * w.Skv
-        # count rows [r0, r1) in closed form by difference of prefixes
-        def pref(n):
-            if n <= 0:
-                return 0
-            if w.mask == "causal":
-                m = min(n, w.Skv)
-                return m * (m + 1) // 2 + max(0, n - w.Skv) * w.Skv
-            k0 = max(0, n - t)
-            return k0 * (k0 + 1) // 2 + t * n
-        assert pref(w.Sq) == full
-        return pref(r1) - pref(r0)
+            return n * w.Skv
+        if w.mask == "causal":
+            m = min(n, w.Skv)
+            return m * (m + 1) // 2 + max(0, n - w.Skv) * w.Skv
+        k0 = max(0, n - t)
+        return k0 * (k0 + 1) // 2 + t * n
+
+    assert pref(w.Sq) == flops.visible_pairs_per_head(w.mask, w.Sq, w.Skv, t)
 
     def run(R):
         r0 = w.Sq - R
@@ -170,16 +187,18 @@ def cpu_sample(w, target_s: float, seed_inputs=None):
         oracle.fwd(q, k, v, w.mask, t, rows=(r0, w.Sq))
         oracle.bwd(q, k, v, do, w.mask, t, rows=(r0, w.Sq))
         dt = time.perf_counter() - t0
-        f = 14.0 * w.D * w.B * hq * vis_rows(r0, w.Sq)
-        return dt, f
+        return dt, 14.0 * w.D * w.B * hq * (pref(w.Sq) - pref(r0))
 
     R = min(w.Sq, 8)
     dt, f = run(R)
-    if dt < target_s and R < w.Sq:
-        R = int(min(w.Sq, max(R + 1, R * target_s / max(dt, 1e-3))))
+    for _ in range(3):
+        if dt >= 0.5 * target_s or R >= w.Sq:
+            break
+        R = int(min(w.Sq, max(2 * R, R * target_s / max(dt, 1e-3))))
         dt, f = run(R)
-    desc = (f"fp64 oracle fwd+bwd, {w.B} batch x {hq} of {w.Hq} q heads ({groups} kv-head "
-            f"groups), last {R} of {w.Sq} query rows, {f / 1e9:.1f} GFLOP mask-aware, {dt:.1f} s")
+    desc = (f"fp64 oracle fwd+bwd on {w.name}: {w.B} batch x {hq} of {w.Hq} q heads "
+            f"({groups} kv-head groups), last {R} of {w.Sq} query rows, {f / 1e9:.1f} GFLOP "
+            f"mask-aware, {dt:.1f} s")
     return f / dt / 1e12, desc, threads
 
 
@@ -193,234 +212,155 @@ def gpu_index_for(local_rank: int) -> str:
     return str(local_rank)
 
 
-def run_ours(args, w, rank, world, local_rank, dist):
+class Case:
+    """Device buffers and the per-step launch sequence of one shape."""
+
+    def __init__(self, w, dev, out, binding, synth):
+        import torch
+        self.w = w
+        self.b = binding
+        self.x = synth.make_inputs(w)
+        self.q, self.k, self.v, self.do = (self.x[n].to(dev) for n in ("q", "k", "v", "dout"))
+        odt = torch.float32 if out == "fp32" else torch.bfloat16
+        self.p = binding.problem(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.mask, w.ttt_step, 0.0, out)
+        binding.check_supported(self.p)
+        self.o = torch.empty(self.q.shape, dtype=odt, device=dev)
+        self.lse = torch.empty(w.B, w.Hq, w.Sq, dtype=torch.float32, device=dev)
+        self.dq = torch.empty(self.q.shape, dtype=odt, device=dev)
+        self.dk = torch.empty(self.k.shape, dtype=odt, device=dev)
+        self.dv = torch.empty(self.v.shape, dtype=odt, device=dev)
+        self.ws = torch.empty(binding.workspace_size(self.p), dtype=torch.uint8, device=dev)
+        has_ttt = w.mask == "ttt" and w.ttt_step > 0
+        self.passes = [("bwd_prep", binding.BWD_PREP), ("bwd_dkdv", binding.BWD_DKDV),
+                       ("bwd_dq", binding.BWD_DQ)]
+        if has_ttt:
+            self.passes.append(("ttt_diag_bwd", binding.BWD_TTT))
+        self.names = ["fwd"] + [n for n, _ in self.passes]
+
+    def step(self, stream, evs=None):
+        b = self.b
+        if evs:
+            evs[0].record(stream)
+        b.fwd_raw(self.p, self.q, self.k, self.v, self.o, self.lse, stream.cuda_stream)
+        if evs:
+            evs[1].record(stream)
+        for i, (_, m) in enumerate(self.passes):
+            b.bwd_passes_raw(self.p, m, self.q, self.k, self.v, self.o, self.do, self.lse, self.dq,
+                             self.dk, self.dv, self.ws, stream.cuda_stream)
+            if evs:
+                evs[2 + i].record(stream)
+
+
+def run_ours(args, ws, local_rank, dist):
     import torch
 
-    from attention_tcgen05_tmem_gb300 import binding, flops, synth
+    from attention_tcgen05_tmem_gb300 import binding, synth
     from attention_tcgen05_tmem_gb300 import build as lib_build
 
     lib_build.build()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
-    x = synth.make_inputs(w)
-    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
-    odt = torch.float32 if args.out == "fp32" else torch.bfloat16
-    p = binding.problem(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.mask, w.ttt_step, 0.0, args.out)
-    binding.check_supported(p)
-    o = torch.empty(q.shape, dtype=odt, device=dev)
-    lse = torch.empty(w.B, w.Hq, w.Sq, dtype=torch.float32, device=dev)
-    dq = torch.empty(q.shape, dtype=odt, device=dev)
-    dk = torch.empty(k.shape, dtype=odt, device=dev)
-    dv = torch.empty(v.shape, dtype=odt, device=dev)
-    ws = torch.empty(binding.workspace_size(p), dtype=torch.uint8, device=dev)
+    cases = [Case(w, dev, args.out, binding, synth) for w in ws]
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > 129 MB L2
-    has_ttt = w.mask == "ttt" and w.ttt_step > 0
-    passes = [("bwd_prep", binding.BWD_PREP), ("bwd_dkdv", binding.BWD_DKDV),
-              ("bwd_dq", binding.BWD_DQ)] + ([("ttt_diag_bwd", binding.BWD_TTT)] if has_ttt else [])
-    names = ["fwd"] + [n for n, _ in passes]
-
-    def step(evs=None):
-        if evs:
-            evs[0].record(stream)
-        binding.fwd_raw(p, q, k, v, o, lse, stream.cuda_stream)
-        if evs:
-            evs[1].record(stream)
-        for i, (_, m) in enumerate(passes):
-            binding.bwd_passes_raw(p, m, q, k, v, o, do, lse, dq, dk, dv, ws, stream.cuda_stream)
-            if evs:
-                evs[2 + i].record(stream)
 
     for _ in range(max(args.warmup, 3)):
-        step()
+        for c in cases:
+            c.step(stream)
     torch.cuda.synchronize(dev)
     binding.device_status()
 
-    F = flops.flops_fwd_bwd(w)
     K = args.steps
-    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(K)]
+    evsets = [[[torch.cuda.Event(enable_timing=True) for _ in range(len(c.names) + 1)]
+               for c in cases] for _ in range(K)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(gpu_index_for(local_rank)) as clk:
-        t_wall0 = time.perf_counter()
         for i in range(K):
             flush.zero_()  # evict L2 between steps (outside the events)
-            step(evsets[i])
+            for c, evs in zip(cases, evsets[i]):
+                c.step(stream, evs)
         torch.cuda.synchronize(dev)
-        t_wall = time.perf_counter() - t_wall0
     if dist:
         dist.barrier()
     binding.device_status()
-    per_kernel = {n: 0.0 for n in names}
+    per_kernel = {}
     total_ms = 0.0
-    for evs in evsets:
-        total_ms += evs[0].elapsed_time(evs[-1])
-        for j, n in enumerate(names):
-            per_kernel[n] += evs[j].elapsed_time(evs[j + 1])
+    for i in range(K):
+        for c, evs in zip(cases, evsets[i]):
+            total_ms += evs[0].elapsed_time(evs[-1])
+            for j, n in enumerate(c.names):
+                per_kernel[n] = per_kernel.get(n, 0.0) + evs[j].elapsed_time(evs[j + 1])
     clocks = clk.summary()
 
-    # ---- end to end through the C ABI with host buffers
-    pin = {n: x[n].pin_memory() for n in ("q", "k", "v", "dout")}
-    host_out = {"o": torch.empty(o.shape, dtype=odt).pin_memory(),
-                "lse": torch.empty(lse.shape, dtype=torch.float32).pin_memory(),
-                "dq": torch.empty(dq.shape, dtype=odt).pin_memory(),
-                "dk": torch.empty(dk.shape, dtype=odt).pin_memory(),
-                "dv": torch.empty(dv.shape, dtype=odt).pin_memory()}
-    h2d = sum(t.numel() * t.element_size() for t in pin.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
-    dev_out = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+    e2e_ms, h2d, d2h = None, 0, 0
+    if not args.no_e2e:
+        # end to end through the C ABI with pinned host buffers: inputs copied in and all
+        # outputs (O, LSE, dQ, dK, dV) copied out inside the timed region
+        hosts = []
+        for c in cases:
+            pin = {n: c.x[n].pin_memory() for n in ("q", "k", "v", "dout")}
+            outs = {n: torch.empty(getattr(c, n).shape, dtype=getattr(c, n).dtype).pin_memory()
+                    for n in ("o", "lse", "dq", "dk", "dv")}
+            hosts.append((pin, outs))
+            h2d += sum(t.numel() * t.element_size() for t in pin.values())
+            d2h += sum(t.numel() * t.element_size() for t in outs.values())
 
-    def e2e_step():
-        q.copy_(pin["q"], non_blocking=True)
-        k.copy_(pin["k"], non_blocking=True)
-        v.copy_(pin["v"], non_blocking=True)
-        do.copy_(pin["dout"], non_blocking=True)
-        binding.fwd_raw(p, q, k, v, o, lse, stream.cuda_stream)
-        binding.bwd_raw(p, q, k, v, o, do, lse, dq, dk, dv, ws, stream.cuda_stream)
-        for n, t in host_out.items():
-            t.copy_(dev_out[n], non_blocking=True)
+        def e2e_step():
+            for c, (pin, outs) in zip(cases, hosts):
+                c.q.copy_(pin["q"], non_blocking=True)
+                c.k.copy_(pin["k"], non_blocking=True)
+                c.v.copy_(pin["v"], non_blocking=True)
+                c.do.copy_(pin["dout"], non_blocking=True)
+                binding.fwd_raw(c.p, c.q, c.k, c.v, c.o, c.lse, stream.cuda_stream)
+                binding.bwd_raw(c.p, c.q, c.k, c.v, c.o, c.do, c.lse, c.dq, c.dk, c.dv, c.ws,
+                                stream.cuda_stream)
+                for n, t in outs.items():
+                    t.copy_(getattr(c, n), non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    e0.record(stream)
-    for _ in range(K):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1)
-    binding.device_status()
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        Ke = max(3, min(K, 20))
+        e0.record(stream)
+        for _ in range(Ke):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1) / Ke * K
+        binding.device_status()
 
-    # ---- max over ranks
-    vals = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
+    vals = torch.tensor([total_ms, e2e_ms or 0.0], dtype=torch.float64, device=dev)
     if dist:
         dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    total_ms, e2e_ms = float(vals[0]), float(vals[1])
-    result = {
-        "F": F, "K": K, "total_ms": total_ms, "e2e_ms": e2e_ms, "per_kernel_ms": per_kernel,
-        "clocks": clocks, "wall_s": t_wall, "h2d": h2d, "d2h": d2h,
-        "launches_per_step": len(names), "names": names,
-    }
-    return result
+    return {"K": K, "total_ms": float(vals[0]), "e2e_ms": float(vals[1]) if e2e_ms else None,
+            "per_kernel_ms": per_kernel, "clocks": clocks, "h2d": h2d, "d2h": d2h,
+            "launches_per_step": sum(len(c.names) for c in cases)}
 
 
-def kernel_flops(w, name):
-    """Algorithmic FLOPs of one launch of each kernel: the tensor-core work the
-    kernel must do on exactly the visible pairs it owns (2*D per pair and
-    GEMM): forward 2 GEMMs; dK/dV 4 (S^T recompute, dP^T, dV, dK) on the tiled
-    part; dQ 3 (S recompute, dP, dQ); the TTT suffix pass 4 on the diagonal
-    pairs."""
+def kernel_flops(ws, name):
+    """Algorithmic FLOPs of one step of each kernel: the tensor-core work it
+    must do on exactly the visible pairs it owns (2*D per pair and GEMM):
+    forward 2 GEMMs; dK/dV 4 (S^T recompute, dP^T, dV, dK) on the tiled part;
+    dQ 3 (S recompute, dP, dQ); the TTT suffix pass 4 on the diagonal pairs."""
     from attention_tcgen05_tmem_gb300 import flops
-    nvis = flops.visible_pairs(w)
-    ndiag = w.B * w.Hq * (w.ttt_step * w.Sq if w.mask == "ttt" else 0)
-    ntiled = nvis - ndiag
-    return {"fwd": 4 * w.D * nvis, "bwd_dkdv": 8 * w.D * ntiled, "bwd_dq": 6 * w.D * nvis,
-            "ttt_diag_bwd": 8 * w.D * ndiag, "bwd_prep": 0}[name]
+    tot = 0
+    for w in ws:
+        nvis = flops.visible_pairs(w)
+        ndiag = w.B * w.Hq * (w.ttt_step * w.Sq if w.mask == "ttt" else 0)
+        per = {"fwd": 4 * nvis, "bwd_dkdv": 8 * (nvis - ndiag), "bwd_dq": 6 * nvis,
+               "ttt_diag_bwd": 8 * ndiag, "bwd_prep": 0}[name]
+        tot += per * w.D
+    return tot
 
 
-def kernel_bytes(w, name, out_bytes):
-    if name == "bwd_prep":
-        return w.B * w.Hq * w.Sq * (w.D * (out_bytes + 2) + 4)
-    return 0
-
-
-def main():
-    args = parse_args()
-    from attention_tcgen05_tmem_gb300 import flops, synth
-    w = synth.by_name(args.workload)
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    n_gpus = max(world, 1)
-    config = dict(w.describe())
-    config.update({"outputs": args.out, "l2": "flushed between steps (256 MiB write)",
-                   "parallelism": f"replicas x{n_gpus}"})
-    F = flops.flops_fwd_bwd(w)
-
-    if args.impl == "reference":
-        if rank != 0:
-            return 0
-        per = []
-        desc, threads = "", 1
-        x = synth.make_inputs(w)
-        for i in range(args.warmup + args.steps):
-            tf, desc, threads = cpu_sample(w, 4.0, x)
-            if i >= args.warmup:
-                per.append(tf)
-        value = statistics.median(per)
-        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
-                "n_gpus": n_gpus, "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": F / (value * 1e12) * 1e3, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": config,
-                "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                                 "sample": desc},
-                "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
-                        "d2h_bytes_per_step": 0}}
-        print(json.dumps(line), flush=True)
-        return 0
-
-    dist = None
-    if world > 1:
-        import torch
-        import torch.distributed as tdist
-        torch.cuda.set_device(local_rank)
-        tdist.init_process_group("nccl")
-        dist = tdist
-    r = run_ours(args, w, rank, world, local_rank, dist)
-    peaks, peak_src = load_peaks()
-    K = r["K"]
-    value = n_gpus * F * K / (r["total_ms"] * 1e-3) / 1e12
-    e2e_value = n_gpus * F * K / (r["e2e_ms"] * 1e-3) / 1e12
-    pk = r["per_kernel_ms"]
-    dom = max(pk, key=lambda n: pk[n])
-    dom_ms = pk[dom] / K
-    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    if dom == "bwd_prep":
-        ach = kernel_bytes(w, dom, 4 if args.out == "fp32" else 2) / (dom_ms * 1e-3) / 1e9
-        pk_hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-        roof = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": pk_hbm, "unit": "GB/s",
-                "frac": ach / pk_hbm, "traffic": None}
-    else:
-        ach = kernel_flops(w, dom) / (dom_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak_sus,
-                "unit": "TFLOP/s", "frac": ach / peak_sus, "traffic": None,
-                "peak_kind": f"bf16 sustained, of {peak_src}"}
-    traffic = load_traffic(w.name, dom)
-    if traffic is not None:
-        roof["traffic"] = traffic
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": n_gpus, "steps": K,
-        "warmup": args.warmup, "ms_per_step": r["total_ms"] / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config,
-        "pct_of_peak": {"bf16_burst": value / n_gpus / peak_burst,
-                        "bf16_sustained": value / n_gpus / peak_sus, "source": peak_src},
-        "fwd_tflops": flops.flops_fwd(w) / (pk["fwd"] / K * 1e-3) / 1e12,
-        "bwd_tflops": flops.flops_bwd(w) / (sum(v for n, v in pk.items() if n != "fwd") / K * 1e-3) / 1e12,
-        "kernel_ms": {n: v / K for n, v in pk.items()},
-        "roofline": roof,
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": r["h2d"],
-                "d2h_bytes_per_step": r["d2h"]},
-        "gpu_launches": r["launches_per_step"] * K,
-        "clocks": r["clocks"],
-    }
-    if rank == 0 and n_gpus == 1 and not args.no_cpu_baseline:
-        tf, desc, threads = cpu_sample(w, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": threads, "kind": "oracle",
-                                "sample": desc}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if dist:
-        dist.barrier()
-        dist.destroy_process_group()
-    return 0
+def prep_bytes(ws, out_bytes):
+    return sum(w.B * w.Hq * w.Sq * (w.D * (out_bytes + 2) + 4) for w in ws)
 
 
 def kernel_source_sha() -> str:
@@ -449,6 +389,118 @@ def load_traffic(workload: str, kernel: str):
     if not ent or ent.get("src_sha") != kernel_source_sha():
         return None
     return ent.get("bytes")
+
+
+def describe(name, ws, out, n_gpus):
+    cfg = dict(ws[0].describe()) if len(ws) == 1 else {
+        "workload": name, "B": ws[0].B, "Hq": ws[0].Hq, "Hkv": ws[0].Hkv, "Sq": ws[0].Sq,
+        "Skv": [w.Skv for w in ws], "D": ws[0].D, "mask": ws[0].mask,
+        "ttt_steps": [w.ttt_step for w in ws]}
+    cfg["workload"] = name
+    cfg.update({"outputs": out, "l2": "flushed between steps (256 MiB write)",
+                "parallelism": f"replicas x{n_gpus}"})
+    return cfg
+
+
+def main():
+    args = parse_args()
+    from attention_tcgen05_tmem_gb300 import flops
+    table = bench_workloads()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    n_gpus = max(world, 1)
+    names = headline_names() if args.all else [args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        for name in names:
+            ws = table[name]
+            F = sum(flops.flops_fwd_bwd(w) for w in ws)
+            per, desc, threads = [], "", 1
+            from attention_tcgen05_tmem_gb300 import synth
+            x = synth.make_inputs(ws[-1])
+            for i in range(args.warmup + args.steps):
+                tf, desc, threads = cpu_sample(ws, 4.0, x)
+                if i >= args.warmup:
+                    per.append(tf)
+            value = statistics.median(per)
+            line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+                    "n_gpus": n_gpus, "steps": args.steps, "warmup": args.warmup,
+                    "ms_per_step": F / (value * 1e12) * 1e3, "higher_is_better": True,
+                    "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                    "config": describe(name, ws, args.out, n_gpus),
+                    "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads,
+                                     "kind": "oracle", "sample": desc},
+                    "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                            "d2h_bytes_per_step": 0}}
+            print(json.dumps(line), flush=True)
+        return 0
+
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(local_rank)
+        tdist.init_process_group("nccl")
+        dist = tdist
+    peaks, peak_src = load_peaks()
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    for name in names:
+        ws = table[name]
+        F = sum(flops.flops_fwd_bwd(w) for w in ws)
+        r = run_ours(args, ws, local_rank, dist)
+        K = r["K"]
+        value = n_gpus * F * K / (r["total_ms"] * 1e-3) / 1e12
+        pk = r["per_kernel_ms"]
+        dom = max(pk, key=lambda n: pk[n])
+        dom_ms = pk[dom] / K
+        if dom == "bwd_prep":
+            ach = prep_bytes(ws, 4 if args.out == "fp32" else 2) / (dom_ms * 1e-3) / 1e9
+            roof = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peak_hbm,
+                    "unit": "GB/s", "frac": ach / peak_hbm, "traffic": None,
+                    "peak_kind": f"HBM copy, of {peak_src}"}
+        else:
+            ach = kernel_flops(ws, dom) / (dom_ms * 1e-3) / 1e12
+            roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak_sus,
+                    "unit": "TFLOP/s", "frac": ach / peak_sus, "traffic": None,
+                    "peak_kind": f"bf16 sustained, of {peak_src}"}
+        traffic = load_traffic(name, dom)
+        if traffic is not None:
+            roof["traffic"] = traffic
+        alg_bytes = sum(flops.bytes_fwd(w) + flops.bytes_bwd(w) for w in ws)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": n_gpus, "steps": K,
+            "warmup": args.warmup, "ms_per_step": r["total_ms"] / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": describe(name, ws, args.out, n_gpus),
+            "pct_of_peak": {"bf16_burst": value / n_gpus / peak_burst,
+                            "bf16_sustained": value / n_gpus / peak_sus, "source": peak_src},
+            "fwd_tflops": sum(flops.flops_fwd(w) for w in ws) / (pk["fwd"] / K * 1e-3) / 1e12,
+            "bwd_tflops": sum(flops.flops_bwd(w) for w in ws) /
+                          (sum(v for n, v in pk.items() if n != "fwd") / K * 1e-3) / 1e12,
+            "hbm_gbs_algorithmic": alg_bytes / (r["total_ms"] / K * 1e-3) / 1e9,
+            "kernel_ms": {n: v / K for n, v in pk.items()},
+            "roofline": roof,
+            "gpu_launches": r["launches_per_step"] * K,
+            "clocks": r["clocks"],
+        }
+        if r["e2e_ms"]:
+            line["e2e"] = {"value": n_gpus * F * K / (r["e2e_ms"] * 1e-3) / 1e12, "unit": UNIT,
+                           "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]}
+        if rank == 0 and n_gpus == 1 and not args.no_cpu_baseline:
+            tf, desc, threads = cpu_sample(ws, args.cpu_seconds)
+            line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                    "sample": desc}
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
 
 
 if __name__ == "__main__":
