@@ -182,10 +182,17 @@ View to_view(const attn_tensor& t) {
   return v;
 }
 
-size_t ws_bytes_for(const attn_problem* p) {
-  const size_t delta = (size_t)p->B * p->Hq * p->Sq * sizeof(float);
-  return (delta + 255) & ~(size_t)255;
+// Workspace: Delta [B, Hq, Sq] fp32, then for TTT steps t > 0 the per-row
+// suffix-diagonal weights p and score gradients ds, [B, Hq, Sq, t] fp32 each.
+size_t ws_round(size_t n) { return (n + 255) & ~(size_t)255; }
+size_t ws_delta_bytes(const attn_problem* p) {
+  return ws_round((size_t)p->B * p->Hq * p->Sq * sizeof(float));
 }
+size_t ws_diag_bytes(const attn_problem* p) {
+  const int t = p->mask == ATTN_MASK_TTT ? p->ttt_step : 0;
+  return ws_round((size_t)p->B * p->Hq * p->Sq * (size_t)t * sizeof(float));
+}
+size_t ws_bytes_for(const attn_problem* p) { return ws_delta_bytes(p) + 2 * ws_diag_bytes(p); }
 
 // ------------------------------------------- built-in scratch (no-alloc bwd)
 // Scratch for attn_train_bwd_noalloc: the backward's only scratch is the
@@ -314,6 +321,13 @@ attn_status attn_train_bwd_passes(const attn_problem* p, unsigned passes, attn_t
   a.dv = to_view(dv);
   a.lse = lse;
   a.delta = static_cast<float*>(workspace);
+  a.ttt_p = nullptr;
+  a.ttt_ds = nullptr;
+  if (ws_diag_bytes(p) > 0) {
+    char* w = static_cast<char*>(workspace) + ws_delta_bytes(p);
+    a.ttt_p = reinterpret_cast<float*>(w);
+    a.ttt_ds = reinterpret_cast<float*>(w + ws_diag_bytes(p));
+  }
   if ((st = device_error_word(&a.ctl.err)) != ATTN_OK) return st;
   a.ctl.budget_ns = g_budget_ns.load();
   attn::Maps m;

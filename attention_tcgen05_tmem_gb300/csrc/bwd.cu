@@ -56,7 +56,25 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 
 
 // ===================================================================== prep
-// Delta[b, h, q] = sum_d dO * O.  D/8 threads per row, 16-byte loads.
+// Dot product of two 8-element bf16 chunks (fp32 accumulate).
+__device__ __forceinline__ float dot8(const uint4& x, const uint4& y) {
+  const __nv_bfloat162* xv = reinterpret_cast<const __nv_bfloat162*>(&x);
+  const __nv_bfloat162* yv = reinterpret_cast<const __nv_bfloat162*>(&y);
+  float acc = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 xf = __bfloat1622float2(xv[e]);
+    const float2 yf = __bfloat1622float2(yv[e]);
+    acc = fmaf(xf.x, yf.x, acc);
+    acc = fmaf(xf.y, yf.y, acc);
+  }
+  return acc;
+}
+
+// Delta[b, h, q] = sum_d dO * O.  D/8 threads per row, 16-byte loads.  For a
+// TTT step t > 0 the same row group also computes, for each suffix diagonal
+// i = 1..t (key row i*Sq + q), p_i = exp(c q.k_i - LSE) and
+// ds_i = p_i (dO.v_i - Delta), for the dQ epilogue and the suffix-key pass.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdArgs a) {
   constexpr int TPR = D / 8;  // threads per row
@@ -64,13 +82,17 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdArgs a) {
   const int64_t total = (int64_t)a.d.B * a.d.Hq * a.d.Sq;
   const int64_t row = (int64_t)blockIdx.x * RPB + threadIdx.x / TPR;
   const int sub = threadIdx.x % TPR;
+  const bool in = row < total;
   float acc = 0.f;
-  if (row < total) {
-    const int q = (int)(row % a.d.Sq);
+  int q = 0, h = 0, b = 0;
+  uint4 ga = make_uint4(0u, 0u, 0u, 0u);
+  if (in) {
+    q = (int)(row % a.d.Sq);
     const int bh = (int)(row / a.d.Sq);
-    const int h = bh % a.d.Hq, b = bh / a.d.Hq;
+    h = bh % a.d.Hq;
+    b = bh / a.d.Hq;
     const __nv_bfloat16* g = row_ptr(a.dout, b, h, q) + sub * 8;
-    const uint4 ga = *reinterpret_cast<const uint4*>(g);
+    ga = *reinterpret_cast<const uint4*>(g);
     const __nv_bfloat162* gv = reinterpret_cast<const __nv_bfloat162*>(&ga);
     float of[8];
     if (a.d.out_f32) {
@@ -99,7 +121,36 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdArgs a) {
   }
 #pragma unroll
   for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, TPR);
-  if (row < total && sub == 0) a.delta[row] = acc;
+  if (in && sub == 0) a.delta[row] = acc;
+
+  const int t = a.d.geom.ttt;  // uniform over the grid
+  if (t > 0) {
+    const int hk = h / a.d.G;
+    uint4 qa = make_uint4(0u, 0u, 0u, 0u);
+    float lse2 = 0.f;
+    if (in) {
+      qa = *reinterpret_cast<const uint4*>(row_ptr(a.q, b, h, q) + sub * 8);
+      lse2 = a.lse[row] * kLog2e;
+    }
+    for (int i = 1; i <= t; ++i) {
+      float s = 0.f, dp = 0.f;
+      if (in) {
+        const int64_t kr = (int64_t)i * a.d.Sq + q;
+        s = dot8(qa, *reinterpret_cast<const uint4*>(row_ptr(a.k, b, hk, kr) + sub * 8));
+        dp = dot8(ga, *reinterpret_cast<const uint4*>(row_ptr(a.v, b, hk, kr) + sub * 8));
+      }
+#pragma unroll
+      for (int off = TPR / 2; off > 0; off >>= 1) {
+        s += __shfl_xor_sync(0xffffffffu, s, off, TPR);
+        dp += __shfl_xor_sync(0xffffffffu, dp, off, TPR);
+      }
+      if (in && sub == 0) {
+        const float p = ex2_approx(fmaf(s, a.d.scale_log2, -lse2));
+        a.ttt_p[row * t + (i - 1)] = p;
+        a.ttt_ds[row * t + (i - 1)] = p * (dp - acc);
+      }
+    }
+  }
 }
 
 // ===================================================================== dK/dV
@@ -678,22 +729,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c0 = 16 * wg; c0 < D; c0 += 32) tmem_st16(tq + c0, z);
         tmem_st_wait();
       }
-      // TTT suffix diagonals: ds_i = p_i (dO . v_i - Delta), dQ += ds_i k_i, folded into
-      // the TMEM accumulator kDiagBatch diagonals at a time
-      const __nv_bfloat16* qrow = row_ptr(a.q, b, h, q);
-      const __nv_bfloat16* dorow = row_ptr(a.dout, b, h, q);
+      // TTT suffix diagonals: dQ += ds_i k_i with ds_i = p_i (dO . v_i - Delta) from the
+      // prep pass, folded into the TMEM accumulator kDiagBatch diagonals at a time
       for (int i0 = 1; i0 <= g.ttt; i0 += kDiagBatch) {
         float dsv[kDiagBatch];
 #pragma unroll
-        for (int u = 0; u < kDiagBatch; ++u) {
-          dsv[u] = 0.f;
-          if (qin && i0 + u <= g.ttt) {
-            const int64_t kr = (int64_t)(i0 + u) * d.Sq + q;
-            const float sv = dot_rows<D>(qrow, row_ptr(a.k, b, hk, kr));
-            const float dp = dot_rows<D>(dorow, row_ptr(a.v, b, hk, kr));
-            dsv[u] = ex2_approx(fmaf(sv, sl2, -lse2)) * (dp - delta);
-          }
-        }
+        for (int u = 0; u < kDiagBatch; ++u)
+          dsv[u] = (qin && i0 + u <= g.ttt) ? a.ttt_ds[rrow * g.ttt + (i0 + u - 1)] : 0.f;
         for (int c0 = 16 * wg; c0 < D; c0 += 32) {
           uint32_t raw[16];
           tmem_ld16(tq + c0, raw);
@@ -762,43 +804,27 @@ __global__ void __launch_bounds__(256) ttt_diag_bwd_kernel(const BwdArgs a) {
   const int hk = (int)(rest % d.Hkv);
   const int b = (int)(rest / d.Hkv);
   const int64_t kr = (int64_t)i * d.Sq + r;
-  const __nv_bfloat16* krow = row_ptr(a.k, b, hk, kr);
-  const __nv_bfloat16* vrow = row_ptr(a.v, b, hk, kr);
-  float kf[EPL], vf[EPL], dk[EPL], dv[EPL];
+  float dk[EPL], dv[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) {
-    const int c = lane + 32 * e;
-    kf[e] = c < D ? __bfloat162float(krow[c]) : 0.f;
-    vf[e] = c < D ? __bfloat162float(vrow[c]) : 0.f;
     dk[e] = 0.f;
     dv[e] = 0.f;
   }
+  // p and ds of (query row r of q head h, diagonal i) come from the prep pass
   for (int gq = 0; gq < d.G; ++gq) {
     const int h = hk * d.G + gq;
+    const int64_t rrow = ((int64_t)b * d.Hq + h) * d.Sq + r;
+    const float p = a.ttt_p[rrow * t + (i - 1)];
+    const float ds = a.ttt_ds[rrow * t + (i - 1)];
     const __nv_bfloat16* qrow = row_ptr(a.q, b, h, r);
     const __nv_bfloat16* dorow = row_ptr(a.dout, b, h, r);
-    float qf[EPL], gf[EPL];
-    float s = 0.f, dp = 0.f;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) {
       const int c = lane + 32 * e;
-      qf[e] = c < D ? __bfloat162float(qrow[c]) : 0.f;
-      gf[e] = c < D ? __bfloat162float(dorow[c]) : 0.f;
-      s = fmaf(qf[e], kf[e], s);
-      dp = fmaf(gf[e], vf[e], dp);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      s += __shfl_xor_sync(0xffffffffu, s, off);
-      dp += __shfl_xor_sync(0xffffffffu, dp, off);
-    }
-    const int64_t rrow = ((int64_t)b * d.Hq + h) * d.Sq + r;
-    const float p = ex2_approx(fmaf(s, d.scale_log2, -a.lse[rrow] * kLog2e));
-    const float ds = p * (dp - a.delta[rrow]);
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      dv[e] = fmaf(p, gf[e], dv[e]);
-      dk[e] = fmaf(ds, qf[e], dk[e]);
+      if (c < D) {
+        dv[e] = fmaf(p, __bfloat162float(dorow[c]), dv[e]);
+        dk[e] = fmaf(ds, __bfloat162float(qrow[c]), dk[e]);
+      }
     }
   }
   const int64_t koff = b * a.dk.sb + hk * a.dk.sh + kr * a.dk.ss;

@@ -44,6 +44,59 @@ namespace {
 constexpr int kFwdThreads = 384;
 constexpr float kRescaleThreshold = 8.0f;
 
+// The TTT suffix-diagonal scores of a query row (t fp32 values) are parked in
+// that row of O between the scores pre-pass and the main kernel when they fit.
+__host__ __device__ inline bool ttt_scores_fit(int t, int D, int out_f32) {
+  return t > 0 && t * 4 <= D * (out_f32 ? 4 : 2);
+}
+
+// Scores pre-pass: for every query row q and suffix diagonal i = 1..t (key
+// row i*Sq + q), c log2(e) q . k_i, written as fp32 into the first t slots of
+// the row's O storage.  D/8 threads per row, 16-byte loads, shuffle reduction.
+template <int D>
+__global__ void __launch_bounds__(256) ttt_scores_kernel(const FwdArgs a) {
+  constexpr int TPR = D / 8;
+  constexpr int RPB = 256 / TPR;
+  const Dims& d = a.d;
+  const int t = d.geom.ttt;
+  const int64_t total = (int64_t)d.B * d.Hq * d.Sq;
+  const int64_t row = (int64_t)blockIdx.x * RPB + threadIdx.x / TPR;
+  const int sub = threadIdx.x % TPR;
+  const bool in = row < total;
+  int q = 0, h = 0, b = 0;
+  uint4 qa = make_uint4(0u, 0u, 0u, 0u);
+  if (in) {
+    q = (int)(row % d.Sq);
+    const int bh = (int)(row / d.Sq);
+    h = bh % d.Hq;
+    b = bh / d.Hq;
+    qa = *reinterpret_cast<const uint4*>(row_ptr(a.q, b, h, q) + sub * 8);
+  }
+  const int hk = h / d.G;
+  float* parked = reinterpret_cast<float*>(static_cast<char*>(a.o.ptr) +
+                                           (b * a.o.sb + h * a.o.sh + (int64_t)q * a.o.ss) *
+                                               (d.out_f32 ? 4 : 2));
+  for (int i = 1; i <= t; ++i) {
+    float s = 0.f;
+    if (in) {
+      const uint4 ka =
+          *reinterpret_cast<const uint4*>(row_ptr(a.k, b, hk, (int64_t)i * d.Sq + q) + sub * 8);
+      const __nv_bfloat162* qv = reinterpret_cast<const __nv_bfloat162*>(&qa);
+      const __nv_bfloat162* kv = reinterpret_cast<const __nv_bfloat162*>(&ka);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 qf = __bfloat1622float2(qv[e]);
+        const float2 kf = __bfloat1622float2(kv[e]);
+        s = fmaf(qf.x, kf.x, s);
+        s = fmaf(qf.y, kf.y, s);
+      }
+    }
+#pragma unroll
+    for (int off = TPR / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off, TPR);
+    if (in && sub == 0) parked[i - 1] = s * d.scale_log2;
+  }
+}
+
 template <int D>
 struct FwdLayout {
   using TG = TileGeom<D>;
@@ -136,6 +189,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
+  const bool scores_parked = ttt_scores_fit(g.ttt, D, d.out_f32);
   if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
@@ -366,10 +420,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tmem_st_wait();
         }
         const __nv_bfloat16* qrow = row_ptr(a.q, b, h, q);
+        // scaled score c log2(e) q . k_i of diagonal i: parked in this row of O by the
+        // scores pre-pass when it fits there (read before this thread writes the row)
+        const float* parked = reinterpret_cast<const float*>(
+            static_cast<const char*>(a.o.ptr) +
+            (b * a.o.sb + h * a.o.sh + (int64_t)q * a.o.ss) * (d.out_f32 ? 4 : 2));
+        auto diag_score = [&](int i) {
+          return scores_parked ? parked[i - 1]
+                               : dot_rows<D>(qrow, row_ptr(a.k, b, hk, (int64_t)i * d.Sq + q)) * sl2;
+        };
         float m_star = m_run;  // pass 1: the merged running max
         if (qin)
-          for (int i = 1; i <= g.ttt; ++i)
-            m_star = fmaxf(m_star, dot_rows<D>(qrow, row_ptr(a.k, b, hk, (int64_t)i * d.Sq + q)) * sl2);
+          for (int i = 1; i <= g.ttt; ++i) m_star = fmaxf(m_star, diag_score(i));
         const float alpha = (m_run == neg_inf()) ? 0.f : ex2_approx(m_run - m_star);
         l_run *= alpha;
         // pass 2: O = alpha O + sum_i w_i v_i, kDiagBatch diagonals per TMEM round trip
@@ -379,8 +441,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int u = 0; u < kDiagBatch; ++u) {
             w[u] = 0.f;
             if (qin && i0 + u <= g.ttt) {
-              const int64_t kr = (int64_t)(i0 + u) * d.Sq + q;
-              w[u] = ex2_approx(fmaf(dot_rows<D>(qrow, row_ptr(a.k, b, hk, kr)), sl2, -m_star));
+              w[u] = ex2_approx(diag_score(i0 + u) - m_star);
               l_run += w[u];
             }
           }
@@ -443,6 +504,12 @@ cudaError_t launch_fwd_d(const FwdArgs& a, const Maps& m, cudaStream_t s) {
   if (regs_ok != cudaSuccess) return regs_ok;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
+  if (ttt_scores_fit(a.d.geom.ttt, D, a.d.out_f32)) {
+    constexpr int RPB = 256 / (D / 8);
+    const int64_t rows = (int64_t)a.d.B * a.d.Hq * a.d.Sq;
+    ttt_scores_kernel<D><<<(unsigned)((rows + RPB - 1) / RPB), 256, 0, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   const int n_qp = cdiv(a.d.Sq, 2 * kBM);
   const unsigned grid = (unsigned)(n_qp * a.d.B * a.d.Hq);
   kern<<<grid, kFwdThreads, L::ALLOC, s>>>(m.q, m.k, m.v, a);

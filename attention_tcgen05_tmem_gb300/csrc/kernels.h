@@ -41,6 +41,10 @@ struct BwdArgs {
   View q, k, v, o, dout, dq, dk, dv;
   const float* lse;  // [B, Hq, Sq]
   float* delta;      // workspace [B, Hq, Sq]
+  // TTT only (else null): per query row, the weight p_i and the score
+  // gradient ds_i of its suffix diagonal i = 1..t, workspace [B, Hq, Sq, t]
+  float* ttt_p;
+  float* ttt_ds;
   Ctl ctl;
 };
 

@@ -112,7 +112,9 @@ typedef struct {
 attn_status attn_train_supports(const attn_problem* p);
 
 /* Bytes of device workspace attn_train_bwd needs: the fp32 Delta row
- * statistic, B * Hq * Sq * 4 bytes rounded up to 256. */
+ * statistic, B * Hq * Sq * 4 bytes rounded up to 256; for a TTT step t > 0
+ * also the per-row weight and score gradient of each suffix diagonal,
+ * 2 * B * Hq * Sq * t * 4 bytes (each part rounded up to 256).  Linear in S. */
 attn_status attn_train_workspace_size(const attn_problem* p, size_t* bytes);
 
 /* Forward.  Inputs q [B,Hq,Sq,D], k and v [B,Hkv,Skv,D]; outputs o

@@ -71,6 +71,9 @@ def test_workspace_size(lib):
     assert binding.workspace_size(p) == ((2 * 3 * 100 * 4 + 255) // 256) * 256
     p = binding.problem(1, 32, 4, 16384, 16384, 128, "causal")
     assert binding.workspace_size(p) == 32 * 16384 * 4  # linear in S
+    # TTT step t: Delta plus per-row weight and score gradient of each diagonal
+    p = binding.problem(1, 32, 8, 8192, 7 * 8192, 128, "ttt", 6)
+    assert binding.workspace_size(p) == 32 * 8192 * 4 * (1 + 2 * 6)
 
 
 def _t(ptr=0x1000, sb=4 * 256 * 64, sh=256 * 64, ss=64):
