@@ -385,20 +385,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       uint32_t raw[64];
       tmem_ld32x2(tS, tS + 32, raw);
-      // keys see queries q >= kv + shift (non-full masks); rows past Sq have lse2 = inf
-      const bool full = tile_is_full(g, q0, k0);
-      const int cmin = (g.kind == kMaskFull) ? 0 : kv + g.shift - q0 - 64 * wg;
+      // keys see queries q >= kv + shift (non-full masks); rows past Sq have lse2 = inf.
+      // Masked scores go to -inf (exponential 0) in a pass of its own, so that the
+      // exponential loop of full tiles carries no per-element select.
+      if (!tile_is_full(g, q0, k0)) {
+        const int cmin = (g.kind == kMaskFull) ? 0 : kv + g.shift - q0 - 64 * wg;
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c < cmin) raw[c] = __float_as_uint(-INFINITY);
+      }
       float p[64];
 #pragma unroll
       for (int c = 0; c < 64; c += 4) {
         const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float v = ex2_approx(fmaf(__uint_as_float(raw[c + e]), sl2, -lv[e]));
-          if (!full && c + e < cmin) v = 0.f;
-          p[c + e] = v;
-        }
+        p[c + 0] = ex2_approx(fmaf(__uint_as_float(raw[c + 0]), sl2, -l4.x));
+        p[c + 1] = ex2_approx(fmaf(__uint_as_float(raw[c + 1]), sl2, -l4.y));
+        p[c + 2] = ex2_approx(fmaf(__uint_as_float(raw[c + 2]), sl2, -l4.z));
+        p[c + 3] = ex2_approx(fmaf(__uint_as_float(raw[c + 3]), sl2, -l4.w));
       }
       uint32_t pk[32];
 #pragma unroll
@@ -478,8 +481,8 @@ struct DqLayout {
   static constexpr int K_OFF = 2 * TG::TILE_BYTES;
   static constexpr int V_OFF = K_OFF + NK * TG::TILE_BYTES;
   static constexpr int BAR_OFF = V_OFF + NV * TG::TILE_BYTES;
-  // qdo_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full, dp_full, sdp_used,
-  // ds_ready, ds_free, done, drain
+  // qdo_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2], dp_full,
+  // dp_free, ds_ready, done, drain
   static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 7;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int BYTES = MISC_OFF + 16;
@@ -496,7 +499,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   using TG = TileGeom<D>;
   using L = DqLayout<D>;
   constexpr int NK = L::NK, NV = L::NV;
-  constexpr int T_S = 0, T_DP = 128, T_DQ = 256, T_DS = 384;
+  // tensor memory: S in two buffers (S(j) in buffer j % 2), dP, the dQ
+  // accumulator.  Once the elementwise warps have read S(j), its buffer takes
+  // dS(j) (bf16) as the A operand of dQ += dS K, so that dP(j+1) can be
+  // computed as soon as dP(j) has been read and S(j+1) long before it is needed.
+  constexpr int T_S = 0, T_DP = 256, T_DQ = 384;
   extern __shared__ uint8_t smem_raw[];
   if (*reinterpret_cast<volatile uint32_t*>(a.ctl.err) != 0) return;
 
@@ -507,12 +514,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* k_empty = k_full + NK;
   uint64_t* v_full = k_empty + NK;
   uint64_t* v_empty = v_full + NV;
-  uint64_t* s_full = v_empty + NV;
-  uint64_t* dp_full = s_full + 1;
-  uint64_t* sdp_used = dp_full + 1;
-  uint64_t* ds_ready = sdp_used + 1;
-  uint64_t* ds_free = ds_ready + 1;
-  uint64_t* done = ds_free + 1;
+  uint64_t* s_full = v_empty + NV;  // [2]
+  uint64_t* dp_full = s_full + 2;
+  uint64_t* dp_free = dp_full + 1;
+  uint64_t* ds_ready = dp_free + 1;
+  uint64_t* done = ds_ready + 1;
   uint64_t* drain = done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
@@ -547,11 +553,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    mbar_init(s_full, 1);
+    for (int x = 0; x < 2; ++x) mbar_init(&s_full[x], 1);
     mbar_init(dp_full, 1);
-    mbar_init(sdp_used, 256);
-    mbar_init(ds_ready, 256);
-    mbar_init(ds_free, 1);
+    mbar_init(dp_free, 8);  // one arrival per elementwise warp
+    mbar_init(ds_ready, 8);
     mbar_init(done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -608,51 +613,79 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dVk = TG::kmajor_base(smem_u32(smem + L::V_OFF));   // V slot 0, K-major
       auto kslot = [](int j) { return TG::bytes((j % NK) * TG::TILE_BYTES); };
       auto vslot = [](int j) { return TG::bytes((j % NV) * TG::TILE_BYTES); };
-      auto issue_dq = [&](int jp, bool acc) {  // dQ += dS K
-        const uint64_t kd = dKm + kslot(jp);
+      // dS(j) (bf16) of keys 16kk.. sits in S buffer j % 2, in the columns of warpgroup
+      // kk/4: 64 (kk/4) + 8 (kk%4)
+      auto issue_dq = [&](int j) {  // dQ += dS(j) K_j
+        const uint64_t kd = dKm + kslot(j);
+        const uint32_t ta = tmem + T_S + 128 * (j & 1);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          umma_ts(tmem + T_DQ, tmem + T_DS + 8 * kk, kd + TG::mnmajor_step(kk), idesc_g,
-                  (acc || kk > 0) ? 1u : 0u);
+          umma_ts(tmem + T_DQ, ta + 64 * (kk / 4) + 8 * (kk % 4), kd + TG::mnmajor_step(kk),
+                  idesc_g, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&k_empty[j % NK]);
       };
-      bool ok = mbar_wait(qdo_full, 0, ctl);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        ATTN_TR(1, 0, j);
-        ok = mbar_wait(&k_full[j % NK], (uint32_t)(j / NK) & 1u, ctl) &&
-             mbar_wait(&v_full[j % NV], (uint32_t)(j / NV) & 1u, ctl);
-        ATTN_TR(1, 1, j);
-        if (ok && j > 0) ok = mbar_wait(sdp_used, (uint32_t)(j - 1) & 1u, ctl);
-        if (!ok) break;
-        ATTN_TR(1, 2, j);
-        tc_fence_after();
-        const uint64_t kd = dKk + kslot(j), vd = dVk + vslot(j);
+      auto issue_s = [&](int j) {  // S(j) = Q K_j^T into buffer j % 2
+        const uint64_t kd = dKk + kslot(j);
 #pragma unroll
         for (int kk = 0; kk < TG::KSTEPS; ++kk)
-          umma_ss(tmem + T_S, dQd + TG::kmajor_step(kk), kd + TG::kmajor_step(kk), idesc_s, kk > 0);
-        umma_commit(s_full);
+          umma_ss(tmem + T_S + 128 * (j & 1), dQd + TG::kmajor_step(kk),
+                  kd + TG::kmajor_step(kk), idesc_s, kk > 0);
+        umma_commit(&s_full[j & 1]);
+      };
+      auto issue_dp = [&](int j) {  // dP(j) = dO V_j^T
+        const uint64_t vd = dVk + vslot(j);
 #pragma unroll
         for (int kk = 0; kk < TG::KSTEPS; ++kk)
           umma_ss(tmem + T_DP, dDO + TG::kmajor_step(kk), vd + TG::kmajor_step(kk), idesc_s,
                   kk > 0);
         umma_commit(dp_full);
         umma_commit(&v_empty[j % NV]);
-        ATTN_TR(1, 3, j);
-        if (j > 0) {
-          if (!(ok = mbar_wait(ds_ready, (uint32_t)(j - 1) & 1u, ctl))) break;
-          ATTN_TR(1, 4, j);
-          tc_fence_after();
-          issue_dq(j - 1, j - 1 > 0);
-          umma_commit(ds_free);
-          umma_commit(&k_empty[(j - 1) % NK]);
-          ATTN_TR(1, 5, j);
-        }
-      }
-      if (ok) ok = mbar_wait(ds_ready, (uint32_t)(n_kv - 1) & 1u, ctl);
+      };
+      // issue order: S(0), dP(0), S(1), then per tile j: dP(j+1), dQ(j), S(j+2).
+      // dP(j+1) waits only until dP(j) has been read; S(j+2) reuses the buffer of
+      // S(j) and dS(j), so it follows dQ(j)
+      bool ok = mbar_wait(qdo_full, 0, ctl) && mbar_wait(&k_full[0], 0, ctl);
       if (ok) {
         tc_fence_after();
-        issue_dq(n_kv - 1, n_kv - 1 > 0);
+        issue_s(0);
+        ok = mbar_wait(&v_full[0], 0, ctl);
+      }
+      if (ok) {
+        tc_fence_after();
+        issue_dp(0);
+        if (n_kv > 1 && (ok = mbar_wait(&k_full[1 % NK], (uint32_t)(1 / NK) & 1u, ctl))) {
+          tc_fence_after();
+          issue_s(1);
+        }
+      }
+      for (int j = 0; ok && j < n_kv; ++j) {
+        ATTN_TR(1, 0, j);
+        if (j + 1 < n_kv) {
+          const int m = j + 1;
+          ok = mbar_wait(dp_free, (uint32_t)j & 1u, ctl) &&
+               mbar_wait(&v_full[m % NV], (uint32_t)(m / NV) & 1u, ctl);
+          if (!ok) break;
+          ATTN_TR(1, 1, j);
+          tc_fence_after();
+          issue_dp(m);
+        }
+        ATTN_TR(1, 2, j);
+        if (!(ok = mbar_wait(ds_ready, (uint32_t)j & 1u, ctl))) break;
+        ATTN_TR(1, 3, j);
+        tc_fence_after();
+        issue_dq(j);
+        ATTN_TR(1, 4, j);
+        if (j + 2 < n_kv) {
+          const int m = j + 2;
+          if (!(ok = mbar_wait(&k_full[m % NK], (uint32_t)(m / NK) & 1u, ctl))) break;
+          ATTN_TR(1, 5, j);
+          tc_fence_after();
+          issue_s(m);
+        }
+        ATTN_TR(1, 6, j);
+      }
+      if (ok) {
         umma_commit(done);
-        umma_commit(&k_empty[(n_kv - 1) % NK]);
       } else {
         umma_commit(drain);
         drain_wait(drain, 0);
@@ -674,46 +707,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float delta = qin ? a.delta[rrow] : 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      // P first (needs only S), while the dP MMAs are still running
+      // P first (needs only S), while the dP MMA may still be running
       const bool tr = lane == 0 && quad == 0;
       if (tr) ATTN_TR(2 + wg, 0, j);
-      if (!(ok = mbar_wait_warp(s_full, (uint32_t)j & 1u, ctl))) break;
+      if (!(ok = mbar_wait_warp(&s_full[j & 1], (uint32_t)(j >> 1) & 1u, ctl))) break;
       if (tr) ATTN_TR(2 + wg, 1, j);
       tc_fence_after();
       uint32_t rs[64];
-      tmem_ld32x2(tmem + lane_base + T_S + 64 * wg, tmem + lane_base + T_S + 64 * wg + 32, rs);
+      const uint32_t tS = tmem + lane_base + T_S + 128 * (j & 1) + 64 * wg;
+      tmem_ld32x2(tS, tS + 32, rs);
       const int k0 = j * kBN;
-      const bool full = tile_is_full(g, q0, k0);
-      const int lim = col_limit(g, q, k0) - 64 * wg;
+      if (!tile_is_full(g, q0, k0)) {
+        // masked scores to -inf (their exponential is 0) in a pass of its own, so that
+        // the exponential loop of full tiles carries no per-element select
+        const int lim = col_limit(g, q, k0) - 64 * wg;
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c > lim) rs[c] = __float_as_uint(-INFINITY);
+      }
       float p[64];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        p[c] = ex2_approx(fmaf(__uint_as_float(rs[c]), sl2, -lse2));
-        if (!full && c > lim) p[c] = 0.f;
-      }
+      for (int c = 0; c < 64; ++c) p[c] = ex2_approx(fmaf(__uint_as_float(rs[c]), sl2, -lse2));
       if (tr) ATTN_TR(2 + wg, 2, j);
       if (!(ok = mbar_wait_warp(dp_full, (uint32_t)j & 1u, ctl))) break;
       if (tr) ATTN_TR(2 + wg, 3, j);
       tc_fence_after();
       uint32_t rp[64];
-      tmem_ld32x2(tmem + lane_base + T_DP + 64 * wg, tmem + lane_base + T_DP + 64 * wg + 32, rp);
+      const uint32_t tP = tmem + lane_base + T_DP + 64 * wg;
+      tmem_ld32x2(tP, tP + 32, rp);
       tc_fence_before();
-      mbar_arrive(sdp_used);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dp_free);  // dP columns free for dP(j+1)
       if (tr) ATTN_TR(2 + wg, 4, j);
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 64; c += 2)
         pk[c / 2] = pack_bf16x2(p[c] * (__uint_as_float(rp[c]) - delta),
                                 p[c + 1] * (__uint_as_float(rp[c + 1]) - delta));
-      if (j > 0) {
-        if (!(ok = mbar_wait_warp(ds_free, (uint32_t)(j - 1) & 1u, ctl))) break;
-        tc_fence_after();
-      }
       if (tr) ATTN_TR(2 + wg, 5, j);
-      tmem_st32(tmem + lane_base + T_DS + 32 * wg, pk);
+      // dS over the first half of this warpgroup's S(j) columns (already read)
+      tmem_st32(tS, pk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(ds_ready);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_ready);
       if (tr) ATTN_TR(2 + wg, 6, j);
     }
     // ------------------------------------------------------------ epilogue
