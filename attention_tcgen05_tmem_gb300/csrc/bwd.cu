@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
     for (int s = 0; s < NST; ++s) {
-      mbar_init(&qdo_full[s], 1);
+      mbar_init(&qdo_full[s], 2);  // the copies' expect_tx and the LSE / Delta rows
       mbar_init(&qdo_empty[s], 1);
     }
     mbar_init(s_full, 1);
@@ -264,6 +264,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait_warp(&qdo_empty[s], ph ^ 1u, ctl)) break;
         const int h = iter_head(it);
         const int q0 = iter_q0(it);
+        // the copies go out first; the LSE / Delta rows (plain loads, an L2 round
+        // trip) follow and are published by a second arrival on the same barrier
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&qdo_full[s], 2 * TG::TILE_BYTES);
+          uint8_t* dst = smem + L::ST_OFF + s * L::STAGE_BYTES;
+          TG::load(dst, &tq, &qdo_full[s], q0, h, b);
+          TG::load(dst + TG::TILE_BYTES, &tdo, &qdo_full[s], q0, h, b);
+        }
         float* st = stats + s * 256;
         const int64_t rbase = ((int64_t)b * d.Hq + h) * d.Sq;
 #pragma unroll
@@ -275,12 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           st[128 + r] = in ? a.delta[rbase + qq] : 0.f;
         }
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&qdo_full[s], 2 * TG::TILE_BYTES);
-          uint8_t* dst = smem + L::ST_OFF + s * L::STAGE_BYTES;
-          TG::load(dst, &tq, &qdo_full[s], q0, h, b);
-          TG::load(dst + TG::TILE_BYTES, &tdo, &qdo_full[s], q0, h, b);
-        }
+        if (lane == 0) mbar_arrive(&qdo_full[s]);
         issued = it + 1;
       }
       if (lane == 0 && *abort_flag) {
