@@ -354,9 +354,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int c = 0; c < 128; ++c)
           if (c > lim) sr[c] = __float_as_uint(neg_inf());
       }
-      float mt = __uint_as_float(sr[0]);
+      // row max over 8 independent chains of three-input max (a single chain of
+      // 127 dependent max operations is latency-bound)
+      float m8[8];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mt = fmaxf(mt, __uint_as_float(sr[c]));
+      for (int i = 0; i < 8; ++i) m8[i] = fmaxf(__uint_as_float(sr[i]), __uint_as_float(sr[8 + i]));
+#pragma unroll
+      for (int c = 16; c < 128; c += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          m8[i] = fmax3(m8[i], __uint_as_float(sr[c + i]), __uint_as_float(sr[c + 8 + i]));
+      const float mt = fmaxf(fmax3(m8[0], m8[1], m8[2]),
+                             fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7]));
       const float m_new = mt * sl2;  // -inf stays -inf (sl2 > 0)
       const bool need = m_new > m_run + kRescaleThreshold;
       float alpha = 1.f;
@@ -367,24 +376,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       const float mu = (m_run == neg_inf()) ? 0.f : m_run;
       if (tr) ATTN_TR(2 + x, 2, j);
-      float rs = 0.f;
+      // P = 2^(c log2(e) s - mu), argument by packed FMA; row sum in four packed
+      // partial sums (eight independent chains)
+      float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int qtr = 0; qtr < 4; ++qtr) {
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[qtr * 32 + 2 * c]), sl2, -mu));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[qtr * 32 + 2 * c + 1]), sl2, -mu));
-          rs += p0 + p1;
+          float x0, x1;
+          fma2_bc(x0, x1, __uint_as_float(sr[qtr * 32 + 2 * c]),
+                  __uint_as_float(sr[qtr * 32 + 2 * c + 1]), sl2, -mu);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          add2(rs[2 * (c & 3)], rs[2 * (c & 3) + 1], p0, p1);
           pk[c] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tS + qtr * 16, pk);
       }
-      l_run += rs;
+      l_run += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
       if (tr) ATTN_TR(2 + x, 3, j);
       if (j > 0) {
-        // PV(j-1) finished before S(j) (in-order MMA); consume its phase
-        if (!(ok = mbar_wait_warp(&o_done[x], (uint32_t)(j - 1) & 1u, ctl))) break;
+        // O holds PV(j-1): the commit that signalled S(j) tracks every MMA issued
+        // before it, PV(j-1) included, so O can be rescaled without a wait
         if (__any_sync(0xffffffffu, need)) {
           tc_fence_after();
 #pragma unroll
