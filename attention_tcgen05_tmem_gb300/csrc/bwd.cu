@@ -162,7 +162,7 @@ struct DkdvLayout {
   static constexpr int V_OFF = TG::TILE_BYTES;
   static constexpr int ST_OFF = 2 * TG::TILE_BYTES;              // stages: Q, dO
   static constexpr int STAGE_BYTES = 2 * TG::TILE_BYTES;
-  static constexpr int STAT_OFF = ST_OFF + NST * STAGE_BYTES;     // per stage: lse2[128], delta[128]
+  static constexpr int STAT_OFF = ST_OFF + NST * STAGE_BYTES;  // per stage: -lse2[128], delta[128]
   static constexpr int BAR_OFF = STAT_OFF + NST * 2 * 128 * 4;
   // kv_full, qdo_full[NST], qdo_empty[NST], s_full, dp_full, p_ready, ds_ready, done, drain
   static constexpr int NBAR = 1 + 2 * NST + 6;
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int r = lane * 4 + e;
           const int qq = q0 + r;
           const bool in = qq < d.Sq;
-          st[r] = in ? a.lse[rbase + qq] * kLog2e : INFINITY;
+          st[r] = in ? -a.lse[rbase + qq] * kLog2e : -INFINITY;  // -LSE in log2 units
           st[128 + r] = in ? a.delta[rbase + qq] : 0.f;
         }
         __syncwarp();
@@ -379,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int it = 0; it < N; ++it) {
       const int s = it % NST;
       const int q0 = iter_q0(it);
-      const float* lse2 = stats + s * 256 + 64 * wg;
+      const float* nlse2 = stats + s * 256 + 64 * wg;  // -LSE * log2(e)
       const float* dl = stats + s * 256 + 128 + 64 * wg;
       const bool tr = lane == 0 && quad == 0;
       if (tr) ATTN_TR(2 + wg, 0, it);
@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       uint32_t raw[64];
       tmem_ld32x2(tS, tS + 32, raw);
-      // keys see queries q >= kv + shift (non-full masks); rows past Sq have lse2 = inf.
+      // keys see queries q >= kv + shift (non-full masks); rows past Sq have -lse2 = -inf.
       // Masked scores go to -inf (exponential 0) in a pass of its own, so that the
       // exponential loop of full tiles carries no per-element select.
       if (!tile_is_full(g, q0, k0)) {
@@ -400,11 +400,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       float p[64];
 #pragma unroll
       for (int c = 0; c < 64; c += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
-        p[c + 0] = ex2_approx(fmaf(__uint_as_float(raw[c + 0]), sl2, -l4.x));
-        p[c + 1] = ex2_approx(fmaf(__uint_as_float(raw[c + 1]), sl2, -l4.y));
-        p[c + 2] = ex2_approx(fmaf(__uint_as_float(raw[c + 2]), sl2, -l4.z));
-        p[c + 3] = ex2_approx(fmaf(__uint_as_float(raw[c + 3]), sl2, -l4.w));
+        const float4 l4 = *reinterpret_cast<const float4*>(nlse2 + c);
+        float x[4];
+        fma2(x[0], x[1], __uint_as_float(raw[c]), __uint_as_float(raw[c + 1]), sl2, sl2, l4.x, l4.y);
+        fma2(x[2], x[3], __uint_as_float(raw[c + 2]), __uint_as_float(raw[c + 3]), sl2, sl2, l4.z,
+             l4.w);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) p[c + e] = ex2_approx(x[e]);
       }
       uint32_t pk[32];
 #pragma unroll
@@ -419,12 +421,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tr) ATTN_TR(2 + wg, 3, it);
       tc_fence_after();
       tmem_ld32x2(tdP, tdP + 32, raw);
+      // dS = P (dP - Delta); packed pairs measure faster except at D = 128, where
+      // they cost registers the kernel does not have to spare
 #pragma unroll
       for (int c = 0; c < 64; c += 4) {
         const float4 d4 = *reinterpret_cast<const float4*>(dl + c);
-        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) p[c + e] = p[c + e] * (__uint_as_float(raw[c + e]) - dv[e]);
+        if constexpr (D == 128) {
+          p[c + 0] = p[c + 0] * (__uint_as_float(raw[c + 0]) - d4.x);
+          p[c + 1] = p[c + 1] * (__uint_as_float(raw[c + 1]) - d4.y);
+          p[c + 2] = p[c + 2] * (__uint_as_float(raw[c + 2]) - d4.z);
+          p[c + 3] = p[c + 3] * (__uint_as_float(raw[c + 3]) - d4.w);
+        } else {
+          sub_mul2(p[c], p[c + 1], __uint_as_float(raw[c]), __uint_as_float(raw[c + 1]), d4.x,
+                   d4.y, p[c], p[c + 1]);
+          sub_mul2(p[c + 2], p[c + 3], __uint_as_float(raw[c + 2]), __uint_as_float(raw[c + 3]),
+                   d4.z, d4.w, p[c + 2], p[c + 3]);
+        }
       }
 #pragma unroll
       for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
@@ -730,7 +742,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float p[64];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) p[c] = ex2_approx(fmaf(__uint_as_float(rs[c]), sl2, -lse2));
+      for (int c = 0; c < 64; c += 2) {
+        float x0, x1;
+        fma2_bc(x0, x1, __uint_as_float(rs[c]), __uint_as_float(rs[c + 1]), sl2, -lse2);
+        p[c] = ex2_approx(x0);
+        p[c + 1] = ex2_approx(x1);
+      }
       if (tr) ATTN_TR(2 + wg, 2, j);
       if (!(ok = mbar_wait_warp(dp_full, (uint32_t)j & 1u, ctl))) break;
       if (tr) ATTN_TR(2 + wg, 3, j);
@@ -744,9 +761,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tr) ATTN_TR(2 + wg, 4, j);
       uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 64; c += 2)
-        pk[c / 2] = pack_bf16x2(p[c] * (__uint_as_float(rp[c]) - delta),
-                                p[c + 1] * (__uint_as_float(rp[c + 1]) - delta));
+      for (int c = 0; c < 64; c += 2) {
+        float ds0, ds1;
+        sub_mul2(ds0, ds1, __uint_as_float(rp[c]), __uint_as_float(rp[c + 1]), delta, delta, p[c],
+                 p[c + 1]);
+        pk[c / 2] = pack_bf16x2(ds0, ds1);
+      }
       if (tr) ATTN_TR(2 + wg, 5, j);
       // dS over the first half of this warpgroup's S(j) columns (already read)
       tmem_st32(tS, pk);
