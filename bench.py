@@ -409,6 +409,24 @@ def load_traffic(workload: str, kernel: str):
     return ent.get("bytes")
 
 
+# Dense bf16 tensor rate of one SM: 4096 multiply-adds per clock (a 128 x 256 x 16
+# tcgen05 MMA every 128 cycles).
+BF16_FLOP_PER_CLK_SM = 8192
+
+
+def theoretical_peak(value_per_gpu, clocks, device):
+    """Fraction of SMs x max SM clock x the per-SM dense bf16 rate, with the
+    figures it is made of; empty when the max clock was not sampled."""
+    import torch
+    mhz = (clocks or {}).get("sm_max_mhz")
+    if not mhz:
+        return {}
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    peak = sms * mhz * 1e6 * BF16_FLOP_PER_CLK_SM / 1e12
+    return {"theoretical": value_per_gpu / peak, "theoretical_tflops": peak,
+            "theoretical_basis": f"{sms} SMs x {mhz:.0f} MHz x {BF16_FLOP_PER_CLK_SM} FLOP/clk"}
+
+
 def describe(name, ws, out, n_gpus):
     cfg = dict(ws[0].describe()) if len(ws) == 1 else {
         "workload": name, "B": ws[0].B, "Hq": ws[0].Hq, "Hkv": ws[0].Hkv, "Sq": ws[0].Sq,
@@ -496,7 +514,8 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": describe(name, ws, args.out, n_gpus),
             "pct_of_peak": {"bf16_burst": value / n_gpus / peak_burst,
-                            "bf16_sustained": value / n_gpus / peak_sus, "source": peak_src},
+                            "bf16_sustained": value / n_gpus / peak_sus, "source": peak_src,
+                            **theoretical_peak(value / n_gpus, r["clocks"], local_rank)},
             "fwd_tflops": sum(flops.flops_fwd(w) for w in ws) / (pk["fwd"] / K * 1e-3) / 1e12,
             "bwd_tflops": sum(flops.flops_bwd(w) for w in ws) /
                           (sum(v for n, v in pk.items() if n != "fwd") / K * 1e-3) / 1e12,
