@@ -18,7 +18,13 @@
  *
  * Visibility (mask) follows the SpecForge post, "Flex Attention": the eagle3
  * mask_mod is or(causal_mask, suffix_mask) with shift_left = t (the number of
- * appended TTT segments), seq_lengths[b] = Q_LEN = Sq and KV_LEN = (t+1)*Sq.
+ * appended TTT segments), Q_LEN = Sq and KV_LEN = (t+1)*Sq.  Its padding
+ * terms take the per-batch key length seq_lengths[b] (kv < seq_lengths[b] in
+ * the causal part, kv % Q_LEN < seq_lengths[b] in the suffix part); without
+ * lengths every key is inside.  The same key-length bound applies to the
+ * full, causal and window masks.  The window mask (the band of the HOT-Step
+ * page's "windowed self" attention, section 4, read as q - left <= kv <=
+ * q + right) takes its two extents from the caller.
  *
  * For every (b, h) and query row q:
  *     s[kv]  = scale * sum_d Q[q,d] K[kv,d]        (visible kv only)
@@ -46,43 +52,64 @@
 #define ORACLE_MASK_FULL 0
 #define ORACLE_MASK_CAUSAL 1
 #define ORACLE_MASK_TTT 2
+#define ORACLE_MASK_WINDOW 3
 
-/* Visibility of key kv to query q.  Returns 1 if visible. */
-int oracle_visible(int mask, int t, long Sq, long Skv, long q, long kv)
+/* Visibility of key kv to query q.  Returns 1 if visible.
+ *   t       TTT step (shift_left and number of suffix segments), TTT only
+ *   wl, wr  window extents (kv in [q - wl, q + wr]), window mask only
+ *   len     key length of this batch (seq_lengths[b]); negative = no padding */
+int oracle_visible(int mask, int t, long wl, long wr, long len, long Sq, long Skv, long q,
+                   long kv)
 {
     if (q < 0 || q >= Sq || kv < 0 || kv >= Skv) return 0;
-    if (mask == ORACLE_MASK_FULL) return 1;
-    if (mask == ORACLE_MASK_CAUSAL) return kv <= q;
     if (mask == ORACLE_MASK_TTT) {
         long S = Sq;
-        /* causal_mask: q_idx - shift_left >= kv_idx, padding kv < seq_len */
-        int causal_part = (kv <= q - t) && (kv < S);
-        /* suffix_mask: kv >= Q_LEN, kv % Q_LEN < seq_len, (kv - q) % Q_LEN == 0 */
-        /* (the padding term kv % Q_LEN < seq_len holds for every kv here,
-         *  since seq_len = Q_LEN: there is no padding) */
-        int suffix_part = (kv >= S) && (kv < (long)(t + 1) * S) && (((kv - q) % S) == 0);
+        long seq_len = len < 0 ? S : len;
+        /* causal_mask: q_idx - shift_left >= kv_idx, padding kv_idx < seq_lengths[b] */
+        int causal_part = (q - t >= kv) && (kv < seq_len);
+        /* suffix_mask: kv_idx >= Q_LEN, kv_idx % Q_LEN < seq_lengths[b],
+         *              (kv_idx - q_idx) % Q_LEN == 0 */
+        int suffix_part = (kv >= S) && (kv < (long)(t + 1) * S) && (kv % S < seq_len) &&
+                          (((kv - q) % S) == 0);
         return causal_part || suffix_part;
     }
+    if (len >= 0 && kv >= len) return 0; /* padding: kv_idx < seq_lengths[b] */
+    if (mask == ORACLE_MASK_FULL) return 1;
+    if (mask == ORACLE_MASK_CAUSAL) return kv <= q;
+    if (mask == ORACLE_MASK_WINDOW) return (kv >= q - wl) && (kv <= q + wr);
     return 0;
 }
 
-/* Dense visibility bitmap out[q*Skv + kv] in {0,1}. */
-void oracle_mask(int mask, int t, long Sq, long Skv, unsigned char *out)
+/* Dense visibility bitmap out[q*Skv + kv] in {0,1} for one batch entry. */
+void oracle_mask(int mask, int t, long wl, long wr, long len, long Sq, long Skv,
+                 unsigned char *out)
 {
     for (long q = 0; q < Sq; ++q)
         for (long kv = 0; kv < Skv; ++kv)
-            out[q * Skv + kv] = (unsigned char)oracle_visible(mask, t, Sq, Skv, q, kv);
+            out[q * Skv + kv] = (unsigned char)oracle_visible(mask, t, wl, wr, len, Sq, Skv, q, kv);
+}
+
+/* The mask parameters that travel together through the passes. */
+typedef struct {
+    int mask, t;
+    long wl, wr;
+    const int *seq_lengths; /* [B] or NULL */
+} geom_t;
+
+static long batch_len(const geom_t *g, int b)
+{
+    return g->seq_lengths ? (long)g->seq_lengths[b] : -1;
 }
 
 /* One query row: fills s[] (scaled scores, -INFINITY where invisible) and
  * returns the number of visible keys; *lse gets log sum exp(s) (0 if none). */
 static long row_scores(const double *qrow, const double *Kh, long Skv, int D, double scale,
-                       int mask, int t, long Sq, long q, double *s, double *lse)
+                       const geom_t *g, long len, long Sq, long q, double *s, double *lse)
 {
     long nvis = 0;
     double mx = -INFINITY;
     for (long kv = 0; kv < Skv; ++kv) {
-        if (!oracle_visible(mask, t, Sq, Skv, q, kv)) {
+        if (!oracle_visible(g->mask, g->t, g->wl, g->wr, len, Sq, Skv, q, kv)) {
             s[kv] = -INFINITY;
             continue;
         }
@@ -104,22 +131,28 @@ static long row_scores(const double *qrow, const double *Kh, long Skv, int D, do
     return nvis;
 }
 
-static int check_shape(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t)
+static int check_shape(int B, int Hq, int Hkv, long Sq, long Skv, int D, const geom_t *g)
 {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || D <= 0) return 1;
     if (Hq % Hkv != 0) return 1;
-    if (mask == ORACLE_MASK_TTT && (t < 0 || Skv != (long)(t + 1) * Sq)) return 1;
-    if (mask < 0 || mask > 2) return 1;
+    if (g->mask < 0 || g->mask > 3) return 1;
+    if (g->mask == ORACLE_MASK_TTT && (g->t < 0 || Skv != (long)(g->t + 1) * Sq)) return 1;
+    if (g->mask == ORACLE_MASK_WINDOW && (g->wl < 0 || g->wr < 0)) return 1;
+    if (g->seq_lengths)
+        for (int b = 0; b < B; ++b)
+            if (g->seq_lengths[b] < 0) return 1;
     return 0;
 }
 
 /* Forward over query rows [q_begin, q_end) of every (b, h): O [B,Hq,Sq,D],
  * LSE [B,Hq,Sq] (other rows untouched).  Returns 0 on success. */
-int oracle_fwd_rows(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t,
-                    double scale, const double *Q, const double *K, const double *V, double *O,
-                    double *LSE, long q_begin, long q_end)
+int oracle_fwd_rows(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t, long wl,
+                    long wr, const int *seq_lengths, double scale, const double *Q,
+                    const double *K, const double *V, double *O, double *LSE, long q_begin,
+                    long q_end)
 {
-    if (check_shape(B, Hq, Hkv, Sq, Skv, D, mask, t)) return 1;
+    const geom_t g = {mask, t, wl, wr, seq_lengths};
+    if (check_shape(B, Hq, Hkv, Sq, Skv, D, &g)) return 1;
     if (q_begin < 0 || q_end > Sq || q_begin > q_end) return 1;
     const int G = Hq / Hkv;
     int ok = 1;
@@ -142,7 +175,8 @@ int oracle_fwd_rows(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, 
                 double *Lh = LSE + ((long)b * Hq + h) * Sq;
                 for (long q = q_begin; q < q_end; ++q) {
                     double lse;
-                    long nvis = row_scores(Qh + q * D, Kh, Skv, D, scale, mask, t, Sq, q, s, &lse);
+                    long nvis = row_scores(Qh + q * D, Kh, Skv, D, scale, &g, batch_len(&g, b), Sq,
+                                           q, s, &lse);
                     double *orow = Oh + q * D;
                     for (int d = 0; d < D; ++d) orow[d] = 0.0;
                     Lh[q] = lse;
@@ -161,10 +195,12 @@ int oracle_fwd_rows(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, 
 }
 
 /* Forward over every row. */
-int oracle_fwd(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t, double scale,
-               const double *Q, const double *K, const double *V, double *O, double *LSE)
+int oracle_fwd(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t, long wl, long wr,
+               const int *seq_lengths, double scale, const double *Q, const double *K,
+               const double *V, double *O, double *LSE)
 {
-    return oracle_fwd_rows(B, Hq, Hkv, Sq, Skv, D, mask, t, scale, Q, K, V, O, LSE, 0, Sq);
+    return oracle_fwd_rows(B, Hq, Hkv, Sq, Skv, D, mask, t, wl, wr, seq_lengths, scale, Q, K, V, O,
+                           LSE, 0, Sq);
 }
 
 /* Backward over query rows [q_begin, q_end): dQ of those rows, and the dK /
@@ -172,12 +208,13 @@ int oracle_fwd(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t
  * [0, Sq)).  dQ [B,Hq,Sq,D], dK and dV [B,Hkv,Skv,D].  Recomputes P and O
  * itself.  dK/dV are accumulated per q head and then summed over the group in
  * ascending head order.  Returns 0 on success. */
-int oracle_bwd_rows(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t,
-                    double scale, const double *Q, const double *K, const double *V,
-                    const double *dO, double *dQ, double *dK, double *dV, long q_begin,
-                    long q_end)
+int oracle_bwd_rows(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t, long wl,
+                    long wr, const int *seq_lengths, double scale, const double *Q,
+                    const double *K, const double *V, const double *dO, double *dQ, double *dK,
+                    double *dV, long q_begin, long q_end)
 {
-    if (check_shape(B, Hq, Hkv, Sq, Skv, D, mask, t)) return 1;
+    const geom_t g = {mask, t, wl, wr, seq_lengths};
+    if (check_shape(B, Hq, Hkv, Sq, Skv, D, &g)) return 1;
     if (q_begin < 0 || q_end > Sq || q_begin > q_end) return 1;
     const int G = Hq / Hkv;
     const size_t head_kv = (size_t)Skv * D;
@@ -214,7 +251,8 @@ int oracle_bwd_rows(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, 
                     const double *qrow = Qh + q * D;
                     const double *dorow = dOh + q * D;
                     double *dqrow = dQh + q * D;
-                    long nvis = row_scores(qrow, Kh, Skv, D, scale, mask, t, Sq, q, s, &lse);
+                    long nvis =
+                        row_scores(qrow, Kh, Skv, D, scale, &g, batch_len(&g, b), Sq, q, s, &lse);
                     for (int d = 0; d < D; ++d) dqrow[d] = 0.0;
                     if (nvis == 0) continue;
                     /* P in place of s; O row in fp64 */
@@ -273,20 +311,21 @@ int oracle_bwd_rows(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, 
 }
 
 /* Backward over every row. */
-int oracle_bwd(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t, double scale,
-               const double *Q, const double *K, const double *V, const double *dO, double *dQ,
-               double *dK, double *dV)
+int oracle_bwd(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t, long wl, long wr,
+               const int *seq_lengths, double scale, const double *Q, const double *K,
+               const double *V, const double *dO, double *dQ, double *dK, double *dV)
 {
-    return oracle_bwd_rows(B, Hq, Hkv, Sq, Skv, D, mask, t, scale, Q, K, V, dO, dQ, dK, dV, 0, Sq);
+    return oracle_bwd_rows(B, Hq, Hkv, Sq, Skv, D, mask, t, wl, wr, seq_lengths, scale, Q, K, V, dO,
+                           dQ, dK, dV, 0, Sq);
 }
 
 /* Exact count of visible (q, kv) pairs for one (b, h); used to pin the
  * mask-aware FLOP counter. */
-long long oracle_count_visible(int mask, int t, long Sq, long Skv)
+long long oracle_count_visible(int mask, int t, long wl, long wr, long len, long Sq, long Skv)
 {
     long long n = 0;
     for (long q = 0; q < Sq; ++q)
-        for (long kv = 0; kv < Skv; ++kv) n += oracle_visible(mask, t, Sq, Skv, q, kv);
+        for (long kv = 0; kv < Skv; ++kv) n += oracle_visible(mask, t, wl, wr, len, Sq, Skv, q, kv);
     return n;
 }
 
