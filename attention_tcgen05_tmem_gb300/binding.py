@@ -16,7 +16,7 @@ import threading
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libattn_train.so")
 
-MASKS = {"full": 0, "causal": 1, "ttt": 2}
+MASKS = {"full": 0, "causal": 1, "ttt": 2, "window": 3}
 STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_ALIGNMENT",
           4: "ATTN_ERR_WORKSPACE", 5: "ATTN_ERR_CUDA", 6: "ATTN_ERR_DEVICE_TIMEOUT"}
 
@@ -41,7 +41,8 @@ class Problem(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
                 ("Sq", ctypes.c_int), ("Skv", ctypes.c_int), ("D", ctypes.c_int),
                 ("mask", ctypes.c_int), ("ttt_step", ctypes.c_int), ("scale", ctypes.c_float),
-                ("out_dtype", ctypes.c_int)]
+                ("out_dtype", ctypes.c_int), ("window_left", ctypes.c_int),
+                ("window_right", ctypes.c_int), ("seq_lengths", ctypes.c_void_p)]
 
 
 OUT_DTYPES = {"bf16": 0, "fp32": 1}
@@ -94,15 +95,32 @@ def _check(status: int):
         raise AttnError(status, msg)
 
 
-def problem(B, Hq, Hkv, Sq, Skv, D, mask="causal", ttt_step=0, scale=0.0, out="bf16") -> Problem:
+def _lens_ptr(seq_lengths) -> int:
+    """Device address of an int32 [B] tensor of key lengths (0 = none)."""
+    if seq_lengths is None:
+        return 0
+    import torch
+    if seq_lengths.dtype != torch.int32 or not seq_lengths.is_cuda or not seq_lengths.is_contiguous():
+        raise ValueError("seq_lengths must be a contiguous int32 CUDA tensor")
+    return seq_lengths.data_ptr()
+
+
+def problem(B, Hq, Hkv, Sq, Skv, D, mask="causal", ttt_step=0, scale=0.0, out="bf16",
+            window=None, seq_lengths=None) -> Problem:
+    """window=(left, right) for the window mask; seq_lengths = device int32 [B]
+    key lengths (the caller keeps the tensor alive while the problem is used)."""
     m = MASKS[mask] if isinstance(mask, str) else int(mask)
-    return Problem(B, Hq, Hkv, Sq, Skv, D, m, ttt_step, float(scale), OUT_DTYPES[out])
+    wl, wr = (0, 0) if window is None else (int(window[0]), int(window[1]))
+    return Problem(B, Hq, Hkv, Sq, Skv, D, m, ttt_step, float(scale), OUT_DTYPES[out], wl, wr,
+                   _lens_ptr(seq_lengths))
 
 
-def problem_for(q, k, mask="causal", ttt_step=0, scale=None, out="bf16") -> Problem:
+def problem_for(q, k, mask="causal", ttt_step=0, scale=None, out="bf16", window=None,
+                seq_lengths=None) -> Problem:
     B, Hq, Sq, D = q.shape
     _, Hkv, Skv, _ = k.shape
-    return problem(B, Hq, Hkv, Sq, Skv, D, mask, ttt_step, 0.0 if scale is None else scale, out)
+    return problem(B, Hq, Hkv, Sq, Skv, D, mask, ttt_step, 0.0 if scale is None else scale, out,
+                   window, seq_lengths)
 
 
 def _torch_out_dtype(out):
@@ -184,23 +202,25 @@ def set_wait_budget_ns(ns: int):
 
 
 # ------------------------------------------------------------ conveniences
-def fwd(q, k, v, mask="causal", ttt_step=0, scale=None, stream=None, out="bf16"):
+def fwd(q, k, v, mask="causal", ttt_step=0, scale=None, stream=None, out="bf16", window=None,
+        seq_lengths=None):
     """Allocates O (bf16 or fp32) and LSE with torch, runs the forward;
     returns (o, lse)."""
     import torch
-    p = problem_for(q, k, mask, ttt_step, scale, out)
+    p = problem_for(q, k, mask, ttt_step, scale, out, window, seq_lengths)
     o = torch.empty(q.shape, dtype=_torch_out_dtype(out), device=q.device)
     lse = torch.empty(q.shape[0], q.shape[1], q.shape[2], dtype=torch.float32, device=q.device)
     fwd_raw(p, q, k, v, o, lse, stream)
     return o, lse
 
 
-def bwd(q, k, v, o, lse, dout, mask="causal", ttt_step=0, scale=None, stream=None, workspace=None):
+def bwd(q, k, v, o, lse, dout, mask="causal", ttt_step=0, scale=None, stream=None, workspace=None,
+        window=None, seq_lengths=None):
     """Allocates dQ, dK, dV (same dtype as o: bf16 or fp32) and the workspace
     unless given; returns (dq, dk, dv)."""
     import torch
     out = "fp32" if o.dtype == torch.float32 else "bf16"
-    p = problem_for(q, k, mask, ttt_step, scale, out)
+    p = problem_for(q, k, mask, ttt_step, scale, out, window, seq_lengths)
     dq = torch.empty(q.shape, dtype=o.dtype, device=q.device)
     dk = torch.empty(k.shape, dtype=o.dtype, device=q.device)
     dv = torch.empty(v.shape, dtype=o.dtype, device=q.device)
@@ -210,10 +230,14 @@ def bwd(q, k, v, o, lse, dout, mask="causal", ttt_step=0, scale=None, stream=Non
     return dq, dk, dv
 
 
-def mask_pattern(Sq, Skv, mask, ttt_step=0, device="cuda", with_tiles=True):
-    """Device view of the mask: (bits[2, Sq, Skv] uint8, tiles or None)."""
+def mask_pattern(Sq, Skv, mask, ttt_step=0, device="cuda", with_tiles=True, window=None,
+                 seq_length=None):
+    """Device view of the mask for one batch entry of key length seq_length
+    (None = every key): (bits[2, Sq, Skv] uint8, tiles or None)."""
     import torch
-    p = problem(1, 1, 1, Sq, Skv, 64, mask, ttt_step)
+    lens = None if seq_length is None else torch.tensor([seq_length], dtype=torch.int32,
+                                                        device=device)
+    p = problem(1, 1, 1, Sq, Skv, 64, mask, ttt_step, window=window, seq_lengths=lens)
     bits = torch.zeros(2, Sq, Skv, dtype=torch.uint8, device=device)
     tiles = None
     if with_tiles:

@@ -117,8 +117,18 @@ attn_status check_problem(const attn_problem* p) {
     return fail(ATTN_ERR_INVALID, "Hq (%d) must be a multiple of Hkv (%d)", p->Hq, p->Hkv);
   if (p->D != 16 && p->D != 32 && p->D != 64 && p->D != 128)
     return fail(ATTN_ERR_UNSUPPORTED, "head dim %d unsupported (16, 32, 64, 128)", p->D);
-  if (p->mask != ATTN_MASK_FULL && p->mask != ATTN_MASK_CAUSAL && p->mask != ATTN_MASK_TTT)
+  if (p->mask != ATTN_MASK_FULL && p->mask != ATTN_MASK_CAUSAL && p->mask != ATTN_MASK_TTT &&
+      p->mask != ATTN_MASK_WINDOW)
     return fail(ATTN_ERR_UNSUPPORTED, "unknown mask kind %d", p->mask);
+  if (p->mask == ATTN_MASK_WINDOW) {
+    if (p->window_left < 0 || p->window_right < 0)
+      return fail(ATTN_ERR_INVALID, "window extents (%d, %d) must be >= 0", p->window_left,
+                  p->window_right);
+  } else if (p->window_left != 0 || p->window_right != 0) {
+    return fail(ATTN_ERR_INVALID, "window extents are set but the mask is not ATTN_MASK_WINDOW");
+  }
+  if (reinterpret_cast<uintptr_t>(p->seq_lengths) % 4 != 0)
+    return fail(ATTN_ERR_ALIGNMENT, "seq_lengths is not 4-byte aligned");
   if (p->mask == ATTN_MASK_TTT) {
     if (p->ttt_step < 0) return fail(ATTN_ERR_INVALID, "ttt_step %d < 0", p->ttt_step);
     if ((int64_t)p->Skv != (int64_t)(p->ttt_step + 1) * p->Sq)
@@ -166,7 +176,9 @@ Dims make_dims(const attn_problem* p) {
   d.Skv = p->Skv;
   d.D = p->D;
   d.G = p->Hq / p->Hkv;
-  d.geom = attn::make_geom(p->mask, p->mask == ATTN_MASK_TTT ? p->ttt_step : 0, p->Sq, p->Skv);
+  d.geom = attn::make_geom(p->mask, p->mask == ATTN_MASK_TTT ? p->ttt_step : 0, p->window_left,
+                           p->window_right, p->Sq, p->Skv);
+  d.seqlens = p->seq_lengths;
   d.scale = p->scale > 0.f ? p->scale : 1.0f / std::sqrt((float)p->D);
   d.scale_log2 = d.scale * 1.4426950408889634f;
   d.out_f32 = p->out_dtype == ATTN_OUT_F32 ? 1 : 0;

@@ -18,8 +18,9 @@ namespace {
 // bits[1][q][kv]: same for the column-side schedule
 // Both include the TTT suffix diagonals exactly as the kernels address them
 // (key row i*Sq + q, i = 1..t).  tiles[qt][kt] = tile class of the tiled part.
+// With per-batch key lengths this is the view of batch entry 0.
 __global__ void mask_pattern_kernel(const Dims d, uint8_t* bits, uint8_t* tiles) {
-  const MaskGeom g = d.geom;
+  const MaskGeom g = with_len(d.geom, d.seqlens, 0);
   const int64_t n = (int64_t)d.Sq * d.Skv;
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
        idx += (int64_t)gridDim.x * blockDim.x) {
@@ -27,22 +28,31 @@ __global__ void mask_pattern_kernel(const Dims d, uint8_t* bits, uint8_t* tiles)
     const int kv = (int)(idx % d.Skv);
     uint8_t row_side = 0, col_side = 0;
     if (kv < g.kv_main) {
-      const int k0 = (kv / kBN) * kBN;
+      const int kt = kv / kBN, k0 = kt * kBN;
       // row side: the forward pairs query tiles; its key range covers both
       const int qp0 = (q / (2 * kBM)) * 2 * kBM;
       const int qt0 = (q / kBM) * kBM;
-      const bool fwd_visits = k0 < kv_end_for_rows(g, qp0, 2 * kBM);
-      const bool dq_visits = k0 < kv_end_for_rows(g, qt0, kBM);
-      const bool unmasked = tile_is_full(g, qt0, k0) || (kv - k0) <= col_limit(g, q, k0);
+      int f0, fn, q0t, qn;
+      kv_tiles_for_rows(g, qp0, 2 * kBM, &f0, &fn);
+      kv_tiles_for_rows(g, qt0, kBM, &q0t, &qn);
+      const bool fwd_visits = kt >= f0 && kt < f0 + fn;
+      const bool dq_visits = kt >= q0t && kt < q0t + qn;
+      int clo, chi;
+      col_range(g, q, k0, &clo, &chi);
+      const bool unmasked = tile_is_full(g, qt0, k0) || (kv - k0 >= clo && kv - k0 <= chi);
       row_side = (fwd_visits && dq_visits && unmasked) ? 1 : 0;
-      // column side: query tiles from q_begin_for_kv(k0) upward
-      const int qt_first = q_begin_for_kv(g, k0) / kBM;
-      const bool visits = q / kBM >= qt_first;
-      const bool keep = tile_is_full(g, qt0, k0) || g.kind == kMaskFull || q >= kv + g.shift;
+      // column side: query tiles of the key tile's query range
+      int qlo, qhi;
+      q_range_for_kv(g, k0, &qlo, &qhi);
+      const bool visits = qhi > qlo && q / kBM >= qlo / kBM && q / kBM < cdiv(qhi, kBM);
+      int rlo, rhi;
+      row_range_for_kv(g, kv, qt0, &rlo, &rhi);
+      const bool keep = tile_is_full(g, qt0, k0) || (q - qt0 >= rlo && q - qt0 <= rhi);
       col_side = (visits && keep) ? 1 : 0;
     } else if (g.ttt > 0) {
       const int64_t rel = (int64_t)kv - q;
-      const bool diag = kv >= d.Sq && rel > 0 && rel % d.Sq == 0 && rel / d.Sq <= g.ttt;
+      const bool diag = kv >= d.Sq && rel > 0 && rel % d.Sq == 0 && rel / d.Sq <= g.ttt &&
+                        q < g.kv_len;
       row_side = col_side = diag ? 1 : 0;
     }
     bits[idx] = row_side;

@@ -126,6 +126,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdArgs a) {
   const int t = a.d.geom.ttt;  // uniform over the grid
   if (t > 0) {
     const int hk = h / a.d.G;
+    const bool diag_vis = in && q < with_len(a.d.geom, a.d.seqlens, b).kv_len;
     uint4 qa = make_uint4(0u, 0u, 0u, 0u);
     float lse2 = 0.f;
     if (in) {
@@ -145,7 +146,9 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdArgs a) {
         dp += __shfl_xor_sync(0xffffffffu, dp, off, TPR);
       }
       if (in && sub == 0) {
-        const float p = ex2_approx(fmaf(s, a.d.scale_log2, -lse2));
+        // the diagonals of rows at or past the batch entry's key length are masked
+        // (their weight and score gradient are 0, and so are their dK, dV and dQ terms)
+        const float p = diag_vis ? ex2_approx(fmaf(s, a.d.scale_log2, -lse2)) : 0.f;
         a.ttt_p[row * t + (i - 1)] = p;
         a.ttt_ds[row * t + (i - 1)] = p * (dp - acc);
       }
@@ -173,7 +176,9 @@ struct DkdvLayout {
   static_assert(ALLOC <= 227 * 1024, "shared memory budget");
 };
 
-template <int D>
+// W: the mask has a lower key bound (window) or per-batch key lengths; the
+// other masks take the one-sided form of the tile arithmetic.
+template <int D, bool W>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -200,8 +205,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* stats = reinterpret_cast<float*>(smem + L::STAT_OFF);  // [NST][2][128]
 
   const Dims& d = a.d;
-  const MaskGeom g = d.geom;
-  const int n_kt = cdiv(g.kv_main, kBN);
   const int BH = d.B * d.Hkv;
   // heaviest key tiles (smallest k0 under causal/TTT) first
   const int kt = (int)(blockIdx.x / BH);
@@ -209,11 +212,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hk = bh % d.Hkv;
   const int b = bh / d.Hkv;
   const int k0 = kt * kBN;
-  const int n_qt_all = cdiv(d.Sq, kBM);
-  const int qt_begin = q_begin_for_kv(g, k0) / kBM;
-  const int n_q = n_qt_all - qt_begin;  // visible query tiles per q head
-  const int N = (n_q > 0 ? n_q : 0) * d.G;
-  (void)n_kt;
+  // this batch entry's geometry; query tiles qt_begin .. qt_begin + n_q - 1 see the key tile
+  const MaskGeom g = W ? with_len(d.geom, d.seqlens, b) : d.geom;
+  int qt_begin, n_q;
+  if constexpr (W) {
+    int q_lo, q_hi;
+    q_range_for_kv(g, k0, &q_lo, &q_hi);
+    qt_begin = q_lo / kBM;
+    n_q = q_hi > q_lo ? cdiv(q_hi, kBM) - qt_begin : 0;
+  } else {
+    qt_begin = upper_q_begin(g, k0) / kBM;
+    n_q = cdiv(d.Sq, kBM) - qt_begin;
+    if (n_q < 0) n_q = 0;
+  }
+  const int N = n_q * d.G;
 
   const int warp = warp_id();
   const int lane = lane_id();
@@ -371,6 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const int kv = k0 + r;
+    const FullRange full_q = full_rows_for_keys(g, k0);  // query tiles without masking (W)
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const uint32_t tS = tmem + lane_base + 64 * wg;         // S^T / P^T columns of this WG
     const uint32_t tdP = tmem + lane_base + 128 + 64 * wg;  // dP^T / dS^T
@@ -388,11 +401,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       uint32_t raw[64];
       tmem_ld32x2(tS, tS + 32, raw);
-      // keys see queries q >= kv + shift (non-full masks); rows past Sq have -lse2 = -inf.
-      // Masked scores go to -inf (exponential 0) in a pass of its own, so that the
-      // exponential loop of full tiles carries no per-element select.
-      if (!tile_is_full(g, q0, k0)) {
-        const int cmin = (g.kind == kMaskFull) ? 0 : kv + g.shift - q0 - 64 * wg;
+      // key row kv sees query columns [clo, chi] of the tile; rows past Sq have
+      // -lse2 = -inf.  Masked scores go to -inf (exponential 0) in a pass of its own,
+      // so that the exponential loop of full tiles carries no per-element select.
+      if constexpr (W) {
+        if (!in_range(full_q, q0)) {
+          int clo, chi;
+          row_range_for_kv(g, kv, q0 + 64 * wg, &clo, &chi);
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c < clo || c > chi) raw[c] = __float_as_uint(-INFINITY);
+        }
+      } else if (!upper_tile_full(g, q0, k0)) {
+        const int cmin = upper_q_begin(g, kv) - q0 - 64 * wg;
 #pragma unroll
         for (int c = 0; c < 64; ++c)
           if (c < cmin) raw[c] = __float_as_uint(-INFINITY);
@@ -506,7 +527,7 @@ struct DqLayout {
   static_assert(ALLOC <= 227 * 1024, "shared memory budget");
 };
 
-template <int D>
+template <int D, bool W>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -539,11 +560,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
 
   const Dims& d = a.d;
-  const MaskGeom g = d.geom;
   const int n_qt = cdiv(d.Sq, kBM);
   const int BH = d.B * d.Hq;
   int qt, bh;
-  if (g.kind == kMaskFull) {
+  if (d.geom.kind == kMaskFull || d.geom.kind == kMaskWindow) {
     qt = blockIdx.x % n_qt;
     bh = blockIdx.x / n_qt;
   } else {
@@ -554,7 +574,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = bh / d.Hq;
   const int hk = h / d.G;
   const int q0 = qt * kBM;
-  const int n_kv = cdiv(kv_end_for_rows(g, q0, kBM), kBN);
+  // this batch entry's geometry; key tiles kt0 .. kt0 + n_kv - 1
+  const MaskGeom g = W ? with_len(d.geom, d.seqlens, b) : d.geom;
+  int kt0 = 0, n_kv;
+  if constexpr (W) kv_tiles_for_rows(g, q0, kBM, &kt0, &n_kv);
+  else n_kv = cdiv(upper_kv_end(g, q0, kBM), kBN);
 
   const int warp = warp_id();
   const int lane = lane_id();
@@ -601,11 +625,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < n_kv; ++j) {
         if (!mbar_wait(&k_empty[j % NK], ((uint32_t)(j / NK) & 1u) ^ 1u, ctl)) break;
         mbar_arrive_expect_tx(&k_full[j % NK], TG::TILE_BYTES);
-        TG::load(smem + L::K_OFF + (j % NK) * TG::TILE_BYTES, &tk, &k_full[j % NK], j * kBN, hk, b);
+        TG::load(smem + L::K_OFF + (j % NK) * TG::TILE_BYTES, &tk, &k_full[j % NK],
+                 (kt0 + j) * kBN, hk, b);
         k_issued = j + 1;
         if (!mbar_wait(&v_empty[j % NV], ((uint32_t)(j / NV) & 1u) ^ 1u, ctl)) break;
         mbar_arrive_expect_tx(&v_full[j % NV], TG::TILE_BYTES);
-        TG::load(smem + L::V_OFF + (j % NV) * TG::TILE_BYTES, &tv, &v_full[j % NV], j * kBN, hk, b);
+        TG::load(smem + L::V_OFF + (j % NV) * TG::TILE_BYTES, &tv, &v_full[j % NV],
+                 (kt0 + j) * kBN, hk, b);
         v_issued = j + 1;
       }
       if (*abort_flag) {
@@ -720,6 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool qin = q < d.Sq;
     const float lse2 = qin ? a.lse[rrow] * kLog2e : INFINITY;
     const float delta = qin ? a.delta[rrow] : 0.f;
+    const FullRange full_k = full_keys_for_rows(g, q0);  // key tiles without masking (W)
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       // P first (needs only S), while the dP MMA may still be running
@@ -731,11 +758,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t rs[64];
       const uint32_t tS = tmem + lane_base + T_S + 128 * (j & 1) + 64 * wg;
       tmem_ld32x2(tS, tS + 32, rs);
-      const int k0 = j * kBN;
-      if (!tile_is_full(g, q0, k0)) {
-        // masked scores to -inf (their exponential is 0) in a pass of its own, so that
-        // the exponential loop of full tiles carries no per-element select
-        const int lim = col_limit(g, q, k0) - 64 * wg;
+      const int k0 = (kt0 + j) * kBN;
+      // masked scores to -inf (their exponential is 0) in a pass of its own, so that
+      // the exponential loop of full tiles carries no per-element select
+      if constexpr (W) {
+        if (!in_range(full_k, k0)) {
+          int clo, chi;
+          col_range(g, q, k0 + 64 * wg, &clo, &chi);
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c < clo || c > chi) rs[c] = __float_as_uint(-INFINITY);
+        }
+      } else if (!upper_tile_full(g, q0, k0)) {
+        const int lim = upper_col_limit(g, q, k0) - 64 * wg;
 #pragma unroll
         for (int c = 0; c < 64; ++c)
           if (c > lim) rs[c] = __float_as_uint(-INFINITY);
@@ -904,8 +939,8 @@ __global__ void __launch_bounds__(256) ttt_diag_bwd_kernel(const BwdArgs a) {
   }
 }
 
-template <int D>
-cudaError_t launch_bwd_d(const BwdArgs& a, const Maps& m, unsigned passes, cudaStream_t s) {
+template <int D, bool W>
+cudaError_t launch_bwd_dw(const BwdArgs& a, const Maps& m, unsigned passes, cudaStream_t s) {
   cudaError_t e;
   if (passes & 1u) {
     constexpr int RPB = 256 / (D / 8);
@@ -915,7 +950,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const Maps& m, unsigned passes, cudaS
   }
   if (passes & 2u) {
     using L = DkdvLayout<D>;
-    auto kern = bwd_dkdv_kernel<D>;
+    auto kern = bwd_dkdv_kernel<D, W>;
     static const cudaError_t regs_ok = check_launch_regs(reinterpret_cast<const void*>(kern));
     if (regs_ok != cudaSuccess) return regs_ok;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC)) !=
@@ -927,7 +962,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const Maps& m, unsigned passes, cudaS
   }
   if (passes & 4u) {
     using L = DqLayout<D>;
-    auto kern = bwd_dq_kernel<D>;
+    auto kern = bwd_dq_kernel<D, W>;
     static const cudaError_t regs_ok = check_launch_regs(reinterpret_cast<const void*>(kern));
     if (regs_ok != cudaSuccess) return regs_ok;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC)) !=
@@ -943,6 +978,12 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const Maps& m, unsigned passes, cudaS
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdArgs& a, const Maps& m, unsigned passes, cudaStream_t s) {
+  return needs_general_mask(a.d) ? launch_bwd_dw<D, true>(a, m, passes, s)
+                                 : launch_bwd_dw<D, false>(a, m, passes, s);
 }
 
 }  // namespace

@@ -129,7 +129,9 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 
 __device__ __forceinline__ float neg_inf() { return -INFINITY; }
 
-template <int D>
+// W: the mask has a lower key bound (window) or per-batch key lengths; the
+// other masks take the one-sided form of the tile arithmetic.
+template <int D, bool W>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
@@ -153,12 +155,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
 
   const Dims& d = a.d;
-  const MaskGeom g = d.geom;
   // ---- work decode: causal/TTT launch the longest query-tile pairs first
   const int n_qp = cdiv(d.Sq, 2 * kBM);
   const int BH = d.B * d.Hq;
   int qp, bh;
-  if (g.kind == kMaskFull) {
+  if (d.geom.kind == kMaskFull || d.geom.kind == kMaskWindow) {
     qp = blockIdx.x % n_qp;
     bh = blockIdx.x / n_qp;
   } else {
@@ -169,7 +170,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int b = bh / d.Hq;
   const int hk = h / d.G;
   const int q0 = qp * 2 * kBM;
-  const int n_kv = cdiv(kv_end_for_rows(g, q0, 2 * kBM), kBN);
+  // this batch entry's geometry; key tiles kt0 .. kt0 + n_kv - 1
+  const MaskGeom g = W ? with_len(d.geom, d.seqlens, b) : d.geom;
+  int kt0 = 0, n_kv;
+  if constexpr (W) kv_tiles_for_rows(g, q0, 2 * kBM, &kt0, &n_kv);
+  else n_kv = cdiv(upper_kv_end(g, q0, 2 * kBM), kBN);
 
   const int warp = warp_id();
   const int lane = lane_id();
@@ -224,7 +229,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
           mbar_arrive_expect_tx(&kv_full[s], TG::TILE_BYTES);
           TG::load(smem + L::KV_OFF + s * TG::TILE_BYTES, w == 0 ? &tk : &tv, &kv_full[s],
-                   j * kBN, hk, b);
+                   (kt0 + j) * kBN, hk, b);
           issued = idx + 1;
         }
         if (!ok) break;
@@ -334,6 +339,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t tO = tmem + lane_base + 256 + x * D;
     const float sl2 = d.scale_log2;
 
+    const FullRange full_k = full_keys_for_rows(g, qt0);  // key tiles without masking (W)
     float m_run = neg_inf();  // running max of c*log2(e)*s
     float l_run = 0.f;
     bool ok = true;
@@ -347,9 +353,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tmem_ld32x2(tS + 0, tS + 32, *reinterpret_cast<uint32_t(*)[64]>(&sr[0]));
       tmem_ld32x2(tS + 64, tS + 96, *reinterpret_cast<uint32_t(*)[64]>(&sr[64]));
 
-      const int k0 = j * kBN;
-      if (!tile_is_full(g, qt0, k0)) {
-        const int lim = col_limit(g, q, k0);
+      const int k0 = (kt0 + j) * kBN;
+      if constexpr (W) {
+        if (!in_range(full_k, k0)) {
+          int clo, chi;
+          col_range(g, q, k0, &clo, &chi);
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c < clo || c > chi) sr[c] = __float_as_uint(neg_inf());
+        }
+      } else if (!upper_tile_full(g, qt0, k0)) {
+        const int lim = upper_col_limit(g, q, k0);
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (c > lim) sr[c] = __float_as_uint(neg_inf());
@@ -422,6 +436,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (ok) {
       if (n_kv > 0) tc_fence_after();
       const bool qin = q < d.Sq;
+      // suffix diagonals exist for rows inside the batch entry's key length
+      const bool qdiag = qin && q < g.kv_len;
       if (g.ttt > 0) {
         // TTT suffix diagonals (key/value row i*Sq + q of segment i = 1..t), merged into
         // the unnormalised O accumulator in TMEM by log-sum-exp
@@ -444,7 +460,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                : dot_rows<D>(qrow, row_ptr(a.k, b, hk, (int64_t)i * d.Sq + q)) * sl2;
         };
         float m_star = m_run;  // pass 1: the merged running max
-        if (qin)
+        if (qdiag)
           for (int i = 1; i <= g.ttt; ++i) m_star = fmaxf(m_star, diag_score(i));
         const float alpha = (m_run == neg_inf()) ? 0.f : ex2_approx(m_run - m_star);
         l_run *= alpha;
@@ -454,7 +470,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int u = 0; u < kDiagBatch; ++u) {
             w[u] = 0.f;
-            if (qin && i0 + u <= g.ttt) {
+            if (qdiag && i0 + u <= g.ttt) {
               w[u] = ex2_approx(diag_score(i0 + u) - m_star);
               l_run += w[u];
             }
@@ -469,7 +485,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             for (int e = 0; e < 16; ++e) vals[e] = __uint_as_float(raw[e]) * scale0;
 #pragma unroll
             for (int u = 0; u < kDiagBatch; ++u)
-              if (qin && i0 + u <= g.ttt)
+              if (qdiag && i0 + u <= g.ttt)
                 axpy16(vals, w[u], row_ptr(a.v, b, hk, (int64_t)(i0 + u) * d.Sq + q) + c0);
 #pragma unroll
             for (int e = 0; e < 16; ++e) raw[e] = __float_as_uint(vals[e]);
@@ -510,10 +526,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D>
-cudaError_t launch_fwd_d(const FwdArgs& a, const Maps& m, cudaStream_t s) {
+template <int D, bool W>
+cudaError_t launch_fwd_dw(const FwdArgs& a, const Maps& m, cudaStream_t s) {
   using L = FwdLayout<D>;
-  auto kern = fwd_kernel<D>;
+  auto kern = fwd_kernel<D, W>;
   static const cudaError_t regs_ok = check_launch_regs(reinterpret_cast<const void*>(kern));
   if (regs_ok != cudaSuccess) return regs_ok;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
@@ -528,6 +544,12 @@ cudaError_t launch_fwd_d(const FwdArgs& a, const Maps& m, cudaStream_t s) {
   const unsigned grid = (unsigned)(n_qp * a.d.B * a.d.Hq);
   kern<<<grid, kFwdThreads, L::ALLOC, s>>>(m.q, m.k, m.v, a);
   return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdArgs& a, const Maps& m, cudaStream_t s) {
+  return needs_general_mask(a.d) ? launch_fwd_dw<D, true>(a, m, s)
+                                 : launch_fwd_dw<D, false>(a, m, s);
 }
 
 }  // namespace

@@ -22,7 +22,14 @@ struct Dims {
   float scale;       // softmax scale c
   float scale_log2;  // c * log2(e)
   int out_f32;       // O, dQ, dK, dV are fp32 (else bf16)
+  const int* seqlens;  // device [B]: key length of each batch entry, or null (all keys)
 };
+
+// Whether a problem needs the general (two-sided, per-batch length) mask
+// arithmetic: a window mask or per-batch key lengths.
+inline bool needs_general_mask(const Dims& d) {
+  return d.geom.kind == kMaskWindow || d.seqlens != nullptr;
+}
 
 struct Ctl {
   uint32_t* err;       // device error word

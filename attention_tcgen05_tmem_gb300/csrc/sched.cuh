@@ -7,13 +7,20 @@
 // HOT-Step page, section 3, reports that skipping all -inf tiles halves the
 // causal work).
 //
-// The tiled part of every mask is one predicate:
-//     visible(q, kv) = kv < kv_main  and  (mask == FULL  or  kv <= q - shift)
-// with shift = 0 (causal), shift = t (TTT step t: segment 0's causal part
-// shrinks by one diagonal per appended segment, SpecForge "Flex Attention"
-// causal_mask with shift_left = t), kv_main = Skv for full/causal and Sq for
-// TTT.  The TTT suffix diagonals (kv = q + i*Sq, i = 1..t) are not tiles:
-// the kernels merge them in a separate per-row pass.
+// The tiled part of every mask is one band predicate:
+//     visible(q, kv) = kv < kv_len  and  q - lo <= kv <= q + hi
+//   full:    lo = hi = unbounded
+//   causal:  lo unbounded, hi = 0
+//   TTT t:   lo unbounded, hi = -t (segment 0's causal part shrinks by one
+//            diagonal per appended segment: SpecForge "Flex Attention",
+//            causal_mask with shift_left = t)
+//   window:  lo = left, hi = right extent (the HOT-Step page's windowed
+//            self-attention, section 4, read as a band around the diagonal)
+// kv_len is the key length of the tiled part for one batch entry: Skv (Sq for
+// TTT), cut to seq_lengths[b] when the caller passes per-batch lengths (the
+// padding term kv < seq_lengths[b] of the eagle3 mask_mod).  The TTT suffix
+// diagonals (kv = q + i*Sq, i = 1..t, visible for q < seq_lengths[b]) are not
+// tiles: the kernels merge them in a separate per-row pass.
 #pragma once
 #include <cstdint>
 
@@ -22,71 +29,181 @@ namespace attn {
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // key rows per tile
 
-enum MaskKind : int { kMaskFull = 0, kMaskCausal = 1, kMaskTTT = 2 };
+enum MaskKind : int { kMaskFull = 0, kMaskCausal = 1, kMaskTTT = 2, kMaskWindow = 3 };
+
+// An extent that no problem reaches (sequence lengths stay below 2^30; the
+// helpers below compute in 64 bits, so q + kUnbounded cannot overflow).
+constexpr int kUnbounded = 1 << 30;
 
 struct MaskGeom {
-  int kind;     // MaskKind
-  int shift;    // 0 for causal, t for TTT, unused for full
-  int Sq;       // query rows
-  int kv_main;  // key rows of the tiled part
-  int ttt;      // number of suffix diagonals (t for TTT, else 0)
+  int kind;      // MaskKind
+  int Sq;        // query rows
+  int kv_main;   // key rows of the tiled part (Skv, or Sq for TTT)
+  int kv_len;    // kv_main cut to this batch entry's key length (see with_len)
+  int ttt;       // number of suffix diagonals (t for TTT, else 0)
+  int lo;        // band: kv >= q - lo
+  int hi;        // band: kv <= q + hi
 };
 
-__host__ __device__ inline MaskGeom make_geom(int kind, int t, int Sq, int Skv) {
+__host__ __device__ inline MaskGeom make_geom(int kind, int t, int wl, int wr, int Sq, int Skv) {
   MaskGeom g;
   g.kind = kind;
-  g.shift = (kind == kMaskTTT) ? t : 0;
   g.Sq = Sq;
   g.kv_main = (kind == kMaskTTT) ? Sq : Skv;
+  g.kv_len = g.kv_main;
   g.ttt = (kind == kMaskTTT) ? t : 0;
+  g.lo = (kind == kMaskWindow) ? (wl < kUnbounded ? wl : kUnbounded) : kUnbounded;
+  g.hi = kind == kMaskFull ? kUnbounded
+       : kind == kMaskCausal ? 0
+       : kind == kMaskTTT ? -t
+                           : (wr < kUnbounded ? wr : kUnbounded);
+  return g;
+}
+
+// The geometry of batch entry b: keys from seq_lengths[b] on are invisible
+// (values are clamped to [0, kv_main]; null = every key).
+__host__ __device__ inline MaskGeom with_len(MaskGeom g, const int* seq_lengths, int b) {
+  if (seq_lengths != nullptr) {
+    int L = seq_lengths[b];
+    if (L < 0) L = 0;
+    if (L > g.kv_main) L = g.kv_main;
+    g.kv_len = L;
+  }
   return g;
 }
 
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-// Keys [0, end) that some query of rows [q0, q0 + rows) may see.
-__host__ __device__ inline int kv_end_for_rows(const MaskGeom& g, int q0, int rows) {
-  if (g.kind == kMaskFull) return g.kv_main;
-  int last_q = q0 + rows - 1;
+__host__ __device__ inline int64_t clamp64(int64_t x, int64_t a, int64_t b) {
+  return x < a ? a : (x > b ? b : x);
+}
+
+// Keys [begin, end) that some query of rows [q0, q0 + rows) may see.
+__host__ __device__ inline void kv_range_for_rows(const MaskGeom& g, int q0, int rows, int* begin,
+                                                  int* end) {
+  int64_t last_q = (int64_t)q0 + rows - 1;
   if (last_q > g.Sq - 1) last_q = g.Sq - 1;
-  long e = (long)last_q - g.shift + 1;
-  if (e < 0) e = 0;
-  if (e > g.kv_main) e = g.kv_main;
-  return (int)e;
+  const int64_t e = clamp64(last_q + g.hi + 1, 0, g.kv_len);
+  const int64_t b = clamp64((int64_t)q0 - g.lo, 0, e);
+  *begin = (int)b;
+  *end = (int)e;
+}
+
+// Key tiles [*kt0, *kt0 + *n) to visit for rows [q0, q0 + rows).
+__host__ __device__ inline void kv_tiles_for_rows(const MaskGeom& g, int q0, int rows, int* kt0,
+                                                  int* n) {
+  int b, e;
+  kv_range_for_rows(g, q0, rows, &b, &e);
+  *kt0 = b / kBN;
+  *n = e > b ? cdiv(e, kBN) - b / kBN : 0;
 }
 
 // A (query tile, key tile) pair needs no per-element test iff every pair in it
 // is visible (rows beyond Sq are never stored, so they do not matter).
 __host__ __device__ inline bool tile_is_full(const MaskGeom& g, int q0, int k0) {
-  if (k0 + kBN > g.kv_main) return false;
-  if (g.kind == kMaskFull) return true;
-  return k0 + kBN - 1 <= q0 - g.shift;
+  if (k0 + kBN > g.kv_len) return false;
+  if ((int64_t)k0 < (int64_t)q0 + kBM - 1 - g.lo) return false;
+  return (int64_t)k0 + kBN - 1 <= (int64_t)q0 + g.hi;
 }
 
-// Per-row column limit inside a key tile: column c (key k0 + c) is visible to
-// query q iff c <= limit.  Negative means nothing visible.
-__host__ __device__ inline int col_limit(const MaskGeom& g, int q, int k0) {
-  long lim = (long)g.kv_main - 1 - k0;
+// Visible columns of query row q inside the key tile at k0: c (key k0 + c)
+// is visible iff *clo <= c <= *chi (empty when *chi < *clo).
+__host__ __device__ inline void col_range(const MaskGeom& g, int q, int k0, int* clo, int* chi) {
+  const int64_t h = (int64_t)q + g.hi < (int64_t)g.kv_len - 1 ? (int64_t)q + g.hi
+                                                              : (int64_t)g.kv_len - 1;
+  *chi = (int)clamp64(h - k0, -1, kBN);
+  *clo = (int)clamp64((int64_t)q - g.lo - k0, 0, kBN);
+}
+
+// Query rows [begin, end) that see some key of the key tile at k0.
+__host__ __device__ inline void q_range_for_kv(const MaskGeom& g, int k0, int* begin, int* end) {
+  if (k0 >= g.kv_len) {
+    *begin = *end = 0;
+    return;
+  }
+  const int64_t kv_last = (k0 + kBN < g.kv_len ? k0 + kBN : g.kv_len) - 1;
+  // q sees kv iff kv - hi <= q <= kv + lo
+  const int64_t e = clamp64(kv_last + g.lo + 1, 0, g.Sq);
+  const int64_t b = clamp64((int64_t)k0 - g.hi, 0, e);
+  *begin = (int)b;
+  *end = (int)e;
+}
+
+// Visible query columns of key row kv inside the query tile starting at q0:
+// column c (query q0 + c) is visible iff *clo <= c <= *chi.
+__host__ __device__ inline void row_range_for_kv(const MaskGeom& g, int kv, int q0, int* clo,
+                                                 int* chi) {
+  if (kv >= g.kv_len) {
+    *clo = kBM;
+    *chi = -1;
+    return;
+  }
+  *clo = (int)clamp64((int64_t)kv - g.hi - q0, 0, kBM);
+  *chi = (int)clamp64((int64_t)kv + g.lo - q0, -1, kBM);
+}
+
+// tile_is_full folded into a range, for the kernels' inner loops: with the
+// query tile fixed (forward, dQ), the key tile at k0 is full iff
+// lo <= k0 <= hi; with the key tile fixed (dK/dV), the query tile at q0 is
+// full iff lo <= q0 <= hi.  The two numbers depend on tile indices only (the
+// compiler can keep them in uniform registers); the per-row bounds of partial
+// tiles come from col_range / row_range_for_kv inside the rare masked branch.
+struct FullRange {
+  int lo, hi;
+};
+
+__host__ __device__ inline int clamp_int(int64_t x) {
+  return (int)clamp64(x, -(int64_t)kUnbounded, (int64_t)kUnbounded);
+}
+
+// Key tiles k0 that are full for the query tile at qt0:
+// k0 + kBN <= kv_len, k0 >= qt0 + kBM - 1 - lo, k0 + kBN - 1 <= qt0 + hi.
+__host__ __device__ inline FullRange full_keys_for_rows(const MaskGeom& g, int qt0) {
+  const int64_t a = (int64_t)qt0 + g.hi - (kBN - 1), b = (int64_t)g.kv_len - kBN;
+  return FullRange{clamp_int((int64_t)qt0 + kBM - 1 - g.lo), clamp_int(a < b ? a : b)};
+}
+// Query tiles q0 that are full for the key tile at k0 (none when it runs past kv_len).
+__host__ __device__ inline FullRange full_rows_for_keys(const MaskGeom& g, int k0) {
+  if (k0 + kBN > g.kv_len) return FullRange{kUnbounded, -kUnbounded};
+  return FullRange{clamp_int((int64_t)k0 + kBN - 1 - g.hi),
+                   clamp_int((int64_t)k0 + g.lo - (kBM - 1))};
+}
+__host__ __device__ inline bool in_range(const FullRange& r, int x) { return x >= r.lo && x <= r.hi; }
+
+// The one-sided forms: masks without a lower key bound (full, causal, TTT) and
+// without per-batch key lengths (kv_len == kv_main).  The kernels are
+// instantiated for this case of their own, so that the general window and
+// length arithmetic costs the common masks nothing; they agree with the
+// general functions above whenever lo is unbounded and kv_len == kv_main.
+__host__ __device__ inline int upper_kv_end(const MaskGeom& g, int q0, int rows) {
+  int64_t last_q = (int64_t)q0 + rows - 1;
+  if (last_q > g.Sq - 1) last_q = g.Sq - 1;
+  return (int)clamp64(last_q + g.hi + 1, 0, g.kv_main);
+}
+__host__ __device__ inline bool upper_tile_full(const MaskGeom& g, int q0, int k0) {
+  if (k0 + kBN > g.kv_main) return false;
+  return g.kind == kMaskFull || (int64_t)k0 + kBN - 1 <= (int64_t)q0 + g.hi;
+}
+// Column c of the key tile at k0 is visible to query q iff c <= the limit.
+__host__ __device__ inline int upper_col_limit(const MaskGeom& g, int q, int k0) {
+  int64_t lim = (int64_t)g.kv_main - 1 - k0;
   if (g.kind != kMaskFull) {
-    long c = (long)q - g.shift - k0;
+    const int64_t c = (int64_t)q + g.hi - k0;
     if (c < lim) lim = c;
   }
-  if (lim < -1) lim = -1;
-  if (lim > kBN) lim = kBN;
-  return (int)lim;
+  return (int)clamp64(lim, -1, kBN);
 }
-
-// First query row that can see any key of the key tile starting at k0.
-__host__ __device__ inline int q_begin_for_kv(const MaskGeom& g, int k0) {
+// First query row that sees key row kv (all of them for the full mask).
+__host__ __device__ inline int upper_q_begin(const MaskGeom& g, int kv) {
   if (g.kind == kMaskFull) return 0;
-  long b = (long)k0 + g.shift;
-  return b > g.Sq ? g.Sq : (int)b;
+  return (int)clamp64((int64_t)kv - g.hi, 0, g.Sq);
 }
 
 // Tile class for the test-only mask-pattern export: 0 empty, 1 partial, 2 full.
 __host__ __device__ inline int tile_class(const MaskGeom& g, int q0, int k0) {
-  const int end = kv_end_for_rows(g, q0, kBM);
-  if (k0 >= end) return 0;
+  int b, e;
+  kv_range_for_rows(g, q0, kBM, &b, &e);
+  if (k0 >= e || k0 + kBN <= b) return 0;
   return tile_is_full(g, q0, k0) ? 2 : 1;
 }
 

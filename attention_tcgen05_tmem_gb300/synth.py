@@ -12,8 +12,9 @@ consume the rounded values; the oracle widens them to fp64.
 The shapes follow the pages' workloads: the CS336 README's benchmark grid
 (B=8, one head, d in {16, 32, 64}, S in {256, 1024, 4096}), the SpecForge
 post's long-context EAGLE3 training (16K tokens, GQA, TTT steps that append
-K/V segments) and HOT-Step's DiT trainer geometries (full self-attention and
-cross-attention with a short encoder sequence).
+K/V segments, padded batches with per-sequence lengths) and HOT-Step's DiT
+trainer geometries (windowed and full self-attention, cross-attention with a
+short encoder sequence).  Per-batch key lengths are fixed tuples, not draws.
 """
 from __future__ import annotations
 
@@ -21,7 +22,7 @@ from dataclasses import dataclass, replace
 
 import torch
 
-MASKS = ("full", "causal", "ttt")
+MASKS = ("full", "causal", "ttt", "window")
 
 
 @dataclass(frozen=True)
@@ -33,9 +34,11 @@ class Workload:
     Sq: int
     Skv: int
     D: int
-    mask: str  # "full" | "causal" | "ttt"
+    mask: str  # "full" | "causal" | "ttt" | "window"
     ttt_step: int = 0
     seed: int = 0
+    window: tuple | None = None       # (left, right) extents of the window mask
+    seq_lengths: tuple | None = None  # per-batch key lengths (padding), None = all keys
 
     @property
     def G(self) -> int:
@@ -49,6 +52,10 @@ class Workload:
              "Skv": self.Skv, "D": self.D, "mask": self.mask}
         if self.mask == "ttt":
             d["ttt_step"] = self.ttt_step
+        if self.window is not None:
+            d["window"] = list(self.window)
+        if self.seq_lengths is not None:
+            d["seq_lengths"] = list(self.seq_lengths)
         return d
 
 
@@ -71,7 +78,22 @@ DIT_SELF = Workload("dit_full_self_B2_H16_S12288_D64", 2, 16, 16, 12288, 12288, 
 DIT_CROSS = Workload("dit_full_cross_B2_H16_Sq12288_Skv512_D64", 2, 16, 16, 12288, 512, 64,
                      "full", 0, 4)
 
-ALL = (TINY,) + SWEEP + (LONG_GQA,) + TTT_STEPS + (DIT_SELF, DIT_CROSS)
+# Windowed self-attention of the DiT geometry (HOT-Step's trainer has windowed,
+# full and cross attention layers; the window extent is not given there: a band
+# of +-1024 keys is taken here) and an LLM-style causal sliding window on the
+# long GQA shape.
+DIT_WINDOW = Workload("dit_window_self_B2_H16_S12288_D64_w1024", 2, 16, 16, 12288, 12288, 64,
+                      "window", 0, 4, window=(1024, 1024))
+SWA_GQA = Workload("swa_causal_gqa_B1_Hq32_Hkv4_S16384_D128_w4096", 1, 32, 4, 16384, 16384, 128,
+                   "window", 0, 2, window=(4095, 0))
+# Padded batches (SpecForge's seq_lengths): causal GQA and a TTT step.
+VARLEN_GQA = Workload("varlen_causal_gqa_B4_Hq32_Hkv4_S8192_D128", 4, 32, 4, 8192, 8192, 128,
+                      "causal", 0, 5, seq_lengths=(8192, 6000, 3100, 1000))
+VARLEN_TTT = Workload("varlen_eagle3_ttt_step2_B2_Hq32_Hkv8_S8192_D128", 2, 32, 8, 8192, 3 * 8192,
+                      128, "ttt", 2, 6, seq_lengths=(8192, 5000))
+
+ALL = ((TINY,) + SWEEP + (LONG_GQA,) + TTT_STEPS + (DIT_SELF, DIT_CROSS) +
+       (DIT_WINDOW, SWA_GQA, VARLEN_GQA, VARLEN_TTT))
 
 # Smaller cases of the same kernels for hardware-counter captures (inputs
 # still larger than the 129 MB L2 once outputs are counted).
@@ -102,6 +124,8 @@ def make_inputs(w: Workload, seed: int | None = None, with_dout: bool = True) ->
     }
     if with_dout:
         out["dout"] = _draw((w.B, w.Hq, w.Sq, w.D), s * 16 + 3)
+    if w.seq_lengths is not None:
+        out["seq_lengths"] = torch.tensor(w.seq_lengths, dtype=torch.int32)
     return out
 
 

@@ -50,7 +50,9 @@ def bench_workloads():
 def headline_names():
     from attention_tcgen05_tmem_gb300 import synth
     return ([synth.TINY.name] + [w.name for w in synth.SWEEP] +
-            [synth.LONG_GQA.name, TTT_ALL, synth.DIT_SELF.name, synth.DIT_CROSS.name])
+            [synth.LONG_GQA.name, TTT_ALL, synth.DIT_SELF.name, synth.DIT_CROSS.name,
+             synth.DIT_WINDOW.name, synth.SWA_GQA.name, synth.VARLEN_GQA.name,
+             synth.VARLEN_TTT.name])
 
 
 def parse_args():
@@ -167,27 +169,20 @@ def cpu_sample(ws, target_s: float, inputs=None):
     v = x["v"][:, :groups].double().numpy()
     do = x["dout"][:, :hq].double().numpy()
     t = w.ttt_step
+    lens = w.seq_lengths if w.seq_lengths is not None else (None,) * w.B
+    kw = dict(window=w.window, seq_lengths=w.seq_lengths)
 
-    def pref(n):  # visible pairs of query rows [0, n) of one head
-        if n <= 0:
-            return 0
-        if w.mask == "full":
-            return n * w.Skv
-        if w.mask == "causal":
-            m = min(n, w.Skv)
-            return m * (m + 1) // 2 + max(0, n - w.Skv) * w.Skv
-        k0 = max(0, n - t)
-        return k0 * (k0 + 1) // 2 + t * n
-
-    assert pref(w.Sq) == flops.visible_pairs_per_head(w.mask, w.Sq, w.Skv, t)
+    def pairs(r0):  # visible pairs of query rows [r0, Sq), one q head of every batch entry
+        return sum(flops.visible_pairs_rows(w.mask, w.Sq, w.Skv, t, w.window, L, r0, w.Sq)
+                   for L in lens)
 
     def run(R):
         r0 = w.Sq - R
         t0 = time.perf_counter()
-        oracle.fwd(q, k, v, w.mask, t, rows=(r0, w.Sq))
-        oracle.bwd(q, k, v, do, w.mask, t, rows=(r0, w.Sq))
+        oracle.fwd(q, k, v, w.mask, t, rows=(r0, w.Sq), **kw)
+        oracle.bwd(q, k, v, do, w.mask, t, rows=(r0, w.Sq), **kw)
         dt = time.perf_counter() - t0
-        return dt, 14.0 * w.D * w.B * hq * (pref(w.Sq) - pref(r0))
+        return dt, 14.0 * w.D * hq * pairs(r0)
 
     R = min(w.Sq, 8)
     dt, f = run(R)
@@ -221,8 +216,12 @@ class Case:
         self.b = binding
         self.x = synth.make_inputs(w)
         self.q, self.k, self.v, self.do = (self.x[n].to(dev) for n in ("q", "k", "v", "dout"))
+        # per-batch key lengths stay on the device for the whole run (the problem
+        # holds their address)
+        self.lens = self.x["seq_lengths"].to(dev) if "seq_lengths" in self.x else None
         odt = torch.float32 if out == "fp32" else torch.bfloat16
-        self.p = binding.problem(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.mask, w.ttt_step, 0.0, out)
+        self.p = binding.problem(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.mask, w.ttt_step, 0.0, out,
+                                 w.window, self.lens)
         binding.check_supported(self.p)
         self.o = torch.empty(self.q.shape, dtype=odt, device=dev)
         self.lse = torch.empty(w.B, w.Hq, w.Sq, dtype=torch.float32, device=dev)
@@ -304,7 +303,8 @@ def run_ours(args, ws, local_rank, dist):
         # outputs (O, LSE, dQ, dK, dV) copied out inside the timed region
         hosts = []
         for c in cases:
-            pin = {n: c.x[n].pin_memory() for n in ("q", "k", "v", "dout")}
+            pin = {n: c.x[n].pin_memory() for n in ("q", "k", "v", "dout", "seq_lengths")
+                   if n in c.x}
             outs = {n: torch.empty(getattr(c, n).shape, dtype=getattr(c, n).dtype).pin_memory()
                     for n in ("o", "lse", "dq", "dk", "dv")}
             hosts.append((pin, outs))
@@ -317,6 +317,8 @@ def run_ours(args, ws, local_rank, dist):
                 c.k.copy_(pin["k"], non_blocking=True)
                 c.v.copy_(pin["v"], non_blocking=True)
                 c.do.copy_(pin["dout"], non_blocking=True)
+                if c.lens is not None:
+                    c.lens.copy_(pin["seq_lengths"], non_blocking=True)
                 binding.fwd_raw(c.p, c.q, c.k, c.v, c.o, c.lse, stream.cuda_stream)
                 binding.bwd_raw(c.p, c.q, c.k, c.v, c.o, c.do, c.lse, c.dq, c.dk, c.dv, c.ws,
                                 stream.cuda_stream)
@@ -370,7 +372,7 @@ def kernel_flops(ws, name):
     tot = 0
     for w in ws:
         nvis = flops.visible_pairs(w)
-        ndiag = w.B * w.Hq * (w.ttt_step * w.Sq if w.mask == "ttt" else 0)
+        ndiag = flops.diagonal_pairs(w)
         per = {"fwd": 4 * nvis, "bwd_dkdv": 8 * (nvis - ndiag), "bwd_dq": 6 * nvis,
                "ttt_diag_bwd": 8 * ndiag, "bwd_prep": 0}[name]
         tot += per * w.D

@@ -17,7 +17,8 @@
  * GQA: q head h reads kv head h / (Hq / Hkv); dK and dV of a kv head are the
  * sum over its q heads, accumulated in ascending head order.
  * A query row that sees no key gets O = 0 and LSE = 0 (HOT-Step section 6,
- * trap 9); none of the three masks produces such a row for a valid problem.
+ * trap 9); full, causal and TTT masks produce such rows only through the
+ * per-batch key lengths, a window mask also through its extents.
  *
  * Masks (SpecForge post, "Flex Attention", eagle3 mask_mod):
  *   ATTN_MASK_FULL    every key visible (self- or cross-attention, Skv != Sq ok)
@@ -27,6 +28,13 @@
  *                     kv <= q - t (the causal part shrinks one diagonal per
  *                     appended segment) plus key i*Sq + q of each appended
  *                     segment i = 1..t (one diagonal entry each).
+ *   ATTN_MASK_WINDOW  the band q - window_left <= kv <= q + window_right (the
+ *                     HOT-Step page's windowed self-attention, section 4);
+ *                     (w, 0) is a causal sliding window, (w, w) a symmetric one.
+ * Per-batch key lengths (the padding terms of the eagle3 mask_mod): with
+ * seq_lengths set, keys kv >= seq_lengths[b] of batch entry b are invisible
+ * (for TTT: segment-0 keys kv >= seq_lengths[b], and the suffix diagonals of
+ * rows q >= seq_lengths[b]); their dK and dV are 0.
  *
  * Layout and types
  * ----------------
@@ -70,7 +78,8 @@ extern "C" {
 typedef enum {
   ATTN_MASK_FULL = 0,
   ATTN_MASK_CAUSAL = 1,
-  ATTN_MASK_TTT = 2
+  ATTN_MASK_TTT = 2,
+  ATTN_MASK_WINDOW = 3
 } attn_mask_kind;
 
 typedef enum {
@@ -97,18 +106,26 @@ typedef enum { ATTN_OUT_BF16 = 0, ATTN_OUT_F32 = 1 } attn_out_dtype;
  * (ignored otherwise); scale <= 0 selects 1/sqrt(D); out_dtype is an
  * attn_out_dtype for O (forward output and backward input), dQ, dK and dV.
  * fp32 outputs avoid the bf16 rounding of large GQA gradient sums (a bf16
- * value of magnitude 8 is only good to 2^-5). */
+ * value of magnitude 8 is only good to 2^-5).  window_left / window_right are
+ * the extents of ATTN_MASK_WINDOW (>= 0; must be 0 for the other masks).
+ * seq_lengths: NULL, or a device array of B int32 key lengths (4-byte
+ * aligned, read by the kernels; values are clamped to [0, Skv], to [0, Sq]
+ * for TTT). */
 typedef struct {
   int B, Hq, Hkv, Sq, Skv, D;
   int mask;
   int ttt_step;
   float scale;
   int out_dtype;
+  int window_left, window_right;
+  const int32_t* seq_lengths;
 } attn_problem;
 
 /* Whether the problem is supported.  Pure host check, no side effects.
  * Requires B, Hq, Hkv, Sq, Skv > 0, Hq % Hkv == 0, D in {16, 32, 64, 128},
- * a known mask, ttt_step >= 0 and Skv == (ttt_step + 1) * Sq for TTT. */
+ * a known mask, ttt_step >= 0 and Skv == (ttt_step + 1) * Sq for TTT,
+ * window extents >= 0 for ATTN_MASK_WINDOW (0 otherwise), and a 4-byte
+ * aligned seq_lengths pointer. */
 attn_status attn_train_supports(const attn_problem* p);
 
 /* Bytes of device workspace attn_train_bwd needs: the fp32 Delta row

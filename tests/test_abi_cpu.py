@@ -50,7 +50,8 @@ def _status(lib, p):
 def test_supports_accepts_the_workloads(lib):
     from attention_tcgen05_tmem_gb300 import synth
     for w in synth.ALL:
-        p = binding.problem(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.mask, w.ttt_step)
+        p = binding.problem(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.mask, w.ttt_step,
+                            window=w.window)
         assert _status(lib, p) == 0, (w.name, lib.attn_train_last_error())
 
 
@@ -59,11 +60,22 @@ def test_supports_accepts_the_workloads(lib):
     (dict(B=0), 1), (dict(Sq=-1), 1), (dict(mask=7), 2),
     (dict(mask="ttt", ttt_step=2, Skv=256), 1), (dict(mask="ttt", ttt_step=-1), 1),
     (dict(scale=float("nan")), 1),
+    (dict(mask="window", window=(-1, 4)), 1), (dict(mask="window", window=(3, -2)), 1),
+    (dict(mask="causal", window=(3, 0)), 1),
 ])
 def test_supports_rejects(lib, kw, status):
     p = _p(**kw)
     assert _status(lib, p) == status
     assert lib.attn_train_last_error()
+
+
+def test_misaligned_seq_lengths_are_rejected(lib):
+    p = _p()
+    p.seq_lengths = 0x1002
+    assert _status(lib, p) == 3
+    p.seq_lengths = 0x1004
+    assert _status(lib, p) == 0
+    assert _status(lib, _p(mask="window", window=(0, 0))) == 0
 
 
 def test_workspace_size(lib):

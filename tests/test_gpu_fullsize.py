@@ -16,18 +16,22 @@ def run_sampled(w, b_idx=(0,), groups=(0,), out="fp32"):
     dev = device()
     x = synth.make_inputs(w)
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
-    o, lse = binding.fwd(q, k, v, w.mask, w.ttt_step, out=out)
-    dq, dk, dv = binding.bwd(q, k, v, o, lse, do, w.mask, w.ttt_step)
+    lens = x["seq_lengths"].to(dev) if "seq_lengths" in x else None
+    kw = dict(window=w.window, seq_lengths=lens)
+    o, lse = binding.fwd(q, k, v, w.mask, w.ttt_step, out=out, **kw)
+    dq, dk, dv = binding.bwd(q, k, v, o, lse, do, w.mask, w.ttt_step, **kw)
     binding.device_status()
     G = w.G
     for b in b_idx:
+        rkw = dict(window=w.window,
+                   seq_lengths=None if w.seq_lengths is None else [w.seq_lengths[b]])
         for g in groups:
             hs = slice(g * G, (g + 1) * G)
             sub = {n: x[n][b:b + 1, hs] for n in ("q", "dout")}
             sub.update({n: x[n][b:b + 1, g:g + 1] for n in ("k", "v")})
-            ro, rl = oracle.fwd(sub["q"], sub["k"], sub["v"], w.mask, w.ttt_step)
+            ro, rl = oracle.fwd(sub["q"], sub["k"], sub["v"], w.mask, w.ttt_step, **rkw)
             rdq, rdk, rdv = oracle.bwd(sub["q"], sub["k"], sub["v"], sub["dout"], w.mask,
-                                       w.ttt_step)
+                                       w.ttt_step, **rkw)
             tag = f"{w.name}[b={b},kv={g}]"
             compare(tag + " O", o[b:b + 1, hs], ro)
             compare(tag + " LSE", lse[b:b + 1, hs], rl, atol=LSE_ATOL, rel_l2=1e-3)
@@ -59,6 +63,20 @@ def test_dit_cross_full_size():
 @pytest.mark.timeout(1800)
 def test_dit_self_full_size():
     run_sampled(synth.DIT_SELF, b_idx=(1,), groups=(3,))
+
+
+@pytest.mark.gpu
+@pytest.mark.timeout(1800)
+def test_window_full_size():
+    run_sampled(synth.DIT_WINDOW, b_idx=(1,), groups=(5,))
+    run_sampled(synth.SWA_GQA, groups=(3,))
+
+
+@pytest.mark.gpu
+@pytest.mark.timeout(1800)
+def test_varlen_full_size():
+    run_sampled(synth.VARLEN_GQA, b_idx=(1, 3), groups=(2,))
+    run_sampled(synth.VARLEN_TTT, b_idx=(1,), groups=(0,))
 
 
 @pytest.mark.gpu

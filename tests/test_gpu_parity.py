@@ -16,24 +16,27 @@ def run_both(w: synth.Workload, check_bwd=True, out="fp32"):
     dev = device()
     x = synth.make_inputs(w)
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
-    o, lse = binding.fwd(q, k, v, w.mask, w.ttt_step, out=out)
+    lens = x["seq_lengths"].to(dev) if "seq_lengths" in x else None
+    kw = dict(window=w.window, seq_lengths=lens)
+    rkw = dict(window=w.window, seq_lengths=w.seq_lengths)
+    o, lse = binding.fwd(q, k, v, w.mask, w.ttt_step, out=out, **kw)
     binding.device_status()
-    ro, rl = oracle.fwd(x["q"], x["k"], x["v"], w.mask, w.ttt_step)
+    ro, rl = oracle.fwd(x["q"], x["k"], x["v"], w.mask, w.ttt_step, **rkw)
     compare("O", o, ro)
     compare("LSE", lse, rl, atol=LSE_ATOL, rel_l2=1e-3)
     if not check_bwd:
         return
-    dq, dk, dv = binding.bwd(q, k, v, o, lse, do, w.mask, w.ttt_step)
+    dq, dk, dv = binding.bwd(q, k, v, o, lse, do, w.mask, w.ttt_step, **kw)
     binding.device_status()
-    rdq, rdk, rdv = oracle.bwd(x["q"], x["k"], x["v"], x["dout"], w.mask, w.ttt_step)
+    rdq, rdk, rdv = oracle.bwd(x["q"], x["k"], x["v"], x["dout"], w.mask, w.ttt_step, **rkw)
     assert np.abs(rdq).max() > 1e-3  # non-vacuous (HOT-Step trap 7)
     compare("dQ", dq, rdq)
     compare("dK", dk, rdk)
     compare("dV", dv, rdv)
 
 
-def W(name, B, Hq, Hkv, Sq, Skv, D, mask, t=0, seed=11):
-    return synth.Workload(name, B, Hq, Hkv, Sq, Skv, D, mask, t, seed)
+def W(name, B, Hq, Hkv, Sq, Skv, D, mask, t=0, seed=11, window=None, lens=None):
+    return synth.Workload(name, B, Hq, Hkv, Sq, Skv, D, mask, t, seed, window, lens)
 
 
 CASES = [
@@ -54,6 +57,20 @@ CASES = [
     W("ttt_t3", 1, 4, 1, 257, 1028, 128, "ttt", 3),
     W("ttt_t6_d64", 1, 2, 1, 200, 1400, 64, "ttt", 6),
     W("ttt_t2_tiny", 1, 2, 1, 5, 15, 32, "ttt", 2),
+    # window masks: causal sliding, symmetric, one-sided ahead, narrow (rows that see
+    # nothing when Sq > Skv), across head dims
+    W("window_causal_gqa_d128", 1, 4, 2, 700, 700, 128, "window", window=(200, 0)),
+    W("window_sym_d64", 2, 2, 2, 1000, 1000, 64, "window", window=(130, 130)),
+    W("window_ahead_d32", 1, 2, 1, 520, 520, 32, "window", window=(0, 300)),
+    W("window_narrow_sq_gt_skv_d64", 1, 2, 1, 450, 300, 64, "window", window=(5, 5)),
+    W("window_d16", 2, 2, 2, 384, 384, 16, "window", window=(64, 64)),
+    W("window_wide_equals_full_d128", 1, 2, 2, 300, 300, 128, "window", window=(400, 400)),
+    # per-batch key lengths (padding), including an empty and a one-key batch entry
+    W("varlen_causal_gqa_d128", 3, 4, 2, 600, 600, 128, "causal", lens=(600, 333, 1)),
+    W("varlen_full_cross_d64", 2, 2, 2, 500, 300, 64, "full", lens=(300, 129)),
+    W("varlen_window_d64", 2, 2, 1, 640, 640, 64, "window", window=(100, 20), lens=(640, 250)),
+    W("varlen_ttt_t2_d128", 2, 4, 2, 384, 1152, 128, "ttt", 2, lens=(384, 200)),
+    W("varlen_empty_entry_d64", 2, 2, 2, 256, 256, 64, "causal", lens=(0, 256)),
 ]
 
 

@@ -235,3 +235,20 @@ def test_window_rows_that_see_nothing():
     np.testing.assert_allclose(o[0, 0, :4], v[0, 0], rtol=0, atol=1e-15)
     np.testing.assert_allclose(lse[0, 0, :4], 0.5 * (q[0, 0, :4] * k[0, 0]).sum(-1), rtol=0,
                                atol=1e-14)
+
+
+# ------------------------------------------------ mask-aware pair counts
+@pytest.mark.parametrize("mask,Sq,Skv,t,window,length", [
+    ("window", 300, 300, 0, (40, 0), None), ("window", 300, 300, 0, (17, 17), 211),
+    ("window", 200, 450, 0, (0, 90), None), ("window", 450, 200, 0, (90, 3), 150),
+    ("causal", 300, 300, 0, None, 123), ("causal", 200, 350, 0, None, 300),
+    ("full", 100, 77, 0, None, 50), ("ttt", 64, 192, 2, None, 40), ("ttt", 64, 256, 3, None, 0),
+])
+def test_pair_counts_with_window_and_lengths(mask, Sq, Skv, t, window, length):
+    from attention_tcgen05_tmem_gb300 import flops
+    want = oracle.count_visible(mask, t, Sq, Skv, window=window, length=length)
+    assert flops.visible_pairs_per_head(mask, Sq, Skv, t, window, length) == want
+    # and the per-row sums that the CPU-baseline sample uses
+    got = sum(flops.visible_pairs_rows(mask, Sq, Skv, t, window, length, r, r + 1)
+              for r in range(Sq))
+    assert got == want
