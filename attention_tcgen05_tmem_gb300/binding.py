@@ -23,7 +23,8 @@ STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID", 2: "ATTN_ERR_UNSUPPORTED", 3: "AT
 # Entry points of include/attn_train.h (checked against the header by the tests).
 EXPORTS = ("attn_train_supports", "attn_train_workspace_size", "attn_train_fwd", "attn_train_bwd",
            "attn_train_bwd_passes", "attn_train_bwd_noalloc", "attn_train_last_error", "attn_train_device_status", "attn_train_set_wait_budget_ns",
-           "attn_train_mask_pattern", "attn_train_probe_mma", "attn_train_selftest_wait_timeout")
+           "attn_train_mask_pattern", "attn_train_probe_mma", "attn_train_selftest_wait_timeout",
+           "attn_train_logsoftmax_loss_fwd", "attn_train_logsoftmax_loss_bwd")
 
 
 class AttnError(RuntimeError):
@@ -80,6 +81,12 @@ def load(path: str = LIB_PATH):
             "attn_train_mask_pattern": (st, [P, vp, vp, vp]),
             "attn_train_probe_mma": (st, [ctypes.c_int, ctypes.c_int, vp, vp, vp, vp]),
             "attn_train_selftest_wait_timeout": (st, [vp]),
+            "attn_train_logsoftmax_loss_fwd": (st, [ctypes.c_int64, ctypes.c_int64, vp,
+                                                    ctypes.c_int64, vp, ctypes.c_int64, vp,
+                                                    vp, vp, vp, vp, vp]),
+            "attn_train_logsoftmax_loss_bwd": (st, [ctypes.c_int64, ctypes.c_int64, vp,
+                                                    ctypes.c_int64, vp, ctypes.c_int64, vp,
+                                                    vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -262,3 +269,57 @@ def probe_mma(mode: int, a, b, D: int):
 
 def selftest_wait_timeout():
     _check(load().attn_train_selftest_wait_timeout(_stream(None)))
+
+
+# ------------------------------------------------- soft-target log-softmax loss
+def _rows2d(t, name):
+    """[..., V] fp32 CUDA tensor -> (rows, V, row stride) with the last dim contiguous."""
+    import torch
+    if t.dtype != torch.float32 or not t.is_cuda:
+        raise ValueError(f"{name} must be a float32 CUDA tensor")
+    if t.stride(-1) != 1:
+        raise ValueError(f"{name}: the vocabulary dimension must be contiguous")
+    V = t.shape[-1]
+    rows = t.numel() // V
+    ld = t.stride(-2) if t.dim() > 1 else V
+    if t.dim() > 2 and t.stride(0) != t.shape[1] * ld:
+        raise ValueError(f"{name}: leading dimensions must be dense (flattenable to rows)")
+    return rows, V, ld
+
+
+def _ptr(t):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def logsoftmax_loss_fwd_raw(logits, target, mask, row_loss, row_lse, row_tsum, loss=None,
+                            stream=None):
+    rows, V, ldl = _rows2d(logits, "logits")
+    rt, Vt, ldt = _rows2d(target, "target")
+    if (rt, Vt) != (rows, V):
+        raise ValueError("logits and target shapes differ")
+    _check(load().attn_train_logsoftmax_loss_fwd(rows, V, _ptr(logits), ldl, _ptr(target), ldt,
+                                                 _ptr(mask), _ptr(row_loss), _ptr(row_lse),
+                                                 _ptr(row_tsum), _ptr(loss), _stream(stream)))
+
+
+def logsoftmax_loss_bwd_raw(logits, target, mask, row_lse, row_tsum, grad_loss=None, stream=None):
+    rows, V, ldl = _rows2d(logits, "logits")
+    rt, Vt, ldt = _rows2d(target, "target")
+    if (rt, Vt) != (rows, V):
+        raise ValueError("logits and target shapes differ")
+    _check(load().attn_train_logsoftmax_loss_bwd(rows, V, _ptr(logits), ldl, _ptr(target), ldt,
+                                                 _ptr(mask), _ptr(row_lse), _ptr(row_tsum),
+                                                 _ptr(grad_loss), _stream(stream)))
+
+
+def logsoftmax_loss(logits, target, mask=None, stream=None):
+    """Forward: allocates the row statistics and the mean; returns
+    (loss [1], row_loss, row_lse, row_tsum), all fp32 on the logits' device."""
+    import torch
+    rows = logits.numel() // logits.shape[-1]
+    f = dict(dtype=torch.float32, device=logits.device)
+    row_loss, row_lse, row_tsum = (torch.empty(rows, **f) for _ in range(3))
+    loss = torch.empty(1, **f)
+    m = None if mask is None else mask.reshape(-1).to(torch.float32).contiguous()
+    logsoftmax_loss_fwd_raw(logits, target, m, row_loss, row_lse, row_tsum, loss, stream)
+    return loss, row_loss, row_lse, row_tsum

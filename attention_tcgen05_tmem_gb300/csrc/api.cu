@@ -372,6 +372,63 @@ attn_status attn_train_bwd_noalloc(const attn_problem* p, attn_tensor q, attn_te
                         stream);
 }
 
+namespace {
+attn_status check_loss_args(int64_t rows, int64_t V, const void* logits, int64_t ld_logits,
+                            const void* target, int64_t ld_target, const void* mask) {
+  if (rows <= 0 || V <= 0) return fail(ATTN_ERR_INVALID, "rows (%lld) and V (%lld) must be positive",
+                                       (long long)rows, (long long)V);
+  if (rows > 0x7fffffffLL || V > 0x7fffffffLL)
+    return fail(ATTN_ERR_UNSUPPORTED, "rows and V must fit in 31 bits");
+  if (logits == nullptr || target == nullptr)
+    return fail(ATTN_ERR_INVALID, "logits and target must not be NULL");
+  if (ld_logits < V || ld_target < V)
+    return fail(ATTN_ERR_INVALID, "row strides must be >= V");
+  if (reinterpret_cast<uintptr_t>(logits) % 4 != 0 || reinterpret_cast<uintptr_t>(target) % 4 != 0)
+    return fail(ATTN_ERR_ALIGNMENT, "logits and target must be 4-byte aligned");
+  if (reinterpret_cast<uintptr_t>(mask) % 4 != 0)
+    return fail(ATTN_ERR_ALIGNMENT, "mask must be 4-byte aligned");
+  return ATTN_OK;
+}
+bool aligned4(const void* p) { return reinterpret_cast<uintptr_t>(p) % 4 == 0; }
+}  // namespace
+
+attn_status attn_train_logsoftmax_loss_fwd(int64_t rows, int64_t V, const float* logits,
+                                           int64_t ld_logits, const float* target,
+                                           int64_t ld_target, const float* mask,
+                                           float* row_loss, float* row_lse, float* row_tsum,
+                                           float* loss, void* stream) {
+  attn_status st = check_loss_args(rows, V, logits, ld_logits, target, ld_target, mask);
+  if (st != ATTN_OK) return st;
+  if (row_loss == nullptr || row_lse == nullptr || row_tsum == nullptr)
+    return fail(ATTN_ERR_INVALID, "row_loss, row_lse and row_tsum must not be NULL");
+  if (!aligned4(row_loss) || !aligned4(row_lse) || !aligned4(row_tsum) || !aligned4(loss))
+    return fail(ATTN_ERR_ALIGNMENT, "row outputs and loss must be 4-byte aligned");
+  attn::LossArgs a{rows, V, ld_logits, ld_target, logits, nullptr, target, mask,
+                   row_loss, row_lse, row_tsum, loss, nullptr};
+  cudaError_t e = attn::launch_logsoftmax_loss_fwd(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "log-softmax loss forward launch");
+  return ATTN_OK;
+}
+
+attn_status attn_train_logsoftmax_loss_bwd(int64_t rows, int64_t V, float* logits,
+                                           int64_t ld_logits, const float* target,
+                                           int64_t ld_target, const float* mask,
+                                           const float* row_lse, const float* row_tsum,
+                                           const float* grad_loss, void* stream) {
+  attn_status st = check_loss_args(rows, V, logits, ld_logits, target, ld_target, mask);
+  if (st != ATTN_OK) return st;
+  if (row_lse == nullptr || row_tsum == nullptr)
+    return fail(ATTN_ERR_INVALID, "row_lse and row_tsum must not be NULL");
+  if (!aligned4(row_lse) || !aligned4(row_tsum) || !aligned4(grad_loss))
+    return fail(ATTN_ERR_ALIGNMENT, "row statistics and grad_loss must be 4-byte aligned");
+  attn::LossArgs a{rows, V, ld_logits, ld_target, logits, logits, target, mask,
+                   nullptr, const_cast<float*>(row_lse), const_cast<float*>(row_tsum), nullptr,
+                   grad_loss};
+  cudaError_t e = attn::launch_logsoftmax_loss_bwd(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "log-softmax loss backward launch");
+  return ATTN_OK;
+}
+
 const char* attn_train_last_error(void) { return g_msg; }
 
 attn_status attn_train_device_status(void* stream) {

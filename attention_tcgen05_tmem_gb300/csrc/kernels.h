@@ -59,6 +59,22 @@ struct Maps {
   CUtensorMap q, k, v, dout;
 };
 
+// Soft-target log-softmax loss over [rows, V] fp32 logits (loss.cu).
+struct LossArgs {
+  int64_t rows, V, ld_logits, ld_target;  // row strides in elements
+  const float* logits;                    // forward input
+  float* logits_out;                      // backward: logits in, gradient out (in place)
+  const float* target;
+  const float* mask;       // [rows] or null (all ones)
+  float* row_loss;         // [rows]: -sum_v target * log_softmax (before the mask)
+  float* row_lse;          // [rows]: logsumexp of the row
+  float* row_tsum;         // [rows]: sum_v target
+  float* loss;             // [1] mean loss, or null (forward)
+  const float* grad_loss;  // [1] upstream gradient, or null = 1 (backward)
+};
+cudaError_t launch_logsoftmax_loss_fwd(const LossArgs& a, cudaStream_t s);
+cudaError_t launch_logsoftmax_loss_bwd(const LossArgs& a, cudaStream_t s);
+
 cudaError_t launch_fwd(const FwdArgs& a, const Maps& m, cudaStream_t s);
 // passes: mask of 1 = Delta prep, 2 = dK/dV, 4 = dQ, 8 = TTT suffix keys
 cudaError_t launch_bwd(const BwdArgs& a, const Maps& m, unsigned passes, cudaStream_t s);

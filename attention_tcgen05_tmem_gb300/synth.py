@@ -134,3 +134,44 @@ def zero_k(inputs: dict) -> dict:
     d = dict(inputs)
     d["k"] = torch.zeros_like(inputs["k"])
     return d
+
+
+# ------------------------------------------------- soft-target log-softmax loss
+@dataclass(frozen=True)
+class LossWorkload:
+    """The SpecForge post's loss benchmark shapes ("In-place Gradient
+    Calculation", table of (B, T, V)): fp32 logits and soft targets over a
+    vocabulary of V, one position mask per (b, t)."""
+    name: str
+    B: int
+    T: int
+    V: int
+    seed: int = 7
+
+    @property
+    def rows(self) -> int:
+        return self.B * self.T
+
+    def describe(self) -> dict:
+        return {"workload": self.name, "B": self.B, "T": self.T, "V": self.V}
+
+
+LOSS = tuple(LossWorkload(f"logsoftmax_loss_B{B}_T{T}_V{V}", B, T, V)
+             for B, T, V in ((1, 1024, 32000), (1, 4096, 32000), (1, 4096, 64000),
+                             (1, 8192, 32000), (1, 8192, 64000), (1, 16384, 32000)))
+
+
+def make_loss_inputs(w: LossWorkload, rows: slice | None = None) -> dict:
+    """fp32 CPU tensors: logits [B, T, V] ~ 2 N(0, 1); target [B, T, V] = u / sum(u)
+    with u ~ Exp(1) (a point drawn uniformly from the probability simplex, the
+    shape of a teacher's soft distribution); mask [B, T] in {0, 1}, about 10%
+    zeros (padding positions).  Each tensor has its own generator seeded
+    seed * 16 + index."""
+    g = [torch.Generator(device="cpu") for _ in range(3)]
+    for i, gi in enumerate(g):
+        gi.manual_seed(w.seed * 16 + 8 + i)
+    logits = torch.randn(w.B, w.T, w.V, generator=g[0], dtype=torch.float32) * 2.0
+    u = torch.empty(w.B, w.T, w.V, dtype=torch.float32).exponential_(generator=g[1])
+    target = u / u.sum(dim=-1, keepdim=True)
+    mask = (torch.rand(w.B, w.T, generator=g[2]) >= 0.1).to(torch.float32)
+    return {"logits": logits, "target": target, "mask": mask}

@@ -63,7 +63,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=synth.LONG_GQA.name,
-                    help="one of: " + ", ".join(bench_workloads()))
+                    help="one of: " + ", ".join(list(bench_workloads()) + list(loss_table())))
     ap.add_argument("--all", action="store_true", help="one line per workload of the pages")
     ap.add_argument("--out", choices=["fp32", "bf16"], default="fp32",
                     help="dtype of O, dQ, dK, dV (fp32 is the parity-gated configuration)")
@@ -440,6 +440,151 @@ def describe(name, ws, out, n_gpus):
     return cfg
 
 
+# ------------------------------------------- soft-target log-softmax loss
+LOSS_METRIC = "soft-target log-softmax loss fwd+bwd HBM throughput (algorithmic bytes)"
+
+
+def loss_table():
+    from attention_tcgen05_tmem_gb300 import synth
+    return {w.name: w for w in synth.LOSS}
+
+
+def loss_bytes(w):
+    """Algorithmic HBM bytes of one forward + in-place backward over [rows, V]
+    fp32: the forward reads logits and target and writes 3 row statistics; the
+    backward reads logits, target and the statistics and writes the gradient;
+    the mask is read by both."""
+    n, V = w.rows, w.V
+    return n * V * 4 * 2 + n * (4 + 12) + n * V * 4 * 3 + n * (4 + 8)
+
+
+def loss_cpu_sample(w, x, target_s):
+    """The fp64 oracle on the first R rows (R grown to about target_s s);
+    returns (GB/s of the same algorithmic bytes per row, description)."""
+    from oracle import softmax_loss as sl
+    N, V = w.rows, w.V
+    lg = x["logits"].reshape(N, V)
+    tg = x["target"].reshape(N, V)
+    mk = x["mask"].reshape(N)
+    R = 8
+    while True:
+        t0 = time.perf_counter()
+        sl.forward(lg[:R], tg[:R], mk[:R])
+        sl.backward(lg[:R], tg[:R], mk[:R])
+        dt = time.perf_counter() - t0
+        if dt >= 0.5 * target_s or R >= N:
+            break
+        R = int(min(N, max(2 * R, R * target_s / max(dt, 1e-3))))
+    gbs = loss_bytes(w) * R / N / dt / 1e9
+    return gbs, f"fp64 oracle fwd+bwd on the first {R} of {N} rows of {w.name}, {dt:.1f} s"
+
+
+def run_loss(args, w, rank, local_rank, dist, n_gpus, peaks, peak_src):
+    import torch
+
+    from attention_tcgen05_tmem_gb300 import binding, synth
+    from attention_tcgen05_tmem_gb300 import build as lib_build
+
+    lib_build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    x = synth.make_loss_inputs(w)
+    pristine = x["logits"].to(dev)
+    logits = torch.empty_like(pristine)
+    target = x["target"].to(dev)
+    mask = x["mask"].reshape(-1).to(dev)
+    N = w.rows
+    f = dict(dtype=torch.float32, device=dev)
+    row_loss, row_lse, row_tsum, loss = (torch.empty(n, **f) for n in (N, N, N, 1))
+    one = torch.ones(1, **f)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        binding.logsoftmax_loss_fwd_raw(logits, target, mask, row_loss, row_lse, row_tsum, loss,
+                                        stream.cuda_stream)
+        if evs:
+            evs[1].record(stream)
+        binding.logsoftmax_loss_bwd_raw(logits, target, mask, row_lse, row_tsum, one,
+                                        stream.cuda_stream)
+        if evs:
+            evs[2].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        logits.copy_(pristine)
+        step()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(gpu_index_for(local_rank)) as clk:
+        for i in range(K):
+            logits.copy_(pristine)  # the backward overwrote the logits (outside the events)
+            step(evsets[i])
+        torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in evsets) / K
+    bwd_ms = sum(e[1].elapsed_time(e[2]) for e in evsets) / K
+    total_ms, = max_over_ranks([(fwd_ms + bwd_ms) * K], dist, dev)
+    per = total_ms / K
+    B = loss_bytes(w)
+    value = n_gpus * B / (per * 1e-3) / 1e9
+    peak_hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    fwd_bytes = N * w.V * 8 + N * 16
+    bwd_bytes = B - fwd_bytes
+    dom, dom_ms, dom_bytes = ("bwd", bwd_ms, bwd_bytes) if bwd_ms >= fwd_ms else ("fwd", fwd_ms, fwd_bytes)
+    ach = dom_bytes / (dom_ms * 1e-3) / 1e9
+    line = {
+        "metric": LOSS_METRIC, "value": value, "unit": "GB/s", "n_gpus": n_gpus, "steps": K,
+        "warmup": args.warmup, "ms_per_step": per, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": dict(w.describe(), **{"l2": "inputs larger than L2 (no flush needed)",
+                                        "parallelism": f"replicas x{n_gpus}"}),
+        "kernel_ms": {"logsoftmax_loss_fwd": fwd_ms, "logsoftmax_loss_bwd": bwd_ms},
+        "roofline": {"bound": "hbm", "kernel": f"logsoftmax_loss_{dom}", "achieved": ach,
+                     "peak": peak_hbm, "unit": "GB/s", "frac": ach / peak_hbm, "traffic": None,
+                     "peak_kind": f"HBM copy, of {peak_src}"},
+        "gpu_launches": 3 * K,
+        "clocks": clk.summary(),
+    }
+    if not args.no_e2e:
+        pin = {n: x[n].pin_memory() for n in ("logits", "target", "mask")}
+        out_grad = torch.empty(x["logits"].shape, dtype=torch.float32).pin_memory()
+        out_loss = torch.empty(1, dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            logits.copy_(pin["logits"].reshape(logits.shape), non_blocking=True)
+            target.copy_(pin["target"].reshape(target.shape), non_blocking=True)
+            mask.copy_(pin["mask"].reshape(-1), non_blocking=True)
+            step()
+            out_loss.copy_(loss, non_blocking=True)
+            out_grad.copy_(logits.reshape(out_grad.shape), non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        Ke = max(3, min(K, 10))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(Ke):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms, = max_over_ranks([e0.elapsed_time(e1) / Ke], dist, dev)
+        line["e2e"] = {"value": n_gpus * B / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                       "h2d_bytes_per_step": sum(t.numel() * 4 for t in pin.values()),
+                       "d2h_bytes_per_step": out_grad.numel() * 4 + 4}
+    if rank == 0 and n_gpus == 1 and not args.no_cpu_baseline:
+        gbs, desc = loss_cpu_sample(w, x, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     from attention_tcgen05_tmem_gb300 import flops
@@ -449,10 +594,35 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     n_gpus = max(world, 1)
     names = headline_names() if args.all else [args.workload]
+    losses = loss_table()
+    loss_names = [n for n in names if n in losses]
+    if args.all:
+        loss_names = list(losses)
+    names = [n for n in names if n not in losses]
 
     if args.impl == "reference":
         if rank != 0:
             return 0
+        for name in loss_names:
+            from attention_tcgen05_tmem_gb300 import synth
+            w = losses[name]
+            x = synth.make_loss_inputs(w)
+            per, desc = [], ""
+            for i in range(args.warmup + args.steps):
+                gbs, desc = loss_cpu_sample(w, x, 2.0)
+                if i >= args.warmup:
+                    per.append(gbs)
+            value = statistics.median(per)
+            line = {"impl": "reference", "metric": LOSS_METRIC, "value": value, "unit": "GB/s",
+                    "n_gpus": n_gpus, "steps": args.steps, "warmup": args.warmup,
+                    "ms_per_step": loss_bytes(w) / (value * 1e9) * 1e3, "higher_is_better": True,
+                    "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                    "config": w.describe(),
+                    "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                     "sample": desc},
+                    "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                            "d2h_bytes_per_step": 0}}
+            print(json.dumps(line), flush=True)
         for name in names:
             ws = table[name]
             F = sum(flops.flops_fwd_bwd(w) for w in ws)
@@ -487,6 +657,8 @@ def main():
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     peak_hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    for name in loss_names:
+        run_loss(args, losses[name], rank, local_rank, dist, n_gpus, peaks, peak_src)
     for name in names:
         ws = table[name]
         F = sum(flops.flops_fwd_bwd(w) for w in ws)

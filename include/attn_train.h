@@ -195,6 +195,39 @@ attn_status attn_train_bwd_noalloc(const attn_problem* p, attn_tensor q, attn_te
                                    const float* lse, attn_tensor dq, attn_tensor dk,
                                    attn_tensor dv, void* stream);
 
+/* Soft-target log-softmax loss (SpecForge long-context post, "In-place
+ * Gradient Calculation": the EAGLE3 loss of one TTT step),
+ *     loss = -(1/rows) sum_r mask[r] sum_v target[r, v] log_softmax(logits[r])_v
+ * over `rows` positions (B * T) and a vocabulary of V entries.
+ *
+ * Forward.  logits and target: device fp32 [rows, V] with row strides
+ * ld_logits, ld_target >= V (elements), 4-byte aligned; rows that all start
+ * on 16-byte boundaries (strides multiples of 4, 16-byte aligned bases) are
+ * read with 16-byte loads, others with 4-byte loads.
+ * mask: device fp32 [rows], or NULL for all ones.  Outputs (device fp32, 4-byte
+ * aligned): row_loss [rows] = -sum_v target log_softmax (before the mask),
+ * row_lse [rows] = logsumexp of the row (the page's m + ln d), row_tsum [rows]
+ * = sum_v target, and loss [1] = the mean (NULL: not computed).  One pass over
+ * logits and target; fixed-order reductions (bitwise reproducible).
+ * Kernels: one per-row pass and, for loss, one single-block mean. */
+attn_status attn_train_logsoftmax_loss_fwd(int64_t rows, int64_t V, const float* logits,
+                                           int64_t ld_logits, const float* target,
+                                           int64_t ld_target, const float* mask,
+                                           float* row_loss, float* row_lse, float* row_tsum,
+                                           float* loss, void* stream);
+
+/* Backward, in place: overwrites logits [rows, V] with dloss/dlogits times
+ * grad_loss[0] (device fp32 scalar; NULL = 1):
+ *     logits[r, v] <- -(grad_loss mask[r] / rows) (target[r, v]
+ *                     - softmax(logits[r])_v row_tsum[r])
+ * using row_lse and row_tsum from the forward on the same logits.  Masked rows
+ * become 0.  Same layout rules as the forward.  One kernel. */
+attn_status attn_train_logsoftmax_loss_bwd(int64_t rows, int64_t V, float* logits,
+                                           int64_t ld_logits, const float* target,
+                                           int64_t ld_target, const float* mask,
+                                           const float* row_lse, const float* row_tsum,
+                                           const float* grad_loss, void* stream);
+
 /* Message for the calling thread's last non-OK status ("" if none). */
 const char* attn_train_last_error(void);
 
