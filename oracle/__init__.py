@@ -14,7 +14,9 @@ arrays.  Every function follows the plain definition of attention:
   appended TTT segments), Q_LEN = Sq and KV_LEN = (t+1) Sq; its padding terms
   take optional per-batch key lengths ``seq_lengths``.
 * HOT-Step flash-attn-training, section 4 ("windowed self" attention): the
-  window mask, read as the band q - left <= kv <= q + right.
+  window mask, read as the band q - left <= kv <= q + right; section 3: an
+  optional additive mask [B or 1, Sq, Skv] added to the scaled scores
+  (-inf hides a pair), shared by every head.
 * CS336 README, "Flash Attention (Triton)": LSE saved by the forward; the
   backward recomputes P from it.
 * HOT-Step flash-attn-training, section 6 trap 9: a row with no visible key
@@ -68,7 +70,8 @@ def _load():
             lib.oracle_visible.argtypes = [ctypes.c_int, ctypes.c_int] + [L] * 7
             lib.oracle_mask.restype = None
             lib.oracle_mask.argtypes = [ctypes.c_int, ctypes.c_int] + [L] * 5 + [ctypes.c_void_p]
-            geom = [ctypes.c_int, ctypes.c_int, L, L, ctypes.c_void_p]  # mask, t, wl, wr, lens
+            # mask, t, wl, wr, lens, additive mask, its batch stride
+            geom = [ctypes.c_int, ctypes.c_int, L, L, ctypes.c_void_p, dp, L]
             lib.oracle_fwd.restype = ctypes.c_int
             lib.oracle_fwd.argtypes = [ctypes.c_int] * 3 + [L, L, ctypes.c_int] + geom + [
                 ctypes.c_double] + [dp] * 5
@@ -160,8 +163,22 @@ def _lens(seq_lengths, B):
     return a, a.ctypes.data_as(ctypes.c_void_p)
 
 
+def _add(add_mask, B, Sq, Skv):
+    """fp64 [Bm, Sq, Skv] copy of an additive mask (Bm = 1 or B), a pointer to it
+    and its batch stride."""
+    if add_mask is None:
+        return None, None, 0
+    a = _f64(add_mask)
+    if a.ndim == 2:
+        a = a[None]
+    if a.shape[1:] != (Sq, Skv) or a.shape[0] not in (1, B):
+        raise ValueError("additive mask must be [Sq, Skv], [1, Sq, Skv] or [B, Sq, Skv]")
+    a = np.ascontiguousarray(a)
+    return a, _ptr(a), (0 if a.shape[0] == 1 else Sq * Skv)
+
+
 def fwd(q, k, v, mask="causal", t: int = 0, scale: float | None = None, rows=None,
-        window=None, seq_lengths=None):
+        window=None, seq_lengths=None, add_mask=None):
     """Returns (O [B,Hq,Sq,D], LSE [B,Hq,Sq]) in fp64.  rows=(begin, end)
     restricts the work to those query rows (others stay zero); window=(left,
     right) for the window mask; seq_lengths = per-batch key lengths."""
@@ -171,18 +188,19 @@ def fwd(q, k, v, mask="causal", t: int = 0, scale: float | None = None, rows=Non
     r0, r1 = (0, Sq) if rows is None else rows
     wl, wr = _window(window)
     keep, lens = _lens(seq_lengths, B)
+    akeep, aptr, asb = _add(add_mask, B, Sq, Skv)
     o = np.zeros((B, Hq, Sq, D))
     lse = np.zeros((B, Hq, Sq))
-    rc = _load().oracle_fwd_rows(B, Hq, Hkv, Sq, Skv, D, _mask_id(mask), t, wl, wr, lens, scale,
-                                 _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), r0, r1)
-    del keep
+    rc = _load().oracle_fwd_rows(B, Hq, Hkv, Sq, Skv, D, _mask_id(mask), t, wl, wr, lens, aptr,
+                                 asb, scale, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), r0, r1)
+    del keep, akeep
     if rc != 0:
         raise ValueError(f"oracle_fwd rejected the problem (code {rc})")
     return o, lse
 
 
 def bwd(q, k, v, do, mask="causal", t: int = 0, scale: float | None = None, rows=None,
-        window=None, seq_lengths=None):
+        window=None, seq_lengths=None, add_mask=None):
     """Returns (dQ, dK, dV) in fp64; dK/dV summed over each kv head's q heads.
     rows=(begin, end) restricts the work to those query rows: dQ of those
     rows and their contributions to dK/dV."""
@@ -192,13 +210,14 @@ def bwd(q, k, v, do, mask="causal", t: int = 0, scale: float | None = None, rows
     r0, r1 = (0, Sq) if rows is None else rows
     wl, wr = _window(window)
     keep, lens = _lens(seq_lengths, B)
+    akeep, aptr, asb = _add(add_mask, B, Sq, Skv)
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
-    rc = _load().oracle_bwd_rows(B, Hq, Hkv, Sq, Skv, D, _mask_id(mask), t, wl, wr, lens, scale,
-                                 _ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
-                                 r0, r1)
-    del keep
+    rc = _load().oracle_bwd_rows(B, Hq, Hkv, Sq, Skv, D, _mask_id(mask), t, wl, wr, lens, aptr, asb,
+                                 scale, _ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk),
+                                 _ptr(dv), r0, r1)
+    del keep, akeep
     if rc != 0:
         raise ValueError(f"oracle_bwd rejected the problem (code {rc})")
     return dq, dk, dv

@@ -26,6 +26,11 @@
  * page's "windowed self" attention, section 4, read as q - left <= kv <=
  * q + right) takes its two extents from the caller.
  *
+ * Additive mask (HOT-Step section 3: the ops take "any additive mask"
+ * [S_kv, S], or [S_kv, S, 1, B] broadcast): an optional M[b][q][kv] added to
+ * the scaled scores of the pairs the mask kind admits; M = -inf hides the
+ * pair.  One M per batch entry (or one for all), shared by every head.
+ *
  * For every (b, h) and query row q:
  *     s[kv]  = scale * sum_d Q[q,d] K[kv,d]        (visible kv only)
  *     LSE[q] = log sum_kv exp(s[kv])               (two-pass: max, then sum)
@@ -94,6 +99,8 @@ typedef struct {
     int mask, t;
     long wl, wr;
     const int *seq_lengths; /* [B] or NULL */
+    const double *add;      /* additive mask [B or 1][Sq][Skv], or NULL */
+    long add_sb;            /* batch stride of add in elements (0: one for all) */
 } geom_t;
 
 static long batch_len(const geom_t *g, int b)
@@ -104,19 +111,21 @@ static long batch_len(const geom_t *g, int b)
 /* One query row: fills s[] (scaled scores, -INFINITY where invisible) and
  * returns the number of visible keys; *lse gets log sum exp(s) (0 if none). */
 static long row_scores(const double *qrow, const double *Kh, long Skv, int D, double scale,
-                       const geom_t *g, long len, long Sq, long q, double *s, double *lse)
+                       const geom_t *g, int b, long len, long Sq, long q, double *s, double *lse)
 {
     long nvis = 0;
     double mx = -INFINITY;
+    const double *arow = g->add ? g->add + (long)b * g->add_sb + q * Skv : NULL;
     for (long kv = 0; kv < Skv; ++kv) {
-        if (!oracle_visible(g->mask, g->t, g->wl, g->wr, len, Sq, Skv, q, kv)) {
+        if (!oracle_visible(g->mask, g->t, g->wl, g->wr, len, Sq, Skv, q, kv) ||
+            (arow && arow[kv] == -INFINITY)) {
             s[kv] = -INFINITY;
             continue;
         }
         const double *krow = Kh + kv * (long)D;
         double acc = 0.0;
         for (int d = 0; d < D; ++d) acc += qrow[d] * krow[d];
-        s[kv] = scale * acc;
+        s[kv] = scale * acc + (arow ? arow[kv] : 0.0);
         if (s[kv] > mx) mx = s[kv];
         ++nvis;
     }
@@ -147,11 +156,11 @@ static int check_shape(int B, int Hq, int Hkv, long Sq, long Skv, int D, const g
 /* Forward over query rows [q_begin, q_end) of every (b, h): O [B,Hq,Sq,D],
  * LSE [B,Hq,Sq] (other rows untouched).  Returns 0 on success. */
 int oracle_fwd_rows(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t, long wl,
-                    long wr, const int *seq_lengths, double scale, const double *Q,
-                    const double *K, const double *V, double *O, double *LSE, long q_begin,
-                    long q_end)
+                    long wr, const int *seq_lengths, const double *add, long add_sb, double scale,
+                    const double *Q, const double *K, const double *V, double *O, double *LSE,
+                    long q_begin, long q_end)
 {
-    const geom_t g = {mask, t, wl, wr, seq_lengths};
+    const geom_t g = {mask, t, wl, wr, seq_lengths, add, add_sb};
     if (check_shape(B, Hq, Hkv, Sq, Skv, D, &g)) return 1;
     if (q_begin < 0 || q_end > Sq || q_begin > q_end) return 1;
     const int G = Hq / Hkv;
@@ -175,8 +184,8 @@ int oracle_fwd_rows(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, 
                 double *Lh = LSE + ((long)b * Hq + h) * Sq;
                 for (long q = q_begin; q < q_end; ++q) {
                     double lse;
-                    long nvis = row_scores(Qh + q * D, Kh, Skv, D, scale, &g, batch_len(&g, b), Sq,
-                                           q, s, &lse);
+                    long nvis = row_scores(Qh + q * D, Kh, Skv, D, scale, &g, b, batch_len(&g, b),
+                                           Sq, q, s, &lse);
                     double *orow = Oh + q * D;
                     for (int d = 0; d < D; ++d) orow[d] = 0.0;
                     Lh[q] = lse;
@@ -196,11 +205,11 @@ int oracle_fwd_rows(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, 
 
 /* Forward over every row. */
 int oracle_fwd(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t, long wl, long wr,
-               const int *seq_lengths, double scale, const double *Q, const double *K,
-               const double *V, double *O, double *LSE)
+               const int *seq_lengths, const double *add, long add_sb, double scale,
+               const double *Q, const double *K, const double *V, double *O, double *LSE)
 {
-    return oracle_fwd_rows(B, Hq, Hkv, Sq, Skv, D, mask, t, wl, wr, seq_lengths, scale, Q, K, V, O,
-                           LSE, 0, Sq);
+    return oracle_fwd_rows(B, Hq, Hkv, Sq, Skv, D, mask, t, wl, wr, seq_lengths, add, add_sb, scale,
+                           Q, K, V, O, LSE, 0, Sq);
 }
 
 /* Backward over query rows [q_begin, q_end): dQ of those rows, and the dK /
@@ -209,11 +218,11 @@ int oracle_fwd(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t
  * itself.  dK/dV are accumulated per q head and then summed over the group in
  * ascending head order.  Returns 0 on success. */
 int oracle_bwd_rows(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t, long wl,
-                    long wr, const int *seq_lengths, double scale, const double *Q,
-                    const double *K, const double *V, const double *dO, double *dQ, double *dK,
-                    double *dV, long q_begin, long q_end)
+                    long wr, const int *seq_lengths, const double *add, long add_sb, double scale,
+                    const double *Q, const double *K, const double *V, const double *dO,
+                    double *dQ, double *dK, double *dV, long q_begin, long q_end)
 {
-    const geom_t g = {mask, t, wl, wr, seq_lengths};
+    const geom_t g = {mask, t, wl, wr, seq_lengths, add, add_sb};
     if (check_shape(B, Hq, Hkv, Sq, Skv, D, &g)) return 1;
     if (q_begin < 0 || q_end > Sq || q_begin > q_end) return 1;
     const int G = Hq / Hkv;
@@ -251,8 +260,8 @@ int oracle_bwd_rows(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, 
                     const double *qrow = Qh + q * D;
                     const double *dorow = dOh + q * D;
                     double *dqrow = dQh + q * D;
-                    long nvis =
-                        row_scores(qrow, Kh, Skv, D, scale, &g, batch_len(&g, b), Sq, q, s, &lse);
+                    long nvis = row_scores(qrow, Kh, Skv, D, scale, &g, b, batch_len(&g, b), Sq, q,
+                                           s, &lse);
                     for (int d = 0; d < D; ++d) dqrow[d] = 0.0;
                     if (nvis == 0) continue;
                     /* P in place of s; O row in fp64 */
@@ -312,11 +321,12 @@ int oracle_bwd_rows(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, 
 
 /* Backward over every row. */
 int oracle_bwd(int B, int Hq, int Hkv, long Sq, long Skv, int D, int mask, int t, long wl, long wr,
-               const int *seq_lengths, double scale, const double *Q, const double *K,
-               const double *V, const double *dO, double *dQ, double *dK, double *dV)
+               const int *seq_lengths, const double *add, long add_sb, double scale,
+               const double *Q, const double *K, const double *V, const double *dO, double *dQ,
+               double *dK, double *dV)
 {
-    return oracle_bwd_rows(B, Hq, Hkv, Sq, Skv, D, mask, t, wl, wr, seq_lengths, scale, Q, K, V, dO,
-                           dQ, dK, dV, 0, Sq);
+    return oracle_bwd_rows(B, Hq, Hkv, Sq, Skv, D, mask, t, wl, wr, seq_lengths, add, add_sb, scale,
+                           Q, K, V, dO, dQ, dK, dV, 0, Sq);
 }
 
 /* Exact count of visible (q, kv) pairs for one (b, h); used to pin the
