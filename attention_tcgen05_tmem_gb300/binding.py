@@ -43,7 +43,9 @@ class Problem(ctypes.Structure):
                 ("Sq", ctypes.c_int), ("Skv", ctypes.c_int), ("D", ctypes.c_int),
                 ("mask", ctypes.c_int), ("ttt_step", ctypes.c_int), ("scale", ctypes.c_float),
                 ("out_dtype", ctypes.c_int), ("window_left", ctypes.c_int),
-                ("window_right", ctypes.c_int), ("seq_lengths", ctypes.c_void_p)]
+                ("window_right", ctypes.c_int), ("seq_lengths", ctypes.c_void_p),
+                ("add_mask", ctypes.c_void_p), ("add_mask_sb", ctypes.c_int64),
+                ("add_mask_sq", ctypes.c_int64)]
 
 
 OUT_DTYPES = {"bf16": 0, "fp32": 1}
@@ -112,22 +114,36 @@ def _lens_ptr(seq_lengths) -> int:
     return seq_lengths.data_ptr()
 
 
+def _add_mask(add_mask):
+    """(address, batch stride, row stride) of a bf16 CUDA additive mask [Sq, Skv]
+    or [B, Sq, Skv] with contiguous keys; a 2-D or batch-1 mask serves every entry."""
+    if add_mask is None:
+        return 0, 0, 0
+    import torch
+    if add_mask.dtype != torch.bfloat16 or not add_mask.is_cuda or add_mask.stride(-1) != 1:
+        raise ValueError("add_mask must be a bf16 CUDA tensor with contiguous keys")
+    sb = 0 if add_mask.dim() == 2 or add_mask.shape[0] == 1 else add_mask.stride(0)
+    return add_mask.data_ptr(), sb, add_mask.stride(-2)
+
+
 def problem(B, Hq, Hkv, Sq, Skv, D, mask="causal", ttt_step=0, scale=0.0, out="bf16",
-            window=None, seq_lengths=None) -> Problem:
+            window=None, seq_lengths=None, add_mask=None) -> Problem:
     """window=(left, right) for the window mask; seq_lengths = device int32 [B]
-    key lengths (the caller keeps the tensor alive while the problem is used)."""
+    key lengths; add_mask = device bf16 additive mask (the caller keeps the
+    tensors alive while the problem is used)."""
     m = MASKS[mask] if isinstance(mask, str) else int(mask)
     wl, wr = (0, 0) if window is None else (int(window[0]), int(window[1]))
+    am, amsb, amsq = _add_mask(add_mask)
     return Problem(B, Hq, Hkv, Sq, Skv, D, m, ttt_step, float(scale), OUT_DTYPES[out], wl, wr,
-                   _lens_ptr(seq_lengths))
+                   _lens_ptr(seq_lengths), am, amsb, amsq)
 
 
 def problem_for(q, k, mask="causal", ttt_step=0, scale=None, out="bf16", window=None,
-                seq_lengths=None) -> Problem:
+                seq_lengths=None, add_mask=None) -> Problem:
     B, Hq, Sq, D = q.shape
     _, Hkv, Skv, _ = k.shape
     return problem(B, Hq, Hkv, Sq, Skv, D, mask, ttt_step, 0.0 if scale is None else scale, out,
-                   window, seq_lengths)
+                   window, seq_lengths, add_mask)
 
 
 def _torch_out_dtype(out):
@@ -210,11 +226,11 @@ def set_wait_budget_ns(ns: int):
 
 # ------------------------------------------------------------ conveniences
 def fwd(q, k, v, mask="causal", ttt_step=0, scale=None, stream=None, out="bf16", window=None,
-        seq_lengths=None):
+        seq_lengths=None, add_mask=None):
     """Allocates O (bf16 or fp32) and LSE with torch, runs the forward;
     returns (o, lse)."""
     import torch
-    p = problem_for(q, k, mask, ttt_step, scale, out, window, seq_lengths)
+    p = problem_for(q, k, mask, ttt_step, scale, out, window, seq_lengths, add_mask)
     o = torch.empty(q.shape, dtype=_torch_out_dtype(out), device=q.device)
     lse = torch.empty(q.shape[0], q.shape[1], q.shape[2], dtype=torch.float32, device=q.device)
     fwd_raw(p, q, k, v, o, lse, stream)
@@ -222,12 +238,12 @@ def fwd(q, k, v, mask="causal", ttt_step=0, scale=None, stream=None, out="bf16",
 
 
 def bwd(q, k, v, o, lse, dout, mask="causal", ttt_step=0, scale=None, stream=None, workspace=None,
-        window=None, seq_lengths=None):
+        window=None, seq_lengths=None, add_mask=None):
     """Allocates dQ, dK, dV (same dtype as o: bf16 or fp32) and the workspace
     unless given; returns (dq, dk, dv)."""
     import torch
     out = "fp32" if o.dtype == torch.float32 else "bf16"
-    p = problem_for(q, k, mask, ttt_step, scale, out, window, seq_lengths)
+    p = problem_for(q, k, mask, ttt_step, scale, out, window, seq_lengths, add_mask)
     dq = torch.empty(q.shape, dtype=o.dtype, device=q.device)
     dk = torch.empty(k.shape, dtype=o.dtype, device=q.device)
     dv = torch.empty(v.shape, dtype=o.dtype, device=q.device)

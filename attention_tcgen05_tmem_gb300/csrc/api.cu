@@ -129,6 +129,16 @@ attn_status check_problem(const attn_problem* p) {
   }
   if (reinterpret_cast<uintptr_t>(p->seq_lengths) % 4 != 0)
     return fail(ATTN_ERR_ALIGNMENT, "seq_lengths is not 4-byte aligned");
+  if (p->add_mask != nullptr) {
+    if (p->mask == ATTN_MASK_TTT)
+      return fail(ATTN_ERR_UNSUPPORTED, "an additive mask does not combine with the TTT mask");
+    if (reinterpret_cast<uintptr_t>(p->add_mask) % 16 != 0)
+      return fail(ATTN_ERR_ALIGNMENT, "add_mask is not 16-byte aligned");
+    if (p->add_mask_sb < 0 || p->add_mask_sq < p->Skv)
+      return fail(ATTN_ERR_INVALID, "add_mask strides: sb >= 0 and sq >= Skv required");
+    if (p->add_mask_sb % 8 != 0 || p->add_mask_sq % 8 != 0)
+      return fail(ATTN_ERR_ALIGNMENT, "add_mask strides must be multiples of 8 elements");
+  }
   if (p->mask == ATTN_MASK_TTT) {
     if (p->ttt_step < 0) return fail(ATTN_ERR_INVALID, "ttt_step %d < 0", p->ttt_step);
     if ((int64_t)p->Skv != (int64_t)(p->ttt_step + 1) * p->Sq)
@@ -179,6 +189,9 @@ Dims make_dims(const attn_problem* p) {
   d.geom = attn::make_geom(p->mask, p->mask == ATTN_MASK_TTT ? p->ttt_step : 0, p->window_left,
                            p->window_right, p->Sq, p->Skv);
   d.seqlens = p->seq_lengths;
+  d.addm = static_cast<const uint16_t*>(p->add_mask);
+  d.addm_sb = p->add_mask_sb;
+  d.addm_sq = p->add_mask_sq;
   d.scale = p->scale > 0.f ? p->scale : 1.0f / std::sqrt((float)p->D);
   d.scale_log2 = d.scale * 1.4426950408889634f;
   d.out_f32 = p->out_dtype == ATTN_OUT_F32 ? 1 : 0;

@@ -384,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quad * 32 + lane;
     const int kv = k0 + r;
     const FullRange full_q = full_rows_for_keys(g, k0);  // query tiles without masking (W)
+    const float inv_scale = 1.f / d.scale;                // additive mask as M / scale (W)
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const uint32_t tS = tmem + lane_base + 64 * wg;         // S^T / P^T columns of this WG
     const uint32_t tdP = tmem + lane_base + 128 + 64 * wg;  // dP^T / dS^T
@@ -405,6 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // -lse2 = -inf.  Masked scores go to -inf (exponential 0) in a pass of its own,
       // so that the exponential loop of full tiles carries no per-element select.
       if constexpr (W) {
+        if (d.addm != nullptr) add_mask_col<64>(raw, d, b, kv, q0 + 64 * wg, inv_scale);
         if (!in_range(full_q, q0)) {
           int clo, chi;
           row_range_for_kv(g, kv, q0 + 64 * wg, &clo, &chi);
@@ -747,6 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float lse2 = qin ? a.lse[rrow] * kLog2e : INFINITY;
     const float delta = qin ? a.delta[rrow] : 0.f;
     const FullRange full_k = full_keys_for_rows(g, q0);  // key tiles without masking (W)
+    const float inv_scale = 1.f / d.scale;                // additive mask as M / scale (W)
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       // P first (needs only S), while the dP MMA may still be running
@@ -762,6 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // masked scores to -inf (their exponential is 0) in a pass of its own, so that
       // the exponential loop of full tiles carries no per-element select
       if constexpr (W) {
+        if (d.addm != nullptr) add_mask_row<64>(rs, d, b, q, k0 + 64 * wg, inv_scale);
         if (!in_range(full_k, k0)) {
           int clo, chi;
           col_range(g, q, k0 + 64 * wg, &clo, &chi);

@@ -340,6 +340,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const float sl2 = d.scale_log2;
 
     const FullRange full_k = full_keys_for_rows(g, qt0);  // key tiles without masking (W)
+    const float inv_scale = 1.f / d.scale;                 // additive mask as M / scale (W)
     float m_run = neg_inf();  // running max of c*log2(e)*s
     float l_run = 0.f;
     bool ok = true;
@@ -355,6 +356,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
       const int k0 = (kt0 + j) * kBN;
       if constexpr (W) {
+        if (d.addm != nullptr) add_mask_row<128>(sr, d, b, q, k0, inv_scale);
         if (!in_range(full_k, k0)) {
           int clo, chi;
           col_range(g, q, k0, &clo, &chi);

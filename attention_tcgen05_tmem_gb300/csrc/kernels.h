@@ -23,12 +23,15 @@ struct Dims {
   float scale_log2;  // c * log2(e)
   int out_f32;       // O, dQ, dK, dV are fp32 (else bf16)
   const int* seqlens;  // device [B]: key length of each batch entry, or null (all keys)
+  // additive mask (bf16 bits): element (b, q, kv) at addm[b * addm_sb + q * addm_sq + kv]
+  const uint16_t* addm;
+  int64_t addm_sb, addm_sq;
 };
 
-// Whether a problem needs the general (two-sided, per-batch length) mask
-// arithmetic: a window mask or per-batch key lengths.
+// Whether a problem needs the general mask arithmetic: a window mask (two-sided
+// bounds), per-batch key lengths or an additive mask.
 inline bool needs_general_mask(const Dims& d) {
-  return d.geom.kind == kMaskWindow || d.seqlens != nullptr;
+  return d.geom.kind == kMaskWindow || d.seqlens != nullptr || d.addm != nullptr;
 }
 
 struct Ctl {

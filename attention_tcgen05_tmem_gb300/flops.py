@@ -15,7 +15,8 @@ Visible pairs per (b, h), in closed form:
 With a window mask or per-batch key lengths the count is the exact sum over
 rows of the visible key interval (plus the t diagonals of rows below the
 length for TTT).  All of them are checked against the oracle's brute-force
-count.
+count.  An additive mask does not change the count: its -inf entries are
+data, and the kernels compute every pair the mask kind admits.
 """
 from __future__ import annotations
 

@@ -39,6 +39,7 @@ class Workload:
     seed: int = 0
     window: tuple | None = None       # (left, right) extents of the window mask
     seq_lengths: tuple | None = None  # per-batch key lengths (padding), None = all keys
+    add_mask: bool = False            # one additive bf16 mask [Sq, Skv] for all entries
 
     @property
     def G(self) -> int:
@@ -56,6 +57,8 @@ class Workload:
             d["window"] = list(self.window)
         if self.seq_lengths is not None:
             d["seq_lengths"] = list(self.seq_lengths)
+        if self.add_mask:
+            d["add_mask"] = "bf16 [Sq, Skv]: 0.5 N(0,1), 10% -inf, key 0 finite"
         return d
 
 
@@ -92,8 +95,13 @@ VARLEN_GQA = Workload("varlen_causal_gqa_B4_Hq32_Hkv4_S8192_D128", 4, 32, 4, 819
 VARLEN_TTT = Workload("varlen_eagle3_ttt_step2_B2_Hq32_Hkv8_S8192_D128", 2, 32, 8, 8192, 3 * 8192,
                       128, "ttt", 2, 6, seq_lengths=(8192, 5000))
 
+# Full self-attention with an additive bias table (HOT-Step section 3: the ops
+# take any additive mask; the DiT trainer passes its masks that way).
+DIT_ADDMASK = Workload("dit_addmask_self_B2_H16_S4096_D64", 2, 16, 16, 4096, 4096, 64, "full", 0,
+                       4, add_mask=True)
+
 ALL = ((TINY,) + SWEEP + (LONG_GQA,) + TTT_STEPS + (DIT_SELF, DIT_CROSS) +
-       (DIT_WINDOW, SWA_GQA, VARLEN_GQA, VARLEN_TTT))
+       (DIT_WINDOW, SWA_GQA, VARLEN_GQA, VARLEN_TTT, DIT_ADDMASK))
 
 # Smaller cases of the same kernels for hardware-counter captures (inputs
 # still larger than the 129 MB L2 once outputs are counted).
@@ -126,6 +134,15 @@ def make_inputs(w: Workload, seed: int | None = None, with_dout: bool = True) ->
         out["dout"] = _draw((w.B, w.Hq, w.Sq, w.D), s * 16 + 3)
     if w.seq_lengths is not None:
         out["seq_lengths"] = torch.tensor(w.seq_lengths, dtype=torch.int32)
+    if w.add_mask:
+        # an additive bias like a relative-position table with holes: 0.5 N(0, 1),
+        # about 10% of the pairs hidden (-inf), key 0 always open (no empty row)
+        g = torch.Generator(device="cpu")
+        g.manual_seed(s * 16 + 4)
+        m = torch.randn(w.Sq, w.Skv, generator=g) * 0.5
+        m[torch.rand(w.Sq, w.Skv, generator=g) < 0.1] = float("-inf")
+        m[:, 0] = 0.0
+        out["add_mask"] = m.to(torch.bfloat16)
     return out
 
 

@@ -52,7 +52,7 @@ def headline_names():
     return ([synth.TINY.name] + [w.name for w in synth.SWEEP] +
             [synth.LONG_GQA.name, TTT_ALL, synth.DIT_SELF.name, synth.DIT_CROSS.name,
              synth.DIT_WINDOW.name, synth.SWA_GQA.name, synth.VARLEN_GQA.name,
-             synth.VARLEN_TTT.name])
+             synth.VARLEN_TTT.name, synth.DIT_ADDMASK.name])
 
 
 def parse_args():
@@ -170,7 +170,7 @@ def cpu_sample(ws, target_s: float, inputs=None):
     do = x["dout"][:, :hq].double().numpy()
     t = w.ttt_step
     lens = w.seq_lengths if w.seq_lengths is not None else (None,) * w.B
-    kw = dict(window=w.window, seq_lengths=w.seq_lengths)
+    kw = dict(window=w.window, seq_lengths=w.seq_lengths, add_mask=x.get("add_mask"))
 
     def pairs(r0):  # visible pairs of query rows [r0, Sq), one q head of every batch entry
         return sum(flops.visible_pairs_rows(w.mask, w.Sq, w.Skv, t, w.window, L, r0, w.Sq)
@@ -219,9 +219,10 @@ class Case:
         # per-batch key lengths stay on the device for the whole run (the problem
         # holds their address)
         self.lens = self.x["seq_lengths"].to(dev) if "seq_lengths" in self.x else None
+        self.add = self.x["add_mask"].to(dev) if "add_mask" in self.x else None
         odt = torch.float32 if out == "fp32" else torch.bfloat16
         self.p = binding.problem(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.mask, w.ttt_step, 0.0, out,
-                                 w.window, self.lens)
+                                 w.window, self.lens, self.add)
         binding.check_supported(self.p)
         self.o = torch.empty(self.q.shape, dtype=odt, device=dev)
         self.lse = torch.empty(w.B, w.Hq, w.Sq, dtype=torch.float32, device=dev)
@@ -303,8 +304,8 @@ def run_ours(args, ws, local_rank, dist):
         # outputs (O, LSE, dQ, dK, dV) copied out inside the timed region
         hosts = []
         for c in cases:
-            pin = {n: c.x[n].pin_memory() for n in ("q", "k", "v", "dout", "seq_lengths")
-                   if n in c.x}
+            pin = {n: c.x[n].pin_memory()
+                   for n in ("q", "k", "v", "dout", "seq_lengths", "add_mask") if n in c.x}
             outs = {n: torch.empty(getattr(c, n).shape, dtype=getattr(c, n).dtype).pin_memory()
                     for n in ("o", "lse", "dq", "dk", "dv")}
             hosts.append((pin, outs))
@@ -319,6 +320,8 @@ def run_ours(args, ws, local_rank, dist):
                 c.do.copy_(pin["dout"], non_blocking=True)
                 if c.lens is not None:
                     c.lens.copy_(pin["seq_lengths"], non_blocking=True)
+                if c.add is not None:
+                    c.add.copy_(pin["add_mask"], non_blocking=True)
                 binding.fwd_raw(c.p, c.q, c.k, c.v, c.o, c.lse, stream.cuda_stream)
                 binding.bwd_raw(c.p, c.q, c.k, c.v, c.o, c.do, c.lse, c.dq, c.dk, c.dv, c.ws,
                                 stream.cuda_stream)

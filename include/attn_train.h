@@ -35,6 +35,10 @@
  * seq_lengths set, keys kv >= seq_lengths[b] of batch entry b are invisible
  * (for TTT: segment-0 keys kv >= seq_lengths[b], and the suffix diagonals of
  * rows q >= seq_lengths[b]); their dK and dV are 0.
+ * Additive mask (HOT-Step section 3: the ops take any additive mask [S_kv, S],
+ * or [S_kv, S, 1, B] broadcast): with add_mask set, the scores of the pairs
+ * the mask kind admits become scale * q.k + M[b][q][kv] (M = -inf hides the
+ * pair); one M for all heads.  Not with ATTN_MASK_TTT.
  *
  * Layout and types
  * ----------------
@@ -110,7 +114,10 @@ typedef enum { ATTN_OUT_BF16 = 0, ATTN_OUT_F32 = 1 } attn_out_dtype;
  * the extents of ATTN_MASK_WINDOW (>= 0; must be 0 for the other masks).
  * seq_lengths: NULL, or a device array of B int32 key lengths (4-byte
  * aligned, read by the kernels; values are clamped to [0, Skv], to [0, Sq]
- * for TTT). */
+ * for TTT).  add_mask: NULL, or a device bf16 additive mask with element
+ * (b, q, kv) at add_mask[b * add_mask_sb + q * add_mask_sq + kv]
+ * (add_mask_sb = 0: one mask for every batch entry); 16-byte aligned, both
+ * strides multiples of 8 elements, add_mask_sq >= Skv. */
 typedef struct {
   int B, Hq, Hkv, Sq, Skv, D;
   int mask;
@@ -119,6 +126,8 @@ typedef struct {
   int out_dtype;
   int window_left, window_right;
   const int32_t* seq_lengths;
+  const void* add_mask;
+  int64_t add_mask_sb, add_mask_sq;
 } attn_problem;
 
 /* Whether the problem is supported.  Pure host check, no side effects.

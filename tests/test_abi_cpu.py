@@ -69,6 +69,21 @@ def test_supports_rejects(lib, kw, status):
     assert lib.attn_train_last_error()
 
 
+def test_additive_mask_rules(lib):
+    p = _p(Skv=256)
+    p.add_mask, p.add_mask_sq = 0x10000, 256
+    assert _status(lib, p) == 0
+    p.add_mask = 0x10008
+    assert _status(lib, p) == 3          # not 16-byte aligned
+    p.add_mask, p.add_mask_sq = 0x10000, 260
+    assert _status(lib, p) == 3          # row stride not a multiple of 8
+    p.add_mask_sq = 248
+    assert _status(lib, p) == 1          # row stride below Skv
+    q = _p(mask="ttt", ttt_step=1, Skv=512)
+    q.add_mask, q.add_mask_sq = 0x10000, 512
+    assert _status(lib, q) == 2          # not with TTT
+
+
 def test_misaligned_seq_lengths_are_rejected(lib):
     p = _p()
     p.seq_lengths = 0x1002

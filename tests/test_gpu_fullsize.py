@@ -17,14 +17,16 @@ def run_sampled(w, b_idx=(0,), groups=(0,), out="fp32"):
     x = synth.make_inputs(w)
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
     lens = x["seq_lengths"].to(dev) if "seq_lengths" in x else None
-    kw = dict(window=w.window, seq_lengths=lens)
+    am = x["add_mask"].to(dev) if "add_mask" in x else None
+    kw = dict(window=w.window, seq_lengths=lens, add_mask=am)
     o, lse = binding.fwd(q, k, v, w.mask, w.ttt_step, out=out, **kw)
     dq, dk, dv = binding.bwd(q, k, v, o, lse, do, w.mask, w.ttt_step, **kw)
     binding.device_status()
     G = w.G
     for b in b_idx:
         rkw = dict(window=w.window,
-                   seq_lengths=None if w.seq_lengths is None else [w.seq_lengths[b]])
+                   seq_lengths=None if w.seq_lengths is None else [w.seq_lengths[b]],
+                   add_mask=x.get("add_mask"))
         for g in groups:
             hs = slice(g * G, (g + 1) * G)
             sub = {n: x[n][b:b + 1, hs] for n in ("q", "dout")}
@@ -70,6 +72,12 @@ def test_dit_self_full_size():
 def test_window_full_size():
     run_sampled(synth.DIT_WINDOW, b_idx=(1,), groups=(5,))
     run_sampled(synth.SWA_GQA, groups=(3,))
+
+
+@pytest.mark.gpu
+@pytest.mark.timeout(1800)
+def test_additive_mask_full_size():
+    run_sampled(synth.DIT_ADDMASK, b_idx=(1,), groups=(7,))
 
 
 @pytest.mark.gpu

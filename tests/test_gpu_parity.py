@@ -17,8 +17,14 @@ def run_both(w: synth.Workload, check_bwd=True, out="fp32"):
     x = synth.make_inputs(w)
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
     lens = x["seq_lengths"].to(dev) if "seq_lengths" in x else None
-    kw = dict(window=w.window, seq_lengths=lens)
-    rkw = dict(window=w.window, seq_lengths=w.seq_lengths)
+    am = None
+    if "add_mask" in x:
+        # device copy with a row stride padded to a multiple of 8 keys
+        pad = -w.Skv % 8
+        am = torch.zeros(w.Sq, w.Skv + pad, dtype=torch.bfloat16, device=dev)[:, :w.Skv]
+        am.copy_(x["add_mask"].to(dev))
+    kw = dict(window=w.window, seq_lengths=lens, add_mask=am)
+    rkw = dict(window=w.window, seq_lengths=w.seq_lengths, add_mask=x.get("add_mask"))
     o, lse = binding.fwd(q, k, v, w.mask, w.ttt_step, out=out, **kw)
     binding.device_status()
     ro, rl = oracle.fwd(x["q"], x["k"], x["v"], w.mask, w.ttt_step, **rkw)
@@ -35,8 +41,8 @@ def run_both(w: synth.Workload, check_bwd=True, out="fp32"):
     compare("dV", dv, rdv)
 
 
-def W(name, B, Hq, Hkv, Sq, Skv, D, mask, t=0, seed=11, window=None, lens=None):
-    return synth.Workload(name, B, Hq, Hkv, Sq, Skv, D, mask, t, seed, window, lens)
+def W(name, B, Hq, Hkv, Sq, Skv, D, mask, t=0, seed=11, window=None, lens=None, add=False):
+    return synth.Workload(name, B, Hq, Hkv, Sq, Skv, D, mask, t, seed, window, lens, add)
 
 
 CASES = [
@@ -71,6 +77,13 @@ CASES = [
     W("varlen_window_d64", 2, 2, 1, 640, 640, 64, "window", window=(100, 20), lens=(640, 250)),
     W("varlen_ttt_t2_d128", 2, 4, 2, 384, 1152, 128, "ttt", 2, lens=(384, 200)),
     W("varlen_empty_entry_d64", 2, 2, 2, 256, 256, 64, "causal", lens=(0, 256)),
+    # additive masks (bf16 bias with -inf holes) on the full, causal and window kinds
+    W("addmask_full_d64", 2, 2, 2, 300, 300, 64, "full", add=True),
+    W("addmask_causal_gqa_d128", 1, 4, 2, 333, 333, 128, "causal", add=True),
+    W("addmask_cross_ragged_d64", 2, 2, 1, 250, 190, 64, "full", add=True),
+    W("addmask_window_d32", 1, 2, 2, 400, 400, 32, "window", window=(64, 64), add=True),
+    W("addmask_varlen_d128", 2, 2, 2, 256, 256, 128, "causal", lens=(256, 100), add=True),
+    W("addmask_d16", 1, 2, 2, 384, 384, 16, "full", add=True),
 ]
 
 
