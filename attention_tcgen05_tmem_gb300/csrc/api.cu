@@ -217,7 +217,18 @@ size_t ws_diag_bytes(const attn_problem* p) {
   const int t = p->mask == ATTN_MASK_TTT ? p->ttt_step : 0;
   return ws_round((size_t)p->B * p->Hq * p->Sq * (size_t)t * sizeof(float));
 }
-size_t ws_bytes_for(const attn_problem* p) { return ws_delta_bytes(p) + 2 * ws_diag_bytes(p); }
+// The additive mask transposed for the dK/dV pass: [Bm][Skv][SqT] bf16 with
+// SqT = Sq rounded up to 8 (16-byte rows), Bm = 1 for a mask shared by every
+// batch entry, else B.
+int64_t mask_t_sq(const attn_problem* p) { return ((int64_t)p->Sq + 7) & ~(int64_t)7; }
+size_t ws_mask_t_bytes(const attn_problem* p) {
+  if (p->add_mask == nullptr) return 0;
+  const size_t bm = p->add_mask_sb == 0 ? 1 : (size_t)p->B;
+  return ws_round(bm * (size_t)p->Skv * (size_t)mask_t_sq(p) * 2);
+}
+size_t ws_bytes_for(const attn_problem* p) {
+  return ws_delta_bytes(p) + 2 * ws_diag_bytes(p) + ws_mask_t_bytes(p);
+}
 
 // ------------------------------------------- built-in scratch (no-alloc bwd)
 // Scratch for attn_train_bwd_noalloc: the backward's only scratch is the
@@ -352,6 +363,14 @@ attn_status attn_train_bwd_passes(const attn_problem* p, unsigned passes, attn_t
     char* w = static_cast<char*>(workspace) + ws_delta_bytes(p);
     a.ttt_p = reinterpret_cast<float*>(w);
     a.ttt_ds = reinterpret_cast<float*>(w + ws_diag_bytes(p));
+  }
+  a.addm_t = nullptr;
+  a.addm_t_sb = a.addm_t_sq = 0;
+  if (p->add_mask != nullptr) {
+    char* w = static_cast<char*>(workspace) + ws_delta_bytes(p) + 2 * ws_diag_bytes(p);
+    a.addm_t = reinterpret_cast<uint16_t*>(w);
+    a.addm_t_sq = mask_t_sq(p);
+    a.addm_t_sb = p->add_mask_sb == 0 ? 0 : (int64_t)p->Skv * a.addm_t_sq;
   }
   if ((st = device_error_word(&a.ctl.err)) != ATTN_OK) return st;
   a.ctl.budget_ns = g_budget_ns.load();

@@ -156,6 +156,27 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdArgs a) {
   }
 }
 
+// Additive mask transpose for the dK/dV pass (which reads the mask by key
+// row): M [Bm][Sq][Skv] -> workspace [Bm][Skv][SqT], 64 x 64 tiles through
+// shared memory, both sides coalesced; columns q >= Sq of the copy are zero.
+__global__ void __launch_bounds__(256) mask_transpose_kernel(const BwdArgs a) {
+  __shared__ uint16_t tile[64][65];
+  const Dims& d = a.d;
+  const int k0 = blockIdx.x * 64, q0 = blockIdx.y * 64, b = blockIdx.z;
+  const uint16_t* src = d.addm + b * d.addm_sb;
+  uint16_t* dst = a.addm_t + b * a.addm_t_sb;
+  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // 64 x 4 threads
+  for (int r = ty; r < 64; r += 4) {
+    const int q = q0 + r, kv = k0 + tx;
+    tile[r][tx] = (q < d.Sq && kv < d.Skv) ? src[(int64_t)q * d.addm_sq + kv] : (uint16_t)0;
+  }
+  __syncthreads();
+  for (int r = ty; r < 64; r += 4) {
+    const int kv = k0 + r, q = q0 + tx;
+    if (kv < d.Skv && q < a.addm_t_sq) dst[(int64_t)kv * a.addm_t_sq + q] = tile[tx][r];
+  }
+}
+
 // ===================================================================== dK/dV
 template <int D>
 struct DkdvLayout {
@@ -406,7 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // -lse2 = -inf.  Masked scores go to -inf (exponential 0) in a pass of its own,
       // so that the exponential loop of full tiles carries no per-element select.
       if constexpr (W) {
-        if (d.addm != nullptr) add_mask_col<64>(raw, d, b, kv, q0 + 64 * wg, inv_scale);
+        if (a.addm_t != nullptr && kv < d.Skv)
+          add_bias_row<64>(raw, a.addm_t + b * a.addm_t_sb + (int64_t)kv * a.addm_t_sq,
+                           q0 + 64 * wg, d.Sq, inv_scale);
         if (!in_range(full_q, q0)) {
           int clo, chi;
           row_range_for_kv(g, kv, q0 + 64 * wg, &clo, &chi);
@@ -765,7 +788,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // masked scores to -inf (their exponential is 0) in a pass of its own, so that
       // the exponential loop of full tiles carries no per-element select
       if constexpr (W) {
-        if (d.addm != nullptr) add_mask_row<64>(rs, d, b, q, k0 + 64 * wg, inv_scale);
+        if (d.addm != nullptr && q < d.Sq)
+          add_bias_row<64>(rs, d.addm + b * d.addm_sb + (int64_t)q * d.addm_sq, k0 + 64 * wg,
+                           d.Skv, inv_scale);
         if (!in_range(full_k, k0)) {
           int clo, chi;
           col_range(g, q, k0 + 64 * wg, &clo, &chi);
@@ -951,6 +976,12 @@ cudaError_t launch_bwd_dw(const BwdArgs& a, const Maps& m, unsigned passes, cuda
     const int64_t rows = (int64_t)a.d.B * a.d.Hq * a.d.Sq;
     bwd_prep_kernel<D><<<(unsigned)((rows + RPB - 1) / RPB), 256, 0, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (a.addm_t != nullptr) {
+      const dim3 grid((unsigned)cdiv(a.d.Skv, 64), (unsigned)cdiv((int)a.addm_t_sq, 64),
+                      a.addm_t_sb == 0 ? 1u : (unsigned)a.d.B);
+      mask_transpose_kernel<<<grid, 256, 0, s>>>(a);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
   }
   if (passes & 2u) {
     using L = DkdvLayout<D>;

@@ -356,7 +356,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
       const int k0 = (kt0 + j) * kBN;
       if constexpr (W) {
-        if (d.addm != nullptr) add_mask_row<128>(sr, d, b, q, k0, inv_scale);
+        if (d.addm != nullptr && q < d.Sq)
+          add_bias_row<128>(sr, d.addm + b * d.addm_sb + (int64_t)q * d.addm_sq, k0, d.Skv,
+                            inv_scale);
         if (!in_range(full_k, k0)) {
           int clo, chi;
           col_range(g, q, k0, &clo, &chi);

@@ -55,6 +55,10 @@ struct BwdArgs {
   // gradient ds_i of its suffix diagonal i = 1..t, workspace [B, Hq, Sq, t]
   float* ttt_p;
   float* ttt_ds;
+  // additive mask transposed by the prep pass (workspace): element (b, kv, q) at
+  // addm_t[b * addm_t_sb + kv * addm_t_sq + q]; null without an additive mask
+  uint16_t* addm_t;
+  int64_t addm_t_sb, addm_t_sq;
   Ctl ctl;
 };
 

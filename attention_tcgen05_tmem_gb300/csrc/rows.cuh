@@ -20,18 +20,18 @@ __device__ __forceinline__ const __nv_bfloat16* row_ptr(const View& v, int b, in
 // s + M / scale (M = -inf gives -inf).
 __device__ __forceinline__ float bf16_bits(uint32_t h) { return __uint_as_float(h << 16); }
 
-// Scores of query row q against keys k0 .. k0+N-1 (N a multiple of 8, k0 of 8):
-// s[c] += M[b][q][k0 + c] / scale.  Rows past Sq and keys past Skv read nothing
-// (those scores are masked or never stored).
+// s[c] += M[col0 + c] / scale for one row of a bf16 table (the additive mask by
+// query row for the forward and dQ, its transpose by key row for dK/dV).  row:
+// the row's first element, 16-byte aligned; col0 a multiple of 8; columns at
+// or past ncols read nothing (those scores are masked or never stored).
 template <int N>
-__device__ __forceinline__ void add_mask_row(uint32_t* s, const Dims& d, int b, int q, int k0,
+__device__ __forceinline__ void add_bias_row(uint32_t* s, const uint16_t* row, int col0, int ncols,
                                              float inv_scale) {
-  if (q >= d.Sq) return;
-  const uint16_t* row = d.addm + b * d.addm_sb + (int64_t)q * d.addm_sq + k0;
-  if (k0 + N <= d.Skv) {
+  const uint16_t* r = row + col0;
+  if (col0 + N <= ncols) {
 #pragma unroll
     for (int c0 = 0; c0 < N; c0 += 8) {
-      const uint4 m = *reinterpret_cast<const uint4*>(row + c0);  // 16-byte aligned
+      const uint4 m = *reinterpret_cast<const uint4*>(r + c0);
       const uint32_t w[4] = {m.x, m.y, m.z, m.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -44,23 +44,9 @@ __device__ __forceinline__ void add_mask_row(uint32_t* s, const Dims& d, int b, 
   } else {
 #pragma unroll
     for (int c = 0; c < N; ++c)
-      if (k0 + c < d.Skv)
-        s[c] = __float_as_uint(fmaf(bf16_bits(row[c]), inv_scale, __uint_as_float(s[c])));
+      if (col0 + c < ncols)
+        s[c] = __float_as_uint(fmaf(bf16_bits(r[c]), inv_scale, __uint_as_float(s[c])));
   }
-}
-
-// Scores of key row kv against queries q0 .. q0+N-1: s[c] += M[b][q0 + c][kv] / scale
-// (one element per query row; consecutive threads read consecutive keys).
-template <int N>
-__device__ __forceinline__ void add_mask_col(uint32_t* s, const Dims& d, int b, int kv, int q0,
-                                             float inv_scale) {
-  if (kv >= d.Skv) return;
-  const uint16_t* col = d.addm + b * d.addm_sb + (int64_t)q0 * d.addm_sq + kv;
-#pragma unroll
-  for (int c = 0; c < N; ++c)
-    if (q0 + c < d.Sq)
-      s[c] = __float_as_uint(
-          fmaf(bf16_bits(col[(int64_t)c * d.addm_sq]), inv_scale, __uint_as_float(s[c])));
 }
 
 // Dot product of two bf16 rows of length D (fp32 accumulate, fixed order).

@@ -140,7 +140,10 @@ attn_status attn_train_supports(const attn_problem* p);
 /* Bytes of device workspace attn_train_bwd needs: the fp32 Delta row
  * statistic, B * Hq * Sq * 4 bytes rounded up to 256; for a TTT step t > 0
  * also the per-row weight and score gradient of each suffix diagonal,
- * 2 * B * Hq * Sq * t * 4 bytes (each part rounded up to 256).  Linear in S. */
+ * 2 * B * Hq * Sq * t * 4 bytes (each part rounded up to 256).  Linear in S.
+ * With an additive mask also its bf16 transpose for the dK/dV pass,
+ * Bm * Skv * round8(Sq) * 2 bytes (Bm = 1 for a shared mask, else B): the
+ * size of the mask itself. */
 attn_status attn_train_workspace_size(const attn_problem* p, size_t* bytes);
 
 /* Forward.  Inputs q [B,Hq,Sq,D], k and v [B,Hkv,Skv,D]; outputs o
