@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(256) ttt_scores_kernel(const FwdArgs a) {
 template <int D>
 struct FwdLayout {
   using TG = TileGeom<D>;
-  static constexpr int NSLOT = (D == 128) ? 4 : (D == 64 ? 6 : 8);
+  static constexpr int NSLOT = (D == 128) ? 5 : (D == 64 ? 6 : 8);
   static constexpr int Q_OFF = 0;
   static constexpr int KV_OFF = 2 * TG::TILE_BYTES;
   static constexpr int BAR_OFF = KV_OFF + NSLOT * TG::TILE_BYTES;

@@ -103,6 +103,30 @@ def test_parity_sweep(w):
     run_both(w)
 
 
+DET_CASES = [W("det_window", 1, 4, 2, 600, 600, 64, "window", seed=5, window=(150, 40)),
+             W("det_varlen_ttt", 2, 4, 2, 384, 1152, 128, "ttt", 2, seed=5, lens=(384, 250)),
+             W("det_addmask", 1, 4, 2, 384, 384, 128, "causal", seed=5, add=True)]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("w", DET_CASES, ids=[c.name for c in DET_CASES])
+def test_general_mask_backward_is_bitwise_deterministic(w):
+    dev = device()
+    x = synth.make_inputs(w)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
+    kw = dict(window=w.window,
+              seq_lengths=x["seq_lengths"].to(dev) if "seq_lengths" in x else None,
+              add_mask=x["add_mask"].to(dev) if "add_mask" in x else None)
+    o, lse = binding.fwd(q, k, v, w.mask, w.ttt_step, out="fp32", **kw)
+    o2, lse2 = binding.fwd(q, k, v, w.mask, w.ttt_step, out="fp32", **kw)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    r1 = binding.bwd(q, k, v, o, lse, do, w.mask, w.ttt_step, **kw)
+    r2 = binding.bwd(q, k, v, o, lse, do, w.mask, w.ttt_step, **kw)
+    binding.device_status()
+    for a, b in zip(r1, r2):
+        assert torch.equal(a, b)
+
+
 @pytest.mark.gpu
 def test_backward_is_bitwise_deterministic():
     dev = device()
