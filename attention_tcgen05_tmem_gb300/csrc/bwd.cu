@@ -188,8 +188,8 @@ struct DkdvLayout {
   static constexpr int STAGE_BYTES = 2 * TG::TILE_BYTES;
   static constexpr int STAT_OFF = ST_OFF + NST * STAGE_BYTES;  // per stage: -lse2[128], delta[128]
   static constexpr int BAR_OFF = STAT_OFF + NST * 2 * 128 * 4;
-  // kv_full, qdo_full[NST], qdo_empty[NST], s_full, dp_full, p_ready, ds_ready, done, drain
-  static constexpr int NBAR = 1 + 2 * NST + 6;
+  // kv_full, qdo_full[NST], qdo_empty[NST], s_full[2], dp_full, p_ready[2], ds_ready, done, drain
+  static constexpr int NBAR = 1 + 2 * NST + 8;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int BYTES = MISC_OFF + 16;
   // at least 116 KB so that only one CTA fits per SM: each holds all 512 TMEM columns
@@ -207,6 +207,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   using TG = TileGeom<D>;
   using L = DkdvLayout<D>;
   constexpr int NST = L::NST;
+  // tensor memory: S^T (two buffers at D <= 64, where the columns allow), dP^T,
+  // then the dV and dK accumulators
+  constexpr bool DB = D <= 64;
+  constexpr uint32_t T_DP = DB ? 256 : 128;
+  constexpr uint32_t T_DV = DB ? 384 : 256;
   extern __shared__ uint8_t smem_raw[];
   if (*reinterpret_cast<volatile uint32_t*>(a.ctl.err) != 0) return;
 
@@ -215,10 +220,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* kv_full = bars;
   uint64_t* qdo_full = bars + 1;
   uint64_t* qdo_empty = qdo_full + NST;
-  uint64_t* s_full = qdo_empty + NST;
-  uint64_t* dp_full = s_full + 1;
-  uint64_t* p_ready = dp_full + 1;
-  uint64_t* ds_ready = p_ready + 1;
+  uint64_t* s_full = qdo_empty + NST;  // [2]
+  uint64_t* dp_full = s_full + 2;
+  // p_ready alternates between two barriers: with S^T double-buffered a warp
+  // can reach iteration it + 1 before a slower warp has arrived for it, and one
+  // barrier would count that early arrival toward the wrong phase (S^T of
+  // iteration it + 2 is issued only after p_ready(it) completes, so two suffice)
+  uint64_t* p_ready = dp_full + 1;  // [2]
+  uint64_t* ds_ready = p_ready + 2;
   uint64_t* done = ds_ready + 1;
   uint64_t* drain = done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
@@ -256,9 +265,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&qdo_full[s], 2);  // the copies' expect_tx and the LSE / Delta rows
       mbar_init(&qdo_empty[s], 1);
     }
-    mbar_init(s_full, 1);
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
     mbar_init(dp_full, 1);
-    mbar_init(p_ready, 256);
+    mbar_init(&p_ready[0], 256);
+    mbar_init(&p_ready[1], 256);
     mbar_init(ds_ready, 256);
     mbar_init(done, 1);
     mbar_init(drain, 1);
@@ -336,17 +347,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dSTm = TG::mnmajor_base(smem_u32(smem + L::ST_OFF));  // stage 0, MN-major
       auto stage = [&](int it) { return TG::bytes((it % NST) * L::STAGE_BYTES); };
       constexpr uint64_t kDo = TG::bytes(TG::TILE_BYTES);  // dO follows Q in a stage
-      auto issue_st = [&](int it) {  // S^T = K Q^T
+      auto issue_st = [&](int it) {  // S^T = K Q^T into buffer it % 2 (one buffer at D = 128)
         const uint64_t qd = dSTk + stage(it);
+        const uint32_t col = DB ? 128u * (uint32_t)(it & 1) : 0u;
 #pragma unroll
         for (int kk = 0; kk < TG::KSTEPS; ++kk)
-          umma_ss(tmem + 0, dK + TG::kmajor_step(kk), qd + TG::kmajor_step(kk), idesc_s, kk > 0);
+          umma_ss(tmem + col, dK + TG::kmajor_step(kk), qd + TG::kmajor_step(kk), idesc_s, kk > 0);
+        umma_commit(&s_full[DB ? (it & 1) : 0]);
       };
       auto issue_dpt = [&](int it) {  // dP^T = V dO^T
         const uint64_t od = dSTk + stage(it) + kDo;
 #pragma unroll
         for (int kk = 0; kk < TG::KSTEPS; ++kk)
-          umma_ss(tmem + 128, dV + TG::kmajor_step(kk), od + TG::kmajor_step(kk), idesc_s, kk > 0);
+          umma_ss(tmem + T_DP, dV + TG::kmajor_step(kk), od + TG::kmajor_step(kk), idesc_s,
+                  kk > 0);
+        umma_commit(dp_full);
       };
       // A operand in TMEM: q columns 16kk.. of warpgroup kk/4 live at 64*(kk/4) + 8*(kk%4)
       auto issue_grad = [&](uint32_t acc_col, uint32_t a_col, uint64_t bd, bool acc) {
@@ -355,38 +370,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_ts(tmem + acc_col, tmem + a_col + 64 * (kk / 4) + 8 * (kk % 4),
                   bd + TG::mnmajor_step(kk), idesc_g, (acc || kk > 0) ? 1u : 0u);
       };
-      bool ok = mbar_wait(kv_full, 0, ctl) && mbar_wait(&qdo_full[0], 0, ctl);
+      auto wait_stage = [&](int it) {
+        return mbar_wait(&qdo_full[it % NST], (uint32_t)(it / NST) & 1u, ctl);
+      };
+      // Issue order.  D = 128: S^T(0), dP^T(0), then per query tile: dV(it),
+      // S^T(it+1) (its columns held P^T(it)), dK(it), dP^T(it+1) (its columns held
+      // dS^T(it)).  D <= 64, two S^T buffers: S^T(0), dP^T(0), S^T(1), then per tile:
+      // dV(it), S^T(it+2) into the buffer dV(it) just read, dK(it), dP^T(it+1) -- the
+      // elementwise warps find S^T(it+1) ready when they finish tile it.
+      bool ok = mbar_wait(kv_full, 0, ctl) && wait_stage(0);
       if (ok) {
         tc_fence_after();
         issue_st(0);
-        umma_commit(s_full);
         issue_dpt(0);
-        umma_commit(dp_full);
+        if (DB && N > 1 && (ok = wait_stage(1))) {
+          tc_fence_after();
+          issue_st(1);
+        }
       }
       for (int it = 0; ok && it < N; ++it) {
         ATTN_TR(1, 0, it);
-        if (!(ok = mbar_wait(p_ready, (uint32_t)it & 1u, ctl))) break;
+        if (!(ok = mbar_wait(&p_ready[it & 1], (uint32_t)(it >> 1) & 1u, ctl))) break;
         ATTN_TR(1, 1, it);
         tc_fence_after();
-        issue_grad(256, 0, dSTm + stage(it) + kDo, it > 0);  // dV += P^T dO
-        const bool more = it + 1 < N;
-        if (more) {
-          if (!(ok = mbar_wait(&qdo_full[(it + 1) % NST], (uint32_t)((it + 1) / NST) & 1u, ctl)))
-            break;
+        issue_grad(T_DV, DB ? 128u * (uint32_t)(it & 1) : 0u, dSTm + stage(it) + kDo,
+                   it > 0);  // dV += P^T dO
+        const int next_s = DB ? it + 2 : it + 1;
+        if (next_s < N) {
+          if (!(ok = wait_stage(next_s))) break;
           ATTN_TR(1, 2, it);
           tc_fence_after();
-          issue_st(it + 1);
-          umma_commit(s_full);
+          issue_st(next_s);
         }
         if (!(ok = mbar_wait(ds_ready, (uint32_t)it & 1u, ctl))) break;
         ATTN_TR(1, 3, it);
         tc_fence_after();
-        issue_grad(256 + D, 128, dSTm + stage(it), it > 0);  // dK += dS^T Q
+        issue_grad(T_DV + D, T_DP, dSTm + stage(it), it > 0);  // dK += dS^T Q
         umma_commit(&qdo_empty[it % NST]);
-        if (more) {
-          issue_dpt(it + 1);
-          umma_commit(dp_full);
-        }
+        if (it + 1 < N) issue_dpt(it + 1);
         ATTN_TR(1, 4, it);
       }
       if (ok) {
@@ -407,8 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const FullRange full_q = full_rows_for_keys(g, k0);  // query tiles without masking (W)
     const float inv_scale = 1.f / d.scale;                // additive mask as M / scale (W)
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    const uint32_t tS = tmem + lane_base + 64 * wg;         // S^T / P^T columns of this WG
-    const uint32_t tdP = tmem + lane_base + 128 + 64 * wg;  // dP^T / dS^T
+    const uint32_t tdP = tmem + lane_base + T_DP + 64 * wg;  // dP^T / dS^T columns of this WG
     const float sl2 = d.scale_log2;
     bool ok = true;
     for (int it = 0; it < N; ++it) {
@@ -418,7 +438,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* dl = stats + s * 256 + 128 + 64 * wg;
       const bool tr = lane == 0 && quad == 0;
       if (tr) ATTN_TR(2 + wg, 0, it);
-      if (!(ok = mbar_wait_warp(s_full, (uint32_t)it & 1u, ctl))) break;
+      if (!(ok = mbar_wait_warp(&s_full[DB ? (it & 1) : 0],
+                                (uint32_t)(DB ? (it >> 1) : it) & 1u, ctl)))
+        break;
+      // S^T / P^T columns of this WG (buffer it % 2 at D <= 64)
+      const uint32_t tS = tmem + lane_base + (DB ? 128u * (uint32_t)(it & 1) : 0u) + 64 * wg;
       if (tr) ATTN_TR(2 + wg, 1, it);
       tc_fence_after();
       uint32_t raw[64];
@@ -460,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st32(tS, pk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(p_ready);
+      mbar_arrive(&p_ready[it & 1]);
       if (tr) ATTN_TR(2 + wg, 2, it);
 
       if (!(ok = mbar_wait_warp(dp_full, (uint32_t)it & 1u, ctl))) break;
@@ -502,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float vals[16];
         uint32_t raw[16];
         if (N > 0) {
-          tmem_ld16(tmem + lane_base + 256 + c0, raw);
+          tmem_ld16(tmem + lane_base + T_DV + c0, raw);
 #pragma unroll
           for (int e = 0; e < 16; ++e) vals[e] = __uint_as_float(raw[e]);
         } else {
@@ -511,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (store) store16(a.dv, b, hk, kv, c0, vals, 1.f, f32);
         if (N > 0) {
-          tmem_ld16(tmem + lane_base + 256 + D + c0, raw);
+          tmem_ld16(tmem + lane_base + T_DV + D + c0, raw);
 #pragma unroll
           for (int e = 0; e < 16; ++e) vals[e] = __uint_as_float(raw[e]);
         }
@@ -543,8 +567,8 @@ struct DqLayout {
   static constexpr int V_OFF = K_OFF + NK * TG::TILE_BYTES;
   static constexpr int BAR_OFF = V_OFF + NV * TG::TILE_BYTES;
   // qdo_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2], dp_full,
-  // dp_free, ds_ready, done, drain
-  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 7;
+  // dp_free, ds_ready[2], done, drain
+  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 8;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int BYTES = MISC_OFF + 16;
   // at least 116 KB so that only one CTA fits per SM: each holds all 512 TMEM columns
@@ -578,8 +602,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_full = v_empty + NV;  // [2]
   uint64_t* dp_full = s_full + 2;
   uint64_t* dp_free = dp_full + 1;
-  uint64_t* ds_ready = dp_free + 1;
-  uint64_t* done = ds_ready + 1;
+  // ds_ready alternates between two barriers: dP(j + 1) is issued once every
+  // warp has read dP(j), so a warp can finish tile j + 1 before a slower one has
+  // arrived for tile j; dP(j + 2) waits for dp_free(j + 1), which every warp
+  // signals after its ds_ready(j), so two barriers keep the phases apart
+  uint64_t* ds_ready = dp_free + 1;  // [2]
+  uint64_t* done = ds_ready + 2;
   uint64_t* drain = done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
@@ -620,7 +648,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int x = 0; x < 2; ++x) mbar_init(&s_full[x], 1);
     mbar_init(dp_full, 1);
     mbar_init(dp_free, 8);  // one arrival per elementwise warp
-    mbar_init(ds_ready, 8);
+    mbar_init(&ds_ready[0], 8);
+    mbar_init(&ds_ready[1], 8);
     mbar_init(done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -736,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_dp(m);
         }
         ATTN_TR(1, 2, j);
-        if (!(ok = mbar_wait(ds_ready, (uint32_t)j & 1u, ctl))) break;
+        if (!(ok = mbar_wait(&ds_ready[j & 1], (uint32_t)(j >> 1) & 1u, ctl))) break;
         ATTN_TR(1, 3, j);
         tc_fence_after();
         issue_dq(j);
@@ -837,7 +866,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(ds_ready);
+      if (lane == 0) mbar_arrive(&ds_ready[j & 1]);
       if (tr) ATTN_TR(2 + wg, 6, j);
     }
     // ------------------------------------------------------------ epilogue
