@@ -24,7 +24,10 @@ STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID", 2: "ATTN_ERR_UNSUPPORTED", 3: "AT
 EXPORTS = ("attn_train_supports", "attn_train_workspace_size", "attn_train_fwd", "attn_train_bwd",
            "attn_train_bwd_passes", "attn_train_bwd_noalloc", "attn_train_last_error", "attn_train_device_status", "attn_train_set_wait_budget_ns",
            "attn_train_mask_pattern", "attn_train_probe_mma", "attn_train_selftest_wait_timeout",
-           "attn_train_logsoftmax_loss_fwd", "attn_train_logsoftmax_loss_bwd")
+           "attn_train_logsoftmax_loss_fwd", "attn_train_logsoftmax_loss_bwd",
+           "attn_train_step_host_arena_size", "attn_train_step_host",
+           "attn_train_host_session_create", "attn_train_host_session_step",
+           "attn_train_host_session_join", "attn_train_host_session_destroy")
 
 
 class AttnError(RuntimeError):
@@ -49,6 +52,11 @@ class Problem(ctypes.Structure):
 
 
 OUT_DTYPES = {"bf16": 0, "fp32": 1}
+
+
+class HostIO(ctypes.Structure):
+    """attn_host_io: host addresses of one step's inputs and outputs."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "dout", "o", "lse", "dq", "dk", "dv")]
 
 
 _lib = None
@@ -89,6 +97,15 @@ def load(path: str = LIB_PATH):
             "attn_train_logsoftmax_loss_bwd": (st, [ctypes.c_int64, ctypes.c_int64, vp,
                                                     ctypes.c_int64, vp, ctypes.c_int64, vp,
                                                     vp, vp, vp, vp]),
+            "attn_train_step_host_arena_size": (st, [P, ctypes.c_int,
+                                                     ctypes.POINTER(ctypes.c_size_t)]),
+            "attn_train_step_host": (st, [P, ctypes.POINTER(HostIO), ctypes.c_int, vp,
+                                          ctypes.c_size_t, vp]),
+            "attn_train_host_session_create": (st, [P, ctypes.c_int, vp, ctypes.c_size_t,
+                                                    ctypes.POINTER(vp)]),
+            "attn_train_host_session_step": (st, [vp, ctypes.POINTER(HostIO), vp]),
+            "attn_train_host_session_join": (st, [vp, vp]),
+            "attn_train_host_session_destroy": (st, [vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -104,38 +121,44 @@ def _check(status: int):
         raise AttnError(status, msg)
 
 
-def _lens_ptr(seq_lengths) -> int:
-    """Device address of an int32 [B] tensor of key lengths (0 = none)."""
+def _lens_ptr(seq_lengths, host=False) -> int:
+    """Address of an int32 [B] tensor of key lengths (0 = none); a CUDA tensor,
+    or a CPU one for the host-memory step (host=True)."""
     if seq_lengths is None:
         return 0
     import torch
-    if seq_lengths.dtype != torch.int32 or not seq_lengths.is_cuda or not seq_lengths.is_contiguous():
-        raise ValueError("seq_lengths must be a contiguous int32 CUDA tensor")
+    where = "CPU" if host else "CUDA"
+    if (seq_lengths.dtype != torch.int32 or seq_lengths.is_cuda == host
+            or not seq_lengths.is_contiguous()):
+        raise ValueError(f"seq_lengths must be a contiguous int32 {where} tensor")
     return seq_lengths.data_ptr()
 
 
-def _add_mask(add_mask):
-    """(address, batch stride, row stride) of a bf16 CUDA additive mask [Sq, Skv]
-    or [B, Sq, Skv] with contiguous keys; a 2-D or batch-1 mask serves every entry."""
+def _add_mask(add_mask, host=False):
+    """(address, batch stride, row stride) of a bf16 additive mask [Sq, Skv]
+    or [B, Sq, Skv] with contiguous keys; a 2-D or batch-1 mask serves every entry.
+    A CUDA tensor, or a CPU one for the host-memory step (host=True)."""
     if add_mask is None:
         return 0, 0, 0
     import torch
-    if add_mask.dtype != torch.bfloat16 or not add_mask.is_cuda or add_mask.stride(-1) != 1:
-        raise ValueError("add_mask must be a bf16 CUDA tensor with contiguous keys")
+    where = "CPU" if host else "CUDA"
+    if add_mask.dtype != torch.bfloat16 or add_mask.is_cuda == host or add_mask.stride(-1) != 1:
+        raise ValueError(f"add_mask must be a bf16 {where} tensor with contiguous keys")
     sb = 0 if add_mask.dim() == 2 or add_mask.shape[0] == 1 else add_mask.stride(0)
     return add_mask.data_ptr(), sb, add_mask.stride(-2)
 
 
 def problem(B, Hq, Hkv, Sq, Skv, D, mask="causal", ttt_step=0, scale=0.0, out="bf16",
-            window=None, seq_lengths=None, add_mask=None) -> Problem:
-    """window=(left, right) for the window mask; seq_lengths = device int32 [B]
-    key lengths; add_mask = device bf16 additive mask (the caller keeps the
-    tensors alive while the problem is used)."""
+            window=None, seq_lengths=None, add_mask=None, host=False) -> Problem:
+    """window=(left, right) for the window mask; seq_lengths = int32 [B] key
+    lengths; add_mask = bf16 additive mask; both device tensors, or CPU tensors
+    with host=True (the problem of step_host).  The caller keeps the tensors
+    alive while the problem is used."""
     m = MASKS[mask] if isinstance(mask, str) else int(mask)
     wl, wr = (0, 0) if window is None else (int(window[0]), int(window[1]))
-    am, amsb, amsq = _add_mask(add_mask)
+    am, amsb, amsq = _add_mask(add_mask, host)
     return Problem(B, Hq, Hkv, Sq, Skv, D, m, ttt_step, float(scale), OUT_DTYPES[out], wl, wr,
-                   _lens_ptr(seq_lengths), am, amsb, amsq)
+                   _lens_ptr(seq_lengths, host), am, amsb, amsq)
 
 
 def problem_for(q, k, mask="causal", ttt_step=0, scale=None, out="bf16", window=None,
@@ -214,6 +237,69 @@ def bwd_noalloc_raw(p: Problem, q, k, v, o, dout, lse, dq, dk, dv, stream=None):
     _check(load().attn_train_bwd_noalloc(ctypes.byref(p), view(q), view(k), view(v), view(o),
                                          view(dout), ctypes.c_void_p(lse.data_ptr()), view(dq),
                                          view(dk), view(dv), _stream(stream)))
+
+
+def step_host_arena_size(p: Problem, kv_heads_per_chunk: int = 0) -> int:
+    """Device arena bytes attn_train_step_host needs (0 = automatic chunk)."""
+    n = ctypes.c_size_t(0)
+    _check(load().attn_train_step_host_arena_size(ctypes.byref(p), int(kv_heads_per_chunk),
+                                                  ctypes.byref(n)))
+    return int(n.value)
+
+
+_HOST_IO = ("q", "k", "v", "dout", "o", "lse", "dq", "dk", "dv")
+
+
+def _host_io(host: dict) -> HostIO:
+    for n in _HOST_IO:
+        t = host[n]
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous CPU tensor")
+    return HostIO(*(host[n].data_ptr() for n in _HOST_IO))
+
+
+def step_host_raw(p: Problem, host: dict, arena, kv_heads_per_chunk: int = 0, stream=None):
+    """attn_train_step_host: one forward + backward from host memory.  `host`
+    maps q, k, v, dout (inputs) and o, lse, dq, dk, dv (outputs) to dense CPU
+    tensors (pinned for overlapped copies); `arena` is a CUDA uint8 tensor of
+    at least step_host_arena_size bytes.  Returns once enqueued: the outputs
+    are valid after the stream is synchronized."""
+    io = _host_io(host)
+    _check(load().attn_train_step_host(ctypes.byref(p), ctypes.byref(io), int(kv_heads_per_chunk),
+                                       ctypes.c_void_p(arena.data_ptr()), arena.numel(),
+                                       _stream(stream)))
+
+
+class HostSession:
+    """attn_train_host_session_*: steps of one problem from host memory whose
+    copies overlap the neighbouring steps' kernels.  Keep `p` (and its host
+    key lengths / mask tensors) and the arena alive while the session is used."""
+
+    def __init__(self, p: Problem, arena, kv_heads_per_chunk: int = 0):
+        self._lib = load()
+        self.p = p
+        self.arena = arena
+        h = ctypes.c_void_p(0)
+        _check(self._lib.attn_train_host_session_create(ctypes.byref(p), int(kv_heads_per_chunk),
+                                                        ctypes.c_void_p(arena.data_ptr()),
+                                                        arena.numel(), ctypes.byref(h)))
+        self._h = h
+
+    def step(self, host: dict, stream=None):
+        """Enqueue one step; outputs are valid after join() and a stream sync."""
+        io = _host_io(host)
+        _check(self._lib.attn_train_host_session_step(self._h, ctypes.byref(io), _stream(stream)))
+
+    def join(self, stream=None):
+        _check(self._lib.attn_train_host_session_join(self._h, _stream(stream)))
+
+    def close(self):
+        if self._h:
+            self._lib.attn_train_host_session_destroy(self._h)
+            self._h = ctypes.c_void_p(0)
+
+    def __del__(self):
+        self.close()
 
 
 def device_status(stream=None):

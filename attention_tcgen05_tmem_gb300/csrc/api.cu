@@ -262,6 +262,12 @@ attn_status noalloc_scratch(void** out) {
 
 }  // namespace
 
+namespace attn {
+int set_last_error(int status, const char* msg) {
+  return fail(static_cast<attn_status>(status), "%s", msg);
+}
+}  // namespace attn
+
 extern "C" {
 
 attn_status attn_train_supports(const attn_problem* p) {

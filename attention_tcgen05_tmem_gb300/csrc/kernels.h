@@ -93,4 +93,8 @@ cudaError_t launch_probe(int mode, int D, const CUtensorMap& ta, const CUtensorM
                          const void* a_global, float* c, Ctl ctl, cudaStream_t s);
 cudaError_t launch_selftest_wait(Ctl ctl, cudaStream_t s);
 
+// Records `msg` as the calling thread's last error message (attn_train_last_error)
+// and returns `status`; for host code outside the C ABI's own translation unit.
+int set_last_error(int status, const char* msg);
+
 }  // namespace attn

@@ -69,6 +69,8 @@ def parse_args():
                     help="dtype of O, dQ, dK, dV (fp32 is the parity-gated configuration)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-chunk", type=int, default=0,
+                    help="kv heads per chunk of the host-memory step (0 = automatic)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     return ap.parse_args()
@@ -300,36 +302,36 @@ def run_ours(args, ws, local_rank, dist):
 
     e2e_ms, h2d, d2h = None, 0, 0
     if not args.no_e2e:
-        # end to end through the C ABI with pinned host buffers: inputs copied in and all
-        # outputs (O, LSE, dQ, dK, dV) copied out inside the timed region
+        # end to end through the C ABI's host-memory session (attn_train_host_session_*):
+        # every step copies q, k, v, dO (and key lengths / mask) in from pinned host
+        # buffers and O, LSE, dQ, dK, dV out; the copies overlap the kernels of the
+        # same and the neighbouring steps, and the timed region ends after the last
+        # step's copies (join + synchronize)
         hosts = []
         for c in cases:
+            w = c.w
             pin = {n: c.x[n].pin_memory()
                    for n in ("q", "k", "v", "dout", "seq_lengths", "add_mask") if n in c.x}
             outs = {n: torch.empty(getattr(c, n).shape, dtype=getattr(c, n).dtype).pin_memory()
                     for n in ("o", "lse", "dq", "dk", "dv")}
-            hosts.append((pin, outs))
+            hp = binding.problem(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.mask, w.ttt_step, 0.0,
+                                 args.out, w.window, pin.get("seq_lengths"), pin.get("add_mask"),
+                                 host=True)
+            io = {"q": pin["q"], "k": pin["k"], "v": pin["v"], "dout": pin["dout"], **outs}
+            arena = torch.empty(binding.step_host_arena_size(hp, args.e2e_chunk),
+                                dtype=torch.uint8, device=dev)
+            hosts.append((binding.HostSession(hp, arena, args.e2e_chunk), io))
             h2d += sum(t.numel() * t.element_size() for t in pin.values())
             d2h += sum(t.numel() * t.element_size() for t in outs.values())
 
         def e2e_step():
-            for c, (pin, outs) in zip(cases, hosts):
-                c.q.copy_(pin["q"], non_blocking=True)
-                c.k.copy_(pin["k"], non_blocking=True)
-                c.v.copy_(pin["v"], non_blocking=True)
-                c.do.copy_(pin["dout"], non_blocking=True)
-                if c.lens is not None:
-                    c.lens.copy_(pin["seq_lengths"], non_blocking=True)
-                if c.add is not None:
-                    c.add.copy_(pin["add_mask"], non_blocking=True)
-                binding.fwd_raw(c.p, c.q, c.k, c.v, c.o, c.lse, stream.cuda_stream)
-                binding.bwd_raw(c.p, c.q, c.k, c.v, c.o, c.do, c.lse, c.dq, c.dk, c.dv, c.ws,
-                                stream.cuda_stream)
-                for n, t in outs.items():
-                    t.copy_(getattr(c, n), non_blocking=True)
+            for sess, io in hosts:
+                sess.step(io, stream.cuda_stream)
 
         for _ in range(2):
             e2e_step()
+        for sess, _ in hosts:
+            sess.join(stream.cuda_stream)
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if dist:
@@ -339,10 +341,14 @@ def run_ours(args, ws, local_rank, dist):
         e0.record(stream)
         for _ in range(Ke):
             e2e_step()
+        for sess, _ in hosts:
+            sess.join(stream.cuda_stream)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = e0.elapsed_time(e1) / Ke * K
         binding.device_status()
+        for sess, _ in hosts:
+            sess.close()
 
     total_ms, e2e_max = max_over_ranks([total_ms, e2e_ms or 0.0], dist, dev)
     return {"K": K, "total_ms": total_ms, "e2e_ms": e2e_max if e2e_ms else None,

@@ -52,9 +52,10 @@
  *
  * Ownership and streams
  * ---------------------
- * All tensor pointers are device pointers owned by the caller; the library
- * allocates no device memory and keeps no state between calls besides a
- * device error word and cached driver entry points.  Work is enqueued on the
+ * All tensor pointers are device pointers owned by the caller (except in the
+ * host-memory step entry points below); the library allocates no device
+ * memory and keeps no state between calls besides a device error word, cached
+ * driver entry points and the host-step sessions a caller creates.  Work is enqueued on the
  * caller's stream (a cudaStream_t passed as void*, NULL = legacy default) and
  * the calls return before it finishes.  Outputs are overwritten, not
  * accumulated; summing gradients over TTT steps is the caller's job.
@@ -206,6 +207,92 @@ attn_status attn_train_bwd_noalloc(const attn_problem* p, attn_tensor q, attn_te
                                    attn_tensor v, attn_tensor o, attn_tensor dout,
                                    const float* lse, attn_tensor dq, attn_tensor dk,
                                    attn_tensor dv, void* stream);
+
+/* ---- steps from host memory --------------------------------------------
+ *
+ * attn_train_step_host runs the forward and the backward of one problem whose
+ * inputs and outputs are HOST arrays: it copies q, k, v and dout to the
+ * device, computes O, LSE, dQ, dK and dV with the same kernels as
+ * attn_train_fwd and attn_train_bwd, and copies the five results back.  A
+ * session (attn_train_host_session_*) does the same for a sequence of steps
+ * of one problem and overlaps each step's copies with its neighbours' kernels.
+ *
+ * Host arrays are dense: q, dout, o, dq [B, Hq, Sq, D]; k, v, dk, dv
+ * [B, Hkv, Skv, D]; lse [B, Hq, Sq] (fp32).  q, k, v, dout are bf16; o, dq,
+ * dk, dv have the problem's out_dtype.  In these entry points the problem's
+ * seq_lengths and add_mask are host pointers as well (add_mask keeps its
+ * strides add_mask_sb / add_mask_sq; no alignment needed); both are copied in
+ * with every step.  Pinned host memory (cudaHostAlloc / cudaHostRegister)
+ * lets the copies run alongside the kernels; pageable memory works but
+ * serializes them.
+ *
+ * arena: caller-owned device buffer of at least
+ * attn_train_step_host_arena_size bytes, 256-byte aligned, contents ignored.
+ * It holds two slots of chunk buffers (see below), two copies of the key
+ * lengths and mask, and the backward's workspace; the library allocates no
+ * device memory.
+ *
+ * Pipelining.  A step is one chunk (kv_heads_per_chunk <= 0: the whole
+ * problem), or chunks of kv_heads_per_chunk kv heads (1 to Hkv, with their
+ * Hq/Hkv query heads each) of one batch entry; GQA groups are independent
+ * problems and contiguous slices of the host arrays.  Chunks take the two
+ * slots in turn, also across the steps of a session.  Per chunk, on three
+ * streams: its inputs are copied in while the previous chunk computes; O and
+ * LSE are copied out during its backward; the backward runs Delta prep and dQ
+ * first, so that dQ is copied out while dK and dV are computed.  In a session
+ * the next step's copy-in overlaps this step's kernels, so one chunk per step
+ * is the fastest choice there; smaller chunks overlap more within a single
+ * step at the price of fuller kernel tails.  No kernel mixes heads, so the
+ * results equal those of attn_train_fwd + attn_train_bwd on the whole problem
+ * bit for bit.
+ *
+ * Streams.  Compute is enqueued on `stream`; the copies run on two streams of
+ * the session.  The first step waits for the work already on `stream` (the
+ * arena may still be in use); later steps do not, so their copy-in runs
+ * during the previous step's compute.  Calls return once everything is
+ * enqueued.  attn_train_host_session_join makes `stream` wait for every copy
+ * enqueued so far: the host outputs are valid after a join followed by a
+ * synchronization of `stream`, and the host inputs of a step may be changed
+ * only then.  Validation happens before anything is enqueued. */
+typedef struct {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* dout;
+  void* o;
+  float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+} attn_host_io;
+
+typedef struct attn_host_session_s* attn_host_session;
+
+/* Arena bytes for this problem and chunk size (kv_heads_per_chunk <= 0: one
+ * chunk for the whole step). */
+attn_status attn_train_step_host_arena_size(const attn_problem* p, int kv_heads_per_chunk,
+                                            size_t* bytes);
+
+/* One step: create a session, enqueue the step, join `stream`, release the
+ * session.  The outputs are valid once `stream` has been synchronized. */
+attn_status attn_train_step_host(const attn_problem* p, const attn_host_io* io,
+                                 int kv_heads_per_chunk, void* arena, size_t arena_bytes,
+                                 void* stream);
+
+/* A session over `arena` for steps of problem *p (copied; its host key
+ * lengths and mask pointers are read at every step).  Creates two CUDA
+ * streams and a few events (host objects; no device memory). */
+attn_status attn_train_host_session_create(const attn_problem* p, int kv_heads_per_chunk,
+                                           void* arena, size_t arena_bytes,
+                                           attn_host_session* out);
+/* Enqueues one step (copy-in, forward, backward, copy-out). */
+attn_status attn_train_host_session_step(attn_host_session s, const attn_host_io* io,
+                                         void* stream);
+/* Makes `stream` wait for every copy the session has enqueued so far. */
+attn_status attn_train_host_session_join(attn_host_session s, void* stream);
+/* Releases the session (work still in flight completes; the arena must stay
+ * allocated until it has). */
+attn_status attn_train_host_session_destroy(attn_host_session s);
 
 /* Soft-target log-softmax loss (SpecForge long-context post, "In-place
  * Gradient Calculation": the EAGLE3 loss of one TTT step),

@@ -8,6 +8,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from attention_tcgen05_tmem_gb300 import binding
 from attention_tcgen05_tmem_gb300 import build as lib_build
@@ -101,6 +102,66 @@ def test_workspace_size(lib):
     # TTT step t: Delta plus per-row weight and score gradient of each diagonal
     p = binding.problem(1, 32, 8, 8192, 7 * 8192, 128, "ttt", 6)
     assert binding.workspace_size(p) == 32 * 8192 * 4 * (1 + 2 * 6)
+
+
+def _up(n):
+    return (n + 255) // 256 * 256
+
+
+def test_step_host_arena_size(lib):
+    """Arena = 2 x [key lengths][mask copy], the chunk workspace, 2 slots; a slot
+    holds one chunk's q, k, v, dout, o, lse, dq, dk, dv."""
+    # B=2, 2 kv heads of 2 q heads each, 1 kv head per chunk -> 4 chunks, 2 slots
+    p = binding.problem(2, 4, 2, 100, 100, 64, "causal", out="bf16", host=True)
+    nq, nk, nl = 2 * 100 * 64, 100 * 64, 2 * 100
+    slot = _up(nq * 2) * 4 + _up(nk * 2) * 4 + _up(nl * 4)  # q, dout, o, dq; k, v, dk, dv; lse
+    ws = _up(nl * 4)  # Delta of one chunk
+    assert binding.step_host_arena_size(p, 1) == ws + 2 * slot
+    # fp32 outputs, one chunk (the whole problem): still two slots (a session's
+    # next step takes the other one)
+    p = binding.problem(1, 4, 2, 100, 100, 64, "causal", out="fp32", host=True)
+    nq, nk, nl = 4 * 100 * 64, 2 * 100 * 64, 4 * 100
+    slot = 2 * _up(nq * 2) + 2 * _up(nk * 2) + 2 * _up(nq * 4) + 2 * _up(nk * 4) + _up(nl * 4)
+    assert binding.step_host_arena_size(p, 2) == _up(nl * 4) + 2 * slot
+    # chunk <= 0: the whole step is one chunk (all batch entries)
+    p = binding.problem(1, 32, 4, 16384, 16384, 128, "causal", out="bf16", host=True)
+    assert binding.step_host_arena_size(p, 0) == binding.step_host_arena_size(p, 4)
+    p = binding.problem(2, 4, 2, 100, 100, 64, "causal", out="bf16", host=True)
+    nq, nk, nl = 2 * 4 * 100 * 64, 2 * 2 * 100 * 64, 2 * 4 * 100
+    slot = _up(nq * 2) * 4 + _up(nk * 2) * 4 + _up(nl * 4)
+    assert binding.step_host_arena_size(p, 0) == _up(nl * 4) + 2 * slot
+    # host key lengths and mask get arena space of their own
+    lens = torch.tensor([100, 50], dtype=torch.int32)
+    am = torch.zeros(100, 104, dtype=torch.bfloat16)[:, :100]
+    p0 = binding.problem(2, 2, 2, 100, 100, 64, "full", host=True)
+    p1 = binding.problem(2, 2, 2, 100, 100, 64, "full", seq_lengths=lens, add_mask=am, host=True)
+    mask_ws = _up(100 * 104 * 2)  # the backward's transposed copy of the mask
+    assert (binding.step_host_arena_size(p1, 1) - binding.step_host_arena_size(p0, 1)
+            == 2 * (_up(2 * 4) + _up((99 * 104 + 100) * 2)) + mask_ws)
+
+
+def test_step_host_validation(lib):
+    p = binding.problem(1, 4, 2, 128, 128, 64, "causal", host=True)
+    need = binding.step_host_arena_size(p, 0)
+    io = binding.HostIO(*([0x10000] * 9))
+    step = lib.attn_train_step_host
+    assert step(ctypes.byref(p), ctypes.byref(io), 3, ctypes.c_void_p(0x100000), need, None) == 1
+    assert b"kv_heads_per_chunk" in lib.attn_train_last_error()
+    assert step(ctypes.byref(p), None, 0, ctypes.c_void_p(0x100000), need, None) == 1
+    bad = binding.HostIO(*([0x10000] * 8 + [0]))
+    assert step(ctypes.byref(p), ctypes.byref(bad), 0, ctypes.c_void_p(0x100000), need, None) == 1
+    assert step(ctypes.byref(p), ctypes.byref(io), 0, None, need, None) == 4
+    assert step(ctypes.byref(p), ctypes.byref(io), 0, ctypes.c_void_p(0x100010), need, None) == 3
+    assert step(ctypes.byref(p), ctypes.byref(io), 0, ctypes.c_void_p(0x100000), need - 1,
+                None) == 4
+    assert b"arena too small" in lib.attn_train_last_error()
+    # the problem itself is validated as for the device entry points
+    q = binding.problem(1, 4, 3, 128, 128, 64, "causal", host=True)
+    assert step(ctypes.byref(q), ctypes.byref(io), 0, ctypes.c_void_p(0x100000), need, None) == 1
+    # a host mask needs no 16-byte alignment (it is copied to an aligned arena offset)
+    am = torch.zeros(130, 136, dtype=torch.bfloat16)[1:129, 4:132]
+    p2 = binding.problem(1, 4, 2, 128, 128, 64, "full", add_mask=am, host=True)
+    assert binding.step_host_arena_size(p2, 0) > 0
 
 
 def _t(ptr=0x1000, sb=4 * 256 * 64, sh=256 * 64, ss=64):
