@@ -75,7 +75,9 @@ __device__ __forceinline__ float dot8(const uint4& x, const uint4& y) {
 // TTT step t > 0 the same row group also computes, for each suffix diagonal
 // i = 1..t (key row i*Sq + q), p_i = exp(c q.k_i - LSE) and
 // ds_i = p_i (dO.v_i - Delta), for the dQ epilogue and the suffix-key pass.
-template <int D>
+// TTT: instantiated separately for steps with suffix diagonals, so that their
+// registers do not lower the occupancy of the plain Delta pass.
+template <int D, bool TTT>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdArgs a) {
   constexpr int TPR = D / 8;  // threads per row
   constexpr int RPB = 256 / TPR;
@@ -86,11 +88,23 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdArgs a) {
   float acc = 0.f;
   int q = 0, h = 0, b = 0;
   uint4 ga = make_uint4(0u, 0u, 0u, 0u);
+  // TTT: the q row, LSE and the k, v rows of the first diagonal are loaded
+  // together with dO and O, and each later diagonal's rows one step ahead of
+  // its reduction, so that the loads' latencies overlap
+  uint4 qa = make_uint4(0u, 0u, 0u, 0u), kk = qa, vv = qa;
+  float lse2 = 0.f;
   if (in) {
     q = (int)(row % a.d.Sq);
     const int bh = (int)(row / a.d.Sq);
     h = bh % a.d.Hq;
     b = bh / a.d.Hq;
+    if constexpr (TTT) {
+      const int hk = h / a.d.G;
+      qa = *reinterpret_cast<const uint4*>(row_ptr(a.q, b, h, q) + sub * 8);
+      lse2 = a.lse[row] * kLog2e;
+      kk = *reinterpret_cast<const uint4*>(row_ptr(a.k, b, hk, (int64_t)a.d.Sq + q) + sub * 8);
+      vv = *reinterpret_cast<const uint4*>(row_ptr(a.v, b, hk, (int64_t)a.d.Sq + q) + sub * 8);
+    }
     const __nv_bfloat16* g = row_ptr(a.dout, b, h, q) + sub * 8;
     ga = *reinterpret_cast<const uint4*>(g);
     const __nv_bfloat162* gv = reinterpret_cast<const __nv_bfloat162*>(&ga);
@@ -123,23 +137,18 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdArgs a) {
   for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, TPR);
   if (in && sub == 0) a.delta[row] = acc;
 
-  const int t = a.d.geom.ttt;  // uniform over the grid
-  if (t > 0) {
+  if constexpr (TTT) {
+    const int t = a.d.geom.ttt;  // uniform over the grid, > 0
     const int hk = h / a.d.G;
     const bool diag_vis = in && q < with_len(a.d.geom, a.d.seqlens, b).kv_len;
-    uint4 qa = make_uint4(0u, 0u, 0u, 0u);
-    float lse2 = 0.f;
-    if (in) {
-      qa = *reinterpret_cast<const uint4*>(row_ptr(a.q, b, h, q) + sub * 8);
-      lse2 = a.lse[row] * kLog2e;
-    }
     for (int i = 1; i <= t; ++i) {
-      float s = 0.f, dp = 0.f;
-      if (in) {
-        const int64_t kr = (int64_t)i * a.d.Sq + q;
-        s = dot8(qa, *reinterpret_cast<const uint4*>(row_ptr(a.k, b, hk, kr) + sub * 8));
-        dp = dot8(ga, *reinterpret_cast<const uint4*>(row_ptr(a.v, b, hk, kr) + sub * 8));
+      const uint4 kc = kk, vc = vv;
+      if (in && i < t) {
+        const int64_t kr = (int64_t)(i + 1) * a.d.Sq + q;
+        kk = *reinterpret_cast<const uint4*>(row_ptr(a.k, b, hk, kr) + sub * 8);
+        vv = *reinterpret_cast<const uint4*>(row_ptr(a.v, b, hk, kr) + sub * 8);
       }
+      float s = dot8(qa, kc), dp = dot8(ga, vc);
 #pragma unroll
       for (int off = TPR / 2; off > 0; off >>= 1) {
         s += __shfl_xor_sync(0xffffffffu, s, off, TPR);
@@ -939,59 +948,120 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ================================================================ TTT diag
 // dK/dV of the keys of appended segments i = 1..t: key row i*Sq + r is seen
-// only by query row r of every q head of its group.  One warp per key row;
-// dot products reduce with warp shuffles in a fixed butterfly order.
+// only by query row r of every q head of its group.  One warp per (batch
+// entry, kv head, row r) serves all t segments of that row, so each q and dO
+// row is read once: lane l holds columns [l*VEC, l*VEC + VEC).  The sums over
+// the group's q heads run in ascending head order.
 template <int D>
+struct SuffixVec {
+  static constexpr int VEC = D >= 32 ? D / 32 : 1;  // columns per lane
+  static constexpr int LANES = D / VEC;             // lanes holding columns
+};
+
+template <int VEC>
+__device__ __forceinline__ void load_bf16_cols(const __nv_bfloat16* p, float* f) {
+  if constexpr (VEC == 4) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+  } else if constexpr (VEC == 2) {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+    f[0] = a.x; f[1] = a.y;
+  } else {
+    f[0] = __bfloat162float(*p);
+  }
+}
+
+template <int VEC>
+__device__ __forceinline__ void store_cols(void* base, int64_t off, bool f32, const float* v) {
+  if (f32) {
+    float* o = reinterpret_cast<float*>(base) + off;
+    if constexpr (VEC == 4) {
+      *reinterpret_cast<float4*>(o) = make_float4(v[0], v[1], v[2], v[3]);
+    } else if constexpr (VEC == 2) {
+      *reinterpret_cast<float2*>(o) = make_float2(v[0], v[1]);
+    } else {
+      o[0] = v[0];
+    }
+  } else {
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(base) + off;
+    if constexpr (VEC == 4) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]), hi = __floats2bfloat162_rn(v[2], v[3]);
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&lo);
+      u.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(o) = u;
+    } else if constexpr (VEC == 2) {
+      *reinterpret_cast<__nv_bfloat162*>(o) = __floats2bfloat162_rn(v[0], v[1]);
+    } else {
+      o[0] = __float2bfloat16_rn(v[0]);
+    }
+  }
+}
+
+// CH: segments per pass over the q and dO rows (1, 2, 4 or 8, the smallest
+// that covers t up to 8), so that the accumulators' registers scale with t.
+template <int D, int CH>
 __global__ void __launch_bounds__(256) ttt_diag_bwd_kernel(const BwdArgs a) {
-  constexpr int EPL = (D + 31) / 32;  // elements per lane
+  constexpr int VEC = SuffixVec<D>::VEC, LANES = SuffixVec<D>::LANES;
   const Dims& d = a.d;
   const int t = d.geom.ttt;
-  const int64_t rows = (int64_t)d.B * d.Hkv * t * d.Sq;
+  const int64_t rows = (int64_t)d.B * d.Hkv * d.Sq;
   const int64_t wrow = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (wrow >= rows) return;
   const int lane = threadIdx.x & 31;
+  const bool act = lane < LANES;
+  const int c0 = lane * VEC;
   const int r = (int)(wrow % d.Sq);
-  int64_t rest = wrow / d.Sq;
-  const int i = 1 + (int)(rest % t);
-  rest /= t;
-  const int hk = (int)(rest % d.Hkv);
-  const int b = (int)(rest / d.Hkv);
-  const int64_t kr = (int64_t)i * d.Sq + r;
-  float dk[EPL], dv[EPL];
+  const int64_t bk = wrow / d.Sq;
+  const int hk = (int)(bk % d.Hkv);
+  const int b = (int)(bk / d.Hkv);
+  for (int i0 = 1; i0 <= t; i0 += CH) {
+    float dk[CH][VEC], dv[CH][VEC];
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) {
-    dk[e] = 0.f;
-    dv[e] = 0.f;
-  }
-  // p and ds of (query row r of q head h, diagonal i) come from the prep pass
-  for (int gq = 0; gq < d.G; ++gq) {
-    const int h = hk * d.G + gq;
-    const int64_t rrow = ((int64_t)b * d.Hq + h) * d.Sq + r;
-    const float p = a.ttt_p[rrow * t + (i - 1)];
-    const float ds = a.ttt_ds[rrow * t + (i - 1)];
-    const __nv_bfloat16* qrow = row_ptr(a.q, b, h, r);
-    const __nv_bfloat16* dorow = row_ptr(a.dout, b, h, r);
+    for (int u = 0; u < CH; ++u)
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      const int c = lane + 32 * e;
-      if (c < D) {
-        dv[e] = fmaf(p, __bfloat162float(dorow[c]), dv[e]);
-        dk[e] = fmaf(ds, __bfloat162float(qrow[c]), dk[e]);
+      for (int e = 0; e < VEC; ++e) dk[u][e] = dv[u][e] = 0.f;
+    // p and ds of (query row r of q head h, diagonal i) come from the prep pass
+    for (int gq = 0; gq < d.G; ++gq) {
+      const int h = hk * d.G + gq;
+      const int64_t rrow = ((int64_t)b * d.Hq + h) * d.Sq + r;
+      float qv[VEC], gv[VEC];
+      if (act) {
+        load_bf16_cols<VEC>(row_ptr(a.q, b, h, r) + c0, qv);
+        load_bf16_cols<VEC>(row_ptr(a.dout, b, h, r) + c0, gv);
+      }
+      float p[CH], ds[CH];
+#pragma unroll
+      for (int u = 0; u < CH; ++u) {
+        const bool ok = i0 + u <= t;
+        p[u] = ok ? a.ttt_p[rrow * t + (i0 + u - 1)] : 0.f;
+        ds[u] = ok ? a.ttt_ds[rrow * t + (i0 + u - 1)] : 0.f;
+      }
+      if (act) {
+#pragma unroll
+        for (int u = 0; u < CH; ++u)
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) {
+            dv[u][e] = fmaf(p[u], gv[e], dv[u][e]);
+            dk[u][e] = fmaf(ds[u], qv[e], dk[u][e]);
+          }
       }
     }
-  }
-  const int64_t koff = b * a.dk.sb + hk * a.dk.sh + kr * a.dk.ss;
-  const int64_t voff = b * a.dv.sb + hk * a.dv.sh + kr * a.dv.ss;
+    if (act) {
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) {
-    const int c = lane + 32 * e;
-    if (c < D) {
-      if (d.out_f32) {
-        reinterpret_cast<float*>(a.dk.ptr)[koff + c] = dk[e] * d.scale;
-        reinterpret_cast<float*>(a.dv.ptr)[voff + c] = dv[e];
-      } else {
-        reinterpret_cast<__nv_bfloat16*>(a.dk.ptr)[koff + c] = __float2bfloat16_rn(dk[e] * d.scale);
-        reinterpret_cast<__nv_bfloat16*>(a.dv.ptr)[voff + c] = __float2bfloat16_rn(dv[e]);
+      for (int u = 0; u < CH; ++u) {
+        const int i = i0 + u;
+        if (i > t) break;
+        const int64_t kr = (int64_t)i * d.Sq + r;
+        float k_out[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) k_out[e] = dk[u][e] * d.scale;
+        store_cols<VEC>(a.dk.ptr, b * a.dk.sb + hk * a.dk.sh + kr * a.dk.ss + c0,
+                        d.out_f32 != 0, k_out);
+        store_cols<VEC>(a.dv.ptr, b * a.dv.sb + hk * a.dv.sh + kr * a.dv.ss + c0,
+                        d.out_f32 != 0, dv[u]);
       }
     }
   }
@@ -1003,7 +1073,10 @@ cudaError_t launch_bwd_dw(const BwdArgs& a, const Maps& m, unsigned passes, cuda
   if (passes & 1u) {
     constexpr int RPB = 256 / (D / 8);
     const int64_t rows = (int64_t)a.d.B * a.d.Hq * a.d.Sq;
-    bwd_prep_kernel<D><<<(unsigned)((rows + RPB - 1) / RPB), 256, 0, s>>>(a);
+    if (a.d.geom.ttt > 0)
+      bwd_prep_kernel<D, true><<<(unsigned)((rows + RPB - 1) / RPB), 256, 0, s>>>(a);
+    else
+      bwd_prep_kernel<D, false><<<(unsigned)((rows + RPB - 1) / RPB), 256, 0, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (a.addm_t != nullptr) {
       const dim3 grid((unsigned)cdiv(a.d.Skv, 64), (unsigned)cdiv((int)a.addm_t_sq, 64),
@@ -1037,8 +1110,17 @@ cudaError_t launch_bwd_dw(const BwdArgs& a, const Maps& m, unsigned passes, cuda
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if ((passes & 8u) && a.d.geom.ttt > 0) {
-    const int64_t rows = (int64_t)a.d.B * a.d.Hkv * a.d.geom.ttt * a.d.Sq;
-    ttt_diag_bwd_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(a);
+    const int64_t rows = (int64_t)a.d.B * a.d.Hkv * a.d.Sq;  // one warp per key row r
+    const unsigned grid = (unsigned)((rows + 7) / 8);
+    const int t = a.d.geom.ttt;
+    if (t <= 1)
+      ttt_diag_bwd_kernel<D, 1><<<grid, 256, 0, s>>>(a);
+    else if (t <= 2)
+      ttt_diag_bwd_kernel<D, 2><<<grid, 256, 0, s>>>(a);
+    else if (t <= 4)
+      ttt_diag_bwd_kernel<D, 4><<<grid, 256, 0, s>>>(a);
+    else
+      ttt_diag_bwd_kernel<D, 8><<<grid, 256, 0, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
