@@ -208,7 +208,9 @@ struct DkdvLayout {
 
 // W: the mask has a lower key bound (window) or per-batch key lengths; the
 // other masks take the one-sided form of the tile arithmetic.
-template <int D, bool W>
+// W: general mask arithmetic (window, key lengths, additive mask); M (implies
+// W): an additive mask is present, in an instantiation of its own.
+template <int D, bool W, bool M>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -447,6 +449,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* dl = stats + s * 256 + 128 + 64 * wg;
       const bool tr = lane == 0 && quad == 0;
       if (tr) ATTN_TR(2 + wg, 0, it);
+      // additive mask (transposed copy, by key row): loaded before the wait for S^T
+      const bool addm = M && kv < d.Skv;
+      uint4 mreg[M ? 8 : 1];
+      if constexpr (M) {
+        if (addm)
+          load_bias_row<64>(mreg, a.addm_t + b * a.addm_t_sb + (int64_t)kv * a.addm_t_sq,
+                            q0 + 64 * wg, d.Sq);
+      }
       if (!(ok = mbar_wait_warp(&s_full[DB ? (it & 1) : 0],
                                 (uint32_t)(DB ? (it >> 1) : it) & 1u, ctl)))
         break;
@@ -460,9 +470,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // -lse2 = -inf.  Masked scores go to -inf (exponential 0) in a pass of its own,
       // so that the exponential loop of full tiles carries no per-element select.
       if constexpr (W) {
-        if (a.addm_t != nullptr && kv < d.Skv)
-          add_bias_row<64>(raw, a.addm_t + b * a.addm_t_sb + (int64_t)kv * a.addm_t_sq,
-                           q0 + 64 * wg, d.Sq, inv_scale);
+        if constexpr (M) {
+          if (addm) apply_bias_row<64>(raw, mreg, inv_scale);
+        }
         if (!in_range(full_q, q0)) {
           int clo, chi;
           row_range_for_kv(g, kv, q0 + 64 * wg, &clo, &chi);
@@ -585,7 +595,7 @@ struct DqLayout {
   static_assert(ALLOC <= 227 * 1024, "shared memory budget");
 };
 
-template <int D, bool W>
+template <int D, bool W, bool M>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -816,19 +826,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       // P first (needs only S), while the dP MMA may still be running
       const bool tr = lane == 0 && quad == 0;
       if (tr) ATTN_TR(2 + wg, 0, j);
+      const int k0 = (kt0 + j) * kBN;
+      // additive mask: this row's 64 values loaded before the wait for S
+      const bool addm = M && qin;
+      uint4 mreg[M ? 8 : 1];
+      if constexpr (M) {
+        if (addm)
+          load_bias_row<64>(mreg, d.addm + b * d.addm_sb + (int64_t)q * d.addm_sq, k0 + 64 * wg,
+                            d.Skv);
+      }
       if (!(ok = mbar_wait_warp(&s_full[j & 1], (uint32_t)(j >> 1) & 1u, ctl))) break;
       if (tr) ATTN_TR(2 + wg, 1, j);
       tc_fence_after();
       uint32_t rs[64];
       const uint32_t tS = tmem + lane_base + T_S + 128 * (j & 1) + 64 * wg;
       tmem_ld32x2(tS, tS + 32, rs);
-      const int k0 = (kt0 + j) * kBN;
       // masked scores to -inf (their exponential is 0) in a pass of its own, so that
       // the exponential loop of full tiles carries no per-element select
       if constexpr (W) {
-        if (d.addm != nullptr && q < d.Sq)
-          add_bias_row<64>(rs, d.addm + b * d.addm_sb + (int64_t)q * d.addm_sq, k0 + 64 * wg,
-                           d.Skv, inv_scale);
+        if constexpr (M) {
+          if (addm) apply_bias_row<64>(rs, mreg, inv_scale);
+        }
         if (!in_range(full_k, k0)) {
           int clo, chi;
           col_range(g, q, k0 + 64 * wg, &clo, &chi);
@@ -1067,7 +1085,7 @@ __global__ void __launch_bounds__(256) ttt_diag_bwd_kernel(const BwdArgs a) {
   }
 }
 
-template <int D, bool W>
+template <int D, bool W, bool M>
 cudaError_t launch_bwd_dw(const BwdArgs& a, const Maps& m, unsigned passes, cudaStream_t s) {
   cudaError_t e;
   if (passes & 1u) {
@@ -1087,7 +1105,7 @@ cudaError_t launch_bwd_dw(const BwdArgs& a, const Maps& m, unsigned passes, cuda
   }
   if (passes & 2u) {
     using L = DkdvLayout<D>;
-    auto kern = bwd_dkdv_kernel<D, W>;
+    auto kern = bwd_dkdv_kernel<D, W, M>;
     static const cudaError_t regs_ok = check_launch_regs(reinterpret_cast<const void*>(kern));
     if (regs_ok != cudaSuccess) return regs_ok;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC)) !=
@@ -1099,7 +1117,7 @@ cudaError_t launch_bwd_dw(const BwdArgs& a, const Maps& m, unsigned passes, cuda
   }
   if (passes & 4u) {
     using L = DqLayout<D>;
-    auto kern = bwd_dq_kernel<D, W>;
+    auto kern = bwd_dq_kernel<D, W, M>;
     static const cudaError_t regs_ok = check_launch_regs(reinterpret_cast<const void*>(kern));
     if (regs_ok != cudaSuccess) return regs_ok;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC)) !=
@@ -1128,8 +1146,9 @@ cudaError_t launch_bwd_dw(const BwdArgs& a, const Maps& m, unsigned passes, cuda
 
 template <int D>
 cudaError_t launch_bwd_d(const BwdArgs& a, const Maps& m, unsigned passes, cudaStream_t s) {
-  return needs_general_mask(a.d) ? launch_bwd_dw<D, true>(a, m, passes, s)
-                                 : launch_bwd_dw<D, false>(a, m, passes, s);
+  if (a.d.addm != nullptr) return launch_bwd_dw<D, true, true>(a, m, passes, s);
+  return needs_general_mask(a.d) ? launch_bwd_dw<D, true, false>(a, m, passes, s)
+                                 : launch_bwd_dw<D, false, false>(a, m, passes, s);
 }
 
 }  // namespace

@@ -13,8 +13,8 @@
 //   warps 4-7  softmax for query tile 1
 //   warp  8    TMA producer: Q0, Q1 once, then K_j, V_j into a slot ring
 //   warp  9    tcgen05 issuer (one thread) and TMEM owner
-// Tensor memory (512 columns x 128 lanes of 32 bit):
-//   [0,128) S0 / P0   [128,256) S1 / P1   [256,256+D) O0   [256+D,256+2D) O1
+// Tensor memory (512 columns x 128 lanes of 32 bit), D = 128:
+//   [0,128) S0 / P0   [128,256) S1 / P1   [256,384) O0   [384,512) O1
 // P (bf16, two per column) overwrites the first 64 columns of its S tile and
 // is the A operand of O += P V straight from tensor memory.
 //
@@ -22,6 +22,21 @@
 // overlaps the other tile's MMAs):  PV0(j-1), S0(j), PV1(j-1), S1(j).
 // Because tcgen05 MMAs of one thread run in issue order, S_x(j) completing
 // implies PV_x(j-1) completed, which makes the O rescale wait free.
+//
+// D <= 64 leaves room for a third S buffer, used by the general masks
+// (window, key lengths, additive): [0,384) three S / P buffers,
+// [384,384+D) O0, [384+D,384+2D) O1.  Score tile n = 2j + x (tile x, key
+// tile j) lives in buffer n % 3, and the issue order becomes
+//     PV0(j), S1(j+1), PV1(j), S0(j+2)
+// so each score tile is computed a full step before its softmax needs it,
+// instead of after the previous P of the same query tile.  The O rescale
+// then waits for PV_x(j-1) explicitly (rarely: only when the max grows).
+// s_full and p_ready are per buffer: a buffer is refilled only after its P
+// was consumed, so neither barrier can run two phases ahead of a waiter.
+// o_done: S_x(j) completing implies only PV_x(j-2); the rescale wait for
+// PV_x(j-1) at step j is unambiguous (PV_x(j-2) done, PV_x(j) not yet
+// issued), but at the end of the row two o_done phases may be open, so the
+// epilogue waits for o_last, committed once after the last PV_x.
 //
 // The running max is refreshed only when it grows by more than 8 (log2
 // units); otherwise the stale max is kept and P stays <= 256.  O, l and m
@@ -104,8 +119,9 @@ struct FwdLayout {
   static constexpr int Q_OFF = 0;
   static constexpr int KV_OFF = 2 * TG::TILE_BYTES;
   static constexpr int BAR_OFF = KV_OFF + NSLOT * TG::TILE_BYTES;
-  // q_full, kv_full[NSLOT], kv_empty[NSLOT], s_full[2], p_ready[2], o_done[2], drain
-  static constexpr int NBAR = 1 + 2 * NSLOT + 7;
+  // q_full, kv_full[NSLOT], kv_empty[NSLOT], s_full[3], p_ready[3], o_done[2], o_last[2],
+  // drain
+  static constexpr int NBAR = 1 + 2 * NSLOT + 11;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int BYTES = MISC_OFF + 16;
   // at least 116 KB so that only one CTA fits per SM: each holds all 512 TMEM columns
@@ -129,15 +145,23 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 
 __device__ __forceinline__ float neg_inf() { return -INFINITY; }
 
-// W: the mask has a lower key bound (window) or per-batch key lengths; the
-// other masks take the one-sided form of the tile arithmetic.
-template <int D, bool W>
+// W: the mask has a lower key bound (window), per-batch key lengths or an
+// additive mask; the other masks take the one-sided form of the tile
+// arithmetic.  M (implies W): an additive mask is present (its own
+// instantiation, so that the registers holding the mask row cost the other
+// general masks nothing).
+template <int D, bool W, bool M>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
   using TG = TileGeom<D>;
   using L = FwdLayout<D>;
   constexpr int NSLOT = L::NSLOT;
+  // three rotating S buffers: for the general masks at D <= 64, whose rows
+  // are short or partly masked; on long full rows the tensor pipe is the
+  // bound and the two-buffer order measures faster
+  constexpr bool TB = W && D <= 64;
+  constexpr uint32_t O_COL = TB ? 384u : 256u;   // first O accumulator column
   extern __shared__ uint8_t smem_raw[];
 
   if (*reinterpret_cast<volatile uint32_t*>(a.ctl.err) != 0) return;  // sticky device error
@@ -147,10 +171,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = kv_full + NSLOT;
-  uint64_t* s_full = kv_empty + NSLOT;
-  uint64_t* p_ready = s_full + 2;
-  uint64_t* o_done = p_ready + 2;
-  uint64_t* drain = o_done + 2;
+  uint64_t* s_full = kv_empty + NSLOT;  // [3]: per tile x (D = 128) or per buffer (D <= 64)
+  uint64_t* p_ready = s_full + 3;       // [3], indexed like s_full
+  uint64_t* o_done = p_ready + 3;       // [2]: per query tile, one phase per PV
+  uint64_t* o_last = o_done + 2;        // [2]: per query tile, after its last PV (D <= 64)
+  uint64_t* drain = o_last + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
 
@@ -185,10 +210,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int x = 0; x < 2; ++x) {
+    for (int x = 0; x < 3; ++x) {
       mbar_init(&s_full[x], 1);
       mbar_init(&p_ready[x], 128);
+    }
+    for (int x = 0; x < 2; ++x) {
       mbar_init(&o_done[x], 1);
+      mbar_init(&o_last[x], 1);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -252,28 +280,80 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const uint64_t dV0 = TG::mnmajor_base(smem_u32(smem + L::KV_OFF));
       auto slot_of = [](int idx) { return idx % NSLOT; };
       auto phase_of = [](int idx) { return (uint32_t)(idx / NSLOT) & 1u; };
-      auto issue_s = [&](int x, int slot) {
+      // S of query tile x into S buffer `buf`; O_x += P V with P in buffer `buf`
+      auto issue_s = [&](int x, int slot, int buf) {
         const uint64_t qd = dQ0 + TG::bytes(x * TG::TILE_BYTES);
         const uint64_t kd = dK0 + TG::bytes(slot * TG::TILE_BYTES);
 #pragma unroll
         for (int kk = 0; kk < TG::KSTEPS; ++kk)
-          umma_ss(tmem + x * 128, qd + TG::kmajor_step(kk), kd + TG::kmajor_step(kk), idesc_s,
+          umma_ss(tmem + buf * 128, qd + TG::kmajor_step(kk), kd + TG::kmajor_step(kk), idesc_s,
                   kk > 0);
       };
-      auto issue_pv = [&](int x, int slot, bool acc) {
+      auto issue_pv = [&](int x, int slot, bool acc, int buf) {
         const uint64_t vd = dV0 + TG::bytes(slot * TG::TILE_BYTES);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          umma_ts(tmem + 256 + x * D, tmem + x * 128 + kk * 8, vd + TG::mnmajor_step(kk), idesc_o,
-                  (acc || kk > 0) ? 1u : 0u);
+          umma_ts(tmem + O_COL + x * D, tmem + buf * 128 + kk * 8, vd + TG::mnmajor_step(kk),
+                  idesc_o, (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(q_full, 0, ctl);
       if (ok) ok = mbar_wait(&kv_full[slot_of(0)], phase_of(0), ctl);
+      if constexpr (TB) {
+        // score tile n = 2j + x in buffer n % 3; p_ready / s_full per buffer,
+        // phase n / 3
+        auto bar_par = [](int n) { return (uint32_t)(n / 3) & 1u; };
+        if (ok) {
+          tc_fence_after();
+          issue_s(0, slot_of(0), 0);
+          umma_commit(&s_full[0]);
+          issue_s(1, slot_of(0), 1);
+          umma_commit(&s_full[1]);
+          umma_commit(&kv_empty[slot_of(0)]);
+          if (n_kv > 1 && (ok = mbar_wait(&kv_full[slot_of(2)], phase_of(2), ctl))) {
+            tc_fence_after();
+            issue_s(0, slot_of(2), 2);  // S0(1)
+            umma_commit(&s_full[2]);
+          }
+        }
+        for (int j = 0; ok && j < n_kv; ++j) {
+          const int vi = 2 * j + 1, n0 = 2 * j, n1 = 2 * j + 1;
+          ATTN_TR(1, 0, j);
+          if (!(ok = mbar_wait(&kv_full[slot_of(vi)], phase_of(vi), ctl))) break;
+          ATTN_TR(1, 1, j);
+          if (!(ok = mbar_wait(&p_ready[n0 % 3], bar_par(n0), ctl))) break;
+          ATTN_TR(1, 2, j);
+          tc_fence_after();
+          issue_pv(0, slot_of(vi), j > 0, n0 % 3);
+          umma_commit(&o_done[0]);
+          if (j + 1 == n_kv) umma_commit(&o_last[0]);
+          if (j + 1 < n_kv) {  // S1(j+1) takes the buffer P0(j) just left
+            const int ki = 2 * (j + 1), n = n0 + 3;
+            issue_s(1, slot_of(ki), n % 3);
+            umma_commit(&s_full[n % 3]);
+            umma_commit(&kv_empty[slot_of(ki)]);
+          }
+          ATTN_TR(1, 3, j);
+          if (!(ok = mbar_wait(&p_ready[n1 % 3], bar_par(n1), ctl))) break;
+          ATTN_TR(1, 4, j);
+          tc_fence_after();
+          issue_pv(1, slot_of(vi), j > 0, n1 % 3);
+          umma_commit(&o_done[1]);
+          if (j + 1 == n_kv) umma_commit(&o_last[1]);
+          umma_commit(&kv_empty[slot_of(vi)]);
+          if (j + 2 < n_kv) {  // S0(j+2) takes the buffer P1(j) just left
+            const int ki = 2 * (j + 2), n = n1 + 3;
+            if (!(ok = mbar_wait(&kv_full[slot_of(ki)], phase_of(ki), ctl))) break;
+            tc_fence_after();
+            issue_s(0, slot_of(ki), n % 3);
+            umma_commit(&s_full[n % 3]);
+          }
+        }
+      } else {
       if (ok) {
         tc_fence_after();
-        issue_s(0, slot_of(0));
+        issue_s(0, slot_of(0), 0);
         umma_commit(&s_full[0]);
-        issue_s(1, slot_of(0));
+        issue_s(1, slot_of(0), 1);
         umma_commit(&s_full[1]);
         umma_commit(&kv_empty[slot_of(0)]);
       }
@@ -287,18 +367,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (!ok) break;
         ATTN_TR(1, 2, j);
         tc_fence_after();
-        issue_pv(0, slot_of(vi), j - 1 > 0);
+        issue_pv(0, slot_of(vi), j - 1 > 0, 0);
         umma_commit(&o_done[0]);
-        issue_s(0, slot_of(ki));
+        issue_s(0, slot_of(ki), 0);
         umma_commit(&s_full[0]);
         ATTN_TR(1, 3, j);
         if (!(ok = mbar_wait(&p_ready[1], (uint32_t)(j - 1) & 1u, ctl))) break;
         ATTN_TR(1, 4, j);
         tc_fence_after();
-        issue_pv(1, slot_of(vi), j - 1 > 0);
+        issue_pv(1, slot_of(vi), j - 1 > 0, 1);
         umma_commit(&o_done[1]);
         umma_commit(&kv_empty[slot_of(vi)]);
-        issue_s(1, slot_of(ki));
+        issue_s(1, slot_of(ki), 1);
         umma_commit(&s_full[1]);
         umma_commit(&kv_empty[slot_of(ki)]);
       }
@@ -308,17 +388,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
              mbar_wait(&p_ready[0], (uint32_t)(n_kv - 1) & 1u, ctl);
         if (ok) {
           tc_fence_after();
-          issue_pv(0, slot_of(vi), n_kv - 1 > 0);
+          issue_pv(0, slot_of(vi), n_kv - 1 > 0, 0);
           umma_commit(&o_done[0]);
           ok = mbar_wait(&p_ready[1], (uint32_t)(n_kv - 1) & 1u, ctl);
         }
         if (ok) {
           tc_fence_after();
-          issue_pv(1, slot_of(vi), n_kv - 1 > 0);
+          issue_pv(1, slot_of(vi), n_kv - 1 > 0, 1);
           umma_commit(&o_done[1]);
           umma_commit(&kv_empty[slot_of(vi)]);
         }
       }
+      }  // TB
       if (!ok) {
         // every MMA issued so far must finish before tensor memory is freed
         umma_commit(drain);
@@ -335,8 +416,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int qt0 = q0 + x * kBM;
     const int q = qt0 + r;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    const uint32_t tS = tmem + lane_base + x * 128;
-    const uint32_t tO = tmem + lane_base + 256 + x * D;
+    const uint32_t tO = tmem + lane_base + O_COL + x * D;
     const float sl2 = d.scale_log2;
 
     const FullRange full_k = full_keys_for_rows(g, qt0);  // key tiles without masking (W)
@@ -347,18 +427,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const bool tr = lane == 0 && quad == 0;
     for (int j = 0; j < n_kv; ++j) {
       if (tr) ATTN_TR(2 + x, 0, j);
-      if (!(ok = mbar_wait_warp(&s_full[x], (uint32_t)j & 1u, ctl))) break;
+      // score tile n = 2j + x: buffer n % 3, barrier phase n / 3 (D <= 64);
+      // buffer and barrier x, phase j (D = 128)
+      const int n = 2 * j + x;
+      const int sb = TB ? n % 3 : x;
+      const uint32_t spar = TB ? (uint32_t)(n / 3) & 1u : (uint32_t)j & 1u;
+      const uint32_t tS = tmem + lane_base + sb * 128;
+      const int k0 = (kt0 + j) * kBN;
+      if (!(ok = mbar_wait_warp(&s_full[sb], spar, ctl))) break;
       if (tr) ATTN_TR(2 + x, 1, j);
       tc_fence_after();
       uint32_t sr[128];  // S row as raw fp32 bits; columns k0 .. k0+127
       tmem_ld32x2(tS + 0, tS + 32, *reinterpret_cast<uint32_t(*)[64]>(&sr[0]));
       tmem_ld32x2(tS + 64, tS + 96, *reinterpret_cast<uint32_t(*)[64]>(&sr[64]));
 
-      const int k0 = (kt0 + j) * kBN;
       if constexpr (W) {
-        if (d.addm != nullptr && q < d.Sq)
-          add_bias_row<128>(sr, d.addm + b * d.addm_sb + (int64_t)q * d.addm_sq, k0, d.Skv,
-                            inv_scale);
+        if constexpr (M) {
+          if (q < d.Sq)
+            add_bias_row<128>(sr, d.addm + b * d.addm_sb + (int64_t)q * d.addm_sq, k0, d.Skv,
+                              inv_scale);
+        }
         if (!in_range(full_k, k0)) {
           int clo, chi;
           col_range(g, q, k0, &clo, &chi);
@@ -415,9 +503,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       l_run += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
       if (tr) ATTN_TR(2 + x, 3, j);
       if (j > 0) {
-        // O holds PV(j-1): the commit that signalled S(j) tracks every MMA issued
-        // before it, PV(j-1) included, so O can be rescaled without a wait
+        // O must hold PV(j-1) before it is rescaled.  D = 128: the commit that
+        // signalled S(j) tracks every MMA issued before it, PV(j-1) included, so
+        // no wait.  D <= 64: S(j) was issued before PV(j-1); wait for it
         if (__any_sync(0xffffffffu, need)) {
+          if constexpr (TB) {
+            if (!(ok = mbar_wait_warp(&o_done[x], (uint32_t)(j - 1) & 1u, ctl))) break;
+          }
           tc_fence_after();
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 16) {
@@ -431,12 +523,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&p_ready[x]);
+      mbar_arrive(&p_ready[sb]);
       if (tr) ATTN_TR(2 + x, 4, j);
     }
 
     // ------------------------------------------------------------ epilogue
-    if (ok && n_kv > 0) ok = mbar_wait_warp(&o_done[x], (uint32_t)(n_kv - 1) & 1u, ctl);
+    // O_x is final once PV_x(n_kv - 1) has completed.  At D = 128 the last S_x
+    // implies PV_x(n_kv - 2), so the o_done phase of the last PV is unambiguous;
+    // with three S buffers two phases may still be open, hence o_last.
+    if (ok && n_kv > 0)
+      ok = TB ? mbar_wait_warp(&o_last[x], 0u, ctl)
+              : mbar_wait_warp(&o_done[x], (uint32_t)(n_kv - 1) & 1u, ctl);
     if (ok) {
       if (n_kv > 0) tc_fence_after();
       const bool qin = q < d.Sq;
@@ -530,10 +627,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D, bool W>
+template <int D, bool W, bool M>
 cudaError_t launch_fwd_dw(const FwdArgs& a, const Maps& m, cudaStream_t s) {
   using L = FwdLayout<D>;
-  auto kern = fwd_kernel<D, W>;
+  auto kern = fwd_kernel<D, W, M>;
   static const cudaError_t regs_ok = check_launch_regs(reinterpret_cast<const void*>(kern));
   if (regs_ok != cudaSuccess) return regs_ok;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
@@ -552,8 +649,9 @@ cudaError_t launch_fwd_dw(const FwdArgs& a, const Maps& m, cudaStream_t s) {
 
 template <int D>
 cudaError_t launch_fwd_d(const FwdArgs& a, const Maps& m, cudaStream_t s) {
-  return needs_general_mask(a.d) ? launch_fwd_dw<D, true>(a, m, s)
-                                 : launch_fwd_dw<D, false>(a, m, s);
+  if (a.d.addm != nullptr) return launch_fwd_dw<D, true, true>(a, m, s);
+  return needs_general_mask(a.d) ? launch_fwd_dw<D, true, false>(a, m, s)
+                                 : launch_fwd_dw<D, false, false>(a, m, s);
 }
 
 }  // namespace

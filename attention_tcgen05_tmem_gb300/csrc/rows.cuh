@@ -49,6 +49,46 @@ __device__ __forceinline__ void add_bias_row(uint32_t* s, const uint16_t* row, i
   }
 }
 
+// The same in two halves, for loads issued well before the scores arrive:
+// load_bias_row fetches M[col0 .. col0 + N) of a row into registers (16-byte
+// loads; zeros past ncols), apply_bias_row adds them as add_bias_row does.
+template <int N>
+__device__ __forceinline__ void load_bias_row(uint4* m, const uint16_t* row, int col0, int ncols) {
+  const uint16_t* r = row + col0;
+  if (col0 + N <= ncols) {
+#pragma unroll
+    for (int c = 0; c < N / 8; ++c) m[c] = *reinterpret_cast<const uint4*>(r + 8 * c);
+  } else {
+#pragma unroll
+    for (int c = 0; c < N / 8; ++c) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int k = 8 * c + 2 * e;
+        const uint32_t lo = col0 + k < ncols ? r[k] : 0u;
+        const uint32_t hi = col0 + k + 1 < ncols ? r[k + 1] : 0u;
+        w[e] = lo | (hi << 16);
+      }
+      m[c] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void apply_bias_row(uint32_t* s, const uint4* m, float inv_scale) {
+#pragma unroll
+  for (int c = 0; c < N / 8; ++c) {
+    const uint32_t w[4] = {m[c].x, m[c].y, m[c].z, m[c].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      s[8 * c + 2 * e] = __float_as_uint(
+          fmaf(bf16_bits(w[e] & 0xffffu), inv_scale, __uint_as_float(s[8 * c + 2 * e])));
+      s[8 * c + 2 * e + 1] = __float_as_uint(
+          fmaf(bf16_bits(w[e] >> 16), inv_scale, __uint_as_float(s[8 * c + 2 * e + 1])));
+    }
+  }
+}
+
 // Dot product of two bf16 rows of length D (fp32 accumulate, fixed order).
 template <int D>
 __device__ __forceinline__ float dot_rows(const __nv_bfloat16* x, const __nv_bfloat16* y) {

@@ -127,6 +127,34 @@ def test_general_mask_backward_is_bitwise_deterministic(w):
         assert torch.equal(a, b)
 
 
+STRESS_CASES = [W("stress_d64_full", 2, 8, 8, 2048, 2048, 64, "full", seed=6),
+                W("stress_d64_addmask", 2, 8, 8, 2048, 2048, 64, "full", seed=6, add=True),
+                W("stress_d32_window", 2, 8, 4, 2048, 2048, 32, "window", seed=6,
+                  window=(300, 300))]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("w", STRESS_CASES, ids=[c.name for c in STRESS_CASES])
+def test_forward_repeated_runs_are_bitwise_equal(w):
+    """Many CTAs, many key tiles, several runs: a forward that read its O
+    accumulator before the last P V products landed (a pipeline ordering bug)
+    would show up as outputs that differ between runs."""
+    dev = device()
+    x = synth.make_inputs(w)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    am = None
+    if "add_mask" in x:
+        pad = -w.Skv % 8
+        am = torch.zeros(w.Sq, w.Skv + pad, dtype=torch.bfloat16, device=dev)[:, :w.Skv]
+        am.copy_(x["add_mask"].to(dev))
+    kw = dict(window=w.window, add_mask=am)
+    o0, lse0 = binding.fwd(q, k, v, w.mask, out="fp32", **kw)
+    for _ in range(5):
+        o, lse = binding.fwd(q, k, v, w.mask, out="fp32", **kw)
+        assert torch.equal(o, o0) and torch.equal(lse, lse0)
+    binding.device_status()
+
+
 @pytest.mark.gpu
 def test_backward_is_bitwise_deterministic():
     dev = device()
