@@ -156,8 +156,10 @@ struct attn_host_session_s {
   cudaEvent_t start = nullptr, stat = nullptr, end_in = nullptr, end_out = nullptr;
   cudaEvent_t step_done[2] = {};  // compute of the last step that used static area i
   cudaEvent_t qkv[2] = {}, inp[2] = {}, fwd[2] = {}, dq[2] = {}, bwd[2] = {}, outd[2] = {};
-  int64_t chunk = 0;  // chunks enqueued so far (slot = chunk % 2)
-  int64_t step = 0;   // steps enqueued so far (static area = step % 2)
+  int64_t chunk = 0;    // chunks enqueued so far (slot = chunk % 2)
+  int64_t step = 0;     // steps enqueued so far (static area = step % 2)
+  bool failed = false;  // a step stopped part-way: the slot bookkeeping no longer
+                        // matches what was enqueued, so no further step is accepted
 
   cudaError_t create() {
     cudaError_t e;
@@ -383,9 +385,15 @@ attn_status attn_train_host_session_create(const attn_problem* p, int kv_heads_p
 attn_status attn_train_host_session_step(attn_host_session s, const attn_host_io* io,
                                          void* stream) {
   if (s == nullptr) return err(ATTN_ERR_INVALID, "session is NULL");
+  if (s->failed)
+    return err(ATTN_ERR_INVALID,
+               "an earlier step of this session failed part-way; join, synchronize and "
+               "destroy it, then create a new session");
   attn_status st = check_io(io);
   if (st != ATTN_OK) return st;
-  return s->enqueue_step(io, static_cast<cudaStream_t>(stream));
+  st = s->enqueue_step(io, static_cast<cudaStream_t>(stream));
+  if (st != ATTN_OK) s->failed = true;
+  return st;
 }
 
 attn_status attn_train_host_session_join(attn_host_session s, void* stream) {

@@ -285,7 +285,10 @@ attn_status attn_train_step_host(const attn_problem* p, const attn_host_io* io,
 attn_status attn_train_host_session_create(const attn_problem* p, int kv_heads_per_chunk,
                                            void* arena, size_t arena_bytes,
                                            attn_host_session* out);
-/* Enqueues one step (copy-in, forward, backward, copy-out). */
+/* Enqueues one step (copy-in, forward, backward, copy-out).  Arguments are
+ * checked before anything is enqueued; a failure after that (a CUDA error)
+ * leaves the session unusable: later steps return ATTN_ERR_INVALID, and the
+ * caller joins, synchronizes and destroys it. */
 attn_status attn_train_host_session_step(attn_host_session s, const attn_host_io* io,
                                          void* stream);
 /* Makes `stream` wait for every copy the session has enqueued so far. */
