@@ -12,6 +12,12 @@ import torch
 
 ATOL = 2e-2
 REL_L2 = 1e-2
+# Inputs outside the workloads' distribution (scores up to +-30, an explicit
+# large scale, 32 heads summed into one dK) give gradients 5-8x larger than the
+# workloads'.  The kernels' error is relative -- P and dS are bf16 MMA operands
+# (unit roundoff 2^-9), accumulation is fp32 -- so on such tensors the absolute
+# bar grows with the tensor's magnitude: ATOL + STRESS_REL * max|ref|.
+STRESS_REL = 2.0 ** -6
 LSE_ATOL = 1e-3
 BF16_HALF_ULP = 2.0 ** -8
 
@@ -26,11 +32,13 @@ def round_allowance(t):
     return BF16_HALF_ULP if (hasattr(t, "dtype") and t.dtype == torch.bfloat16) else 0.0
 
 
-def compare(name, got, ref, atol=ATOL, rel_l2=REL_L2, round_rel=None):
+def compare(name, got, ref, atol=ATOL, rel_l2=REL_L2, round_rel=None, stress=False):
     if round_rel is None:
         round_rel = round_allowance(got)
     g = got.detach().double().cpu().numpy() if hasattr(got, "detach") else np.asarray(got)
     r = np.asarray(ref, dtype=np.float64)
+    if stress and r.size:
+        atol = atol + STRESS_REL * float(np.abs(r).max())
     assert g.shape == r.shape, (name, g.shape, r.shape)
     assert np.all(np.isfinite(g)), f"{name}: non-finite output"
     diff = np.abs(g - r)

@@ -12,7 +12,7 @@ from attention_tcgen05_tmem_gb300 import binding, synth
 from tests.gpu_util import LSE_ATOL, compare, device
 
 
-def run_both(w: synth.Workload, check_bwd=True, out="fp32"):
+def run_both(w: synth.Workload, check_bwd=True, out="fp32", stress=False):
     dev = device()
     x = synth.make_inputs(w)
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
@@ -28,7 +28,7 @@ def run_both(w: synth.Workload, check_bwd=True, out="fp32"):
     o, lse = binding.fwd(q, k, v, w.mask, w.ttt_step, out=out, **kw)
     binding.device_status()
     ro, rl = oracle.fwd(x["q"], x["k"], x["v"], w.mask, w.ttt_step, **rkw)
-    compare("O", o, ro)
+    compare("O", o, ro, stress=stress)
     compare("LSE", lse, rl, atol=LSE_ATOL, rel_l2=1e-3)
     if not check_bwd:
         return
@@ -36,9 +36,9 @@ def run_both(w: synth.Workload, check_bwd=True, out="fp32"):
     binding.device_status()
     rdq, rdk, rdv = oracle.bwd(x["q"], x["k"], x["v"], x["dout"], w.mask, w.ttt_step, **rkw)
     assert np.abs(rdq).max() > 1e-3  # non-vacuous (HOT-Step trap 7)
-    compare("dQ", dq, rdq)
-    compare("dK", dk, rdk)
-    compare("dV", dv, rdv)
+    compare("dQ", dq, rdq, stress=stress)
+    compare("dK", dk, rdk, stress=stress)
+    compare("dV", dv, rdv, stress=stress)
 
 
 def W(name, B, Hq, Hkv, Sq, Skv, D, mask, t=0, seed=11, window=None, lens=None, add=False):
@@ -84,6 +84,9 @@ CASES = [
     W("addmask_window_d32", 1, 2, 2, 400, 400, 32, "window", window=(64, 64), add=True),
     W("addmask_varlen_d128", 2, 2, 2, 256, 256, 128, "causal", lens=(256, 100), add=True),
     W("addmask_d16", 1, 2, 2, 384, 384, 16, "full", add=True),
+    # degenerate extents: one query row, TTT at D = 16
+    W("sq1_full_cross_d64", 2, 2, 1, 1, 257, 64, "full"),
+    W("ttt_t1_d16", 1, 2, 2, 130, 260, 16, "ttt", 1),
 ]
 
 
@@ -188,6 +191,81 @@ def test_strided_bshd_layout():
     compare("dQ", dq, rdq)
     compare("dK", dk, rdk)
     compare("dV", dv, rdv)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("out", ["fp32", "bf16"])
+def test_gqa_32_heads_per_kv_head(out):
+    """32 query heads summed into each dK / dV row (gradients ~5x the workloads')."""
+    run_both(W("gqa32_causal_d64", 1, 32, 1, 200, 200, 64, "causal"), out=out, stress=True)
+
+
+@pytest.mark.gpu
+def test_single_key():
+    """Skv = 1: every row's only key has weight 1, so O = V and LSE = c q.k; then
+    dP = dO.v = Delta, so dS and dQ are 0 and dK = 0, dV = sum of dO."""
+    dev = device()
+    w = W("skv1", 1, 2, 2, 129, 1, 128, "full", seed=14)
+    x = synth.make_inputs(w)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
+    o, lse = binding.fwd(q, k, v, "full", out="fp32")
+    dq, dk, dv = binding.bwd(q, k, v, o, lse, do, "full")
+    binding.device_status()
+    ro, rl = oracle.fwd(x["q"], x["k"], x["v"], "full")
+    rdq, rdk, rdv = oracle.bwd(x["q"], x["k"], x["v"], x["dout"], "full")
+    compare("O", o, ro)
+    compare("LSE", lse, rl, atol=LSE_ATOL, rel_l2=1e-3)
+    assert torch.equal(o.cpu(), x["v"].float().expand(1, 2, 129, 128))
+    assert float(dq.abs().max()) < 1e-4 and float(dk.abs().max()) < 1e-3
+    compare("dV", dv, rdv)
+
+
+@pytest.mark.gpu
+def test_explicit_scale():
+    """A caller-chosen softmax scale (not 1/sqrt(D)) reaches every pass."""
+    dev = device()
+    w = W("scale", 1, 4, 2, 300, 300, 128, "causal", seed=12)
+    x = synth.make_inputs(w)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
+    o, lse = binding.fwd(q, k, v, "causal", scale=0.3, out="fp32")
+    dq, dk, dv = binding.bwd(q, k, v, o, lse, do, "causal", scale=0.3)
+    binding.device_status()
+    ro, rl = oracle.fwd(x["q"], x["k"], x["v"], "causal", scale=0.3)
+    rdq, rdk, rdv = oracle.bwd(x["q"], x["k"], x["v"], x["dout"], "causal", scale=0.3)
+    compare("O", o, ro, stress=True)
+    compare("LSE", lse, rl, atol=LSE_ATOL, rel_l2=1e-3)
+    compare("dQ", dq, rdq, stress=True)
+    compare("dK", dk, rdk, stress=True)
+    compare("dV", dv, rdv, stress=True)
+
+
+RESCALE_CASES = [W("rescale_window_d64", 1, 2, 2, 1024, 1024, 64, "window", seed=13,
+                   window=(700, 100)),
+                 W("rescale_full_d128", 1, 2, 1, 512, 1024, 128, "full", seed=13),
+                 W("rescale_causal_d32", 1, 2, 2, 768, 768, 32, "causal", seed=13)]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("w", RESCALE_CASES, ids=[c.name for c in RESCALE_CASES])
+def test_growing_scores_rescale_often(w):
+    """Key norms that grow along the key axis (x 1 .. x 6) make each row's score
+    maximum rise tile after tile, so the forward's lazy O rescale (and, at D <= 64
+    with a general mask, its wait for the previous P V) runs on most tiles."""
+    dev = device()
+    x = synth.make_inputs(w)
+    grow = torch.linspace(1.0, 6.0, w.Skv).view(1, 1, w.Skv, 1)
+    x["k"] = (x["k"].float() * grow).to(torch.bfloat16)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
+    o, lse = binding.fwd(q, k, v, w.mask, window=w.window, out="fp32")
+    dq, dk, dv = binding.bwd(q, k, v, o, lse, do, w.mask, window=w.window)
+    binding.device_status()
+    ro, rl = oracle.fwd(x["q"], x["k"], x["v"], w.mask, window=w.window)
+    rdq, rdk, rdv = oracle.bwd(x["q"], x["k"], x["v"], x["dout"], w.mask, window=w.window)
+    compare("O", o, ro, stress=True)
+    compare("LSE", lse, rl, atol=LSE_ATOL, rel_l2=1e-3)
+    compare("dQ", dq, rdq, stress=True)
+    compare("dK", dk, rdk, stress=True)
+    compare("dV", dv, rdv, stress=True)
 
 
 @pytest.mark.gpu
