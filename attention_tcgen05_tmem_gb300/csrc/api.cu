@@ -115,6 +115,10 @@ attn_status check_problem(const attn_problem* p) {
                 p->B, p->Hq, p->Hkv, p->Sq, p->Skv, p->D);
   if (p->Hq % p->Hkv != 0)
     return fail(ATTN_ERR_INVALID, "Hq (%d) must be a multiple of Hkv (%d)", p->Hq, p->Hkv);
+  // the mask arithmetic takes 2^30 as an unbounded extent
+  if (p->Sq >= (1 << 30) || p->Skv >= (1 << 30))
+    return fail(ATTN_ERR_UNSUPPORTED, "sequence lengths must be below 2^30 (Sq=%d Skv=%d)",
+                p->Sq, p->Skv);
   if (p->D != 16 && p->D != 32 && p->D != 64 && p->D != 128)
     return fail(ATTN_ERR_UNSUPPORTED, "head dim %d unsupported (16, 32, 64, 128)", p->D);
   if (p->mask != ATTN_MASK_FULL && p->mask != ATTN_MASK_CAUSAL && p->mask != ATTN_MASK_TTT &&
@@ -148,10 +152,21 @@ attn_status check_problem(const attn_problem* p) {
   if (!std::isfinite(p->scale)) return fail(ATTN_ERR_INVALID, "scale is not finite");
   if (p->out_dtype != ATTN_OUT_BF16 && p->out_dtype != ATTN_OUT_F32)
     return fail(ATTN_ERR_UNSUPPORTED, "unknown out_dtype %d", p->out_dtype);
+  // launch limits: tile grids, the row-wise passes (at least 16 rows per block
+  // for the Delta prep, 8 key rows for the TTT suffix pass) and the additive
+  // mask's transpose (grid y = query columns / 64, z = batch entries)
   const int64_t grid_q = (int64_t)((p->Sq + 127) / 128) * p->B * p->Hq;
   const int64_t grid_k = (int64_t)((p->Skv + 127) / 128) * p->B * p->Hkv;
-  if (grid_q > 0x7fffffffLL || grid_k > 0x7fffffffLL)
+  const int64_t rows = (int64_t)p->B * p->Hq * p->Sq;
+  const int64_t suffix_rows = (int64_t)p->B * p->Hkv * p->Sq;
+  if (grid_q > 0x7fffffffLL || grid_k > 0x7fffffffLL || rows / 16 >= 0x7fffffffLL ||
+      suffix_rows / 8 >= 0x7fffffffLL)
     return fail(ATTN_ERR_UNSUPPORTED, "problem too large for one launch");
+  if (p->add_mask != nullptr && ((int64_t)p->Sq + 7) / 8 * 8 > 64LL * 65535)
+    return fail(ATTN_ERR_UNSUPPORTED, "additive mask with Sq = %d above %lld", p->Sq,
+                64LL * 65535 - 7);
+  if (p->add_mask != nullptr && p->add_mask_sb != 0 && p->B > 65535)
+    return fail(ATTN_ERR_UNSUPPORTED, "per-batch additive mask with B = %d above 65535", p->B);
   return ATTN_OK;
 }
 

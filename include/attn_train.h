@@ -135,7 +135,10 @@ typedef struct {
  * Requires B, Hq, Hkv, Sq, Skv > 0, Hq % Hkv == 0, D in {16, 32, 64, 128},
  * a known mask, ttt_step >= 0 and Skv == (ttt_step + 1) * Sq for TTT,
  * window extents >= 0 for ATTN_MASK_WINDOW (0 otherwise), and a 4-byte
- * aligned seq_lengths pointer. */
+ * aligned seq_lengths pointer.  Size limits (ATTN_ERR_UNSUPPORTED beyond):
+ * Sq, Skv < 2^30; every launch's grid within CUDA's limits (128-row tiles
+ * and B*Hq*Sq / 16 row blocks below 2^31); with an additive mask
+ * round8(Sq) <= 64 * 65535 and, for a per-batch mask, B <= 65535. */
 attn_status attn_train_supports(const attn_problem* p);
 
 /* Bytes of device workspace attn_train_bwd needs: the fp32 Delta row

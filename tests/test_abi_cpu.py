@@ -140,6 +140,24 @@ def test_step_host_arena_size(lib):
             == 2 * (_up(2 * 4) + _up((99 * 104 + 100) * 2)) + mask_ws)
 
 
+def test_size_limits(lib):
+    # the mask arithmetic's unbounded extent is 2^30: longer sequences are refused
+    p = binding.problem(1, 1, 1, 1 << 30, 128, 16, "full")
+    assert lib.attn_train_supports(ctypes.byref(p)) == 2
+    assert b"2^30" in lib.attn_train_last_error()
+    p = binding.problem(1, 1, 1, 128, (1 << 30) + 5, 16, "full")
+    assert lib.attn_train_supports(ctypes.byref(p)) == 2
+    # the additive mask's transpose grid bounds Sq
+    p = binding.problem(1, 1, 1, 5_000_000, 128, 64, "full")
+    p.add_mask, p.add_mask_sb, p.add_mask_sq = 0x10000, 0, 128
+    assert lib.attn_train_supports(ctypes.byref(p)) == 2
+    p.add_mask = None
+    assert lib.attn_train_supports(ctypes.byref(p)) == 0
+    # row-wise passes: B*Hq*Sq rows at 16 per block must fit one launch
+    p = binding.problem(65536, 64, 64, 1 << 20, 128, 16, "full")
+    assert lib.attn_train_supports(ctypes.byref(p)) == 2
+
+
 def test_step_host_validation(lib):
     p = binding.problem(1, 4, 2, 128, 128, 64, "causal", host=True)
     need = binding.step_host_arena_size(p, 0)
