@@ -157,7 +157,9 @@ def cpu_sample(ws, target_s: float, inputs=None):
     workload's first (or only) shape: the q heads of the first kv-head
     groups (at least as many q heads as host threads) and the last R query
     rows (those with the most visible keys), R grown until the run takes
-    about target_s seconds.  Returns (TFLOP/s, description, threads)."""
+    about target_s seconds.  Returns (TFLOP/s, description, threads, per pass)
+    with per pass = {"fwd": TFLOP/s, "bwd": TFLOP/s} (4 D and 10 D FLOP per
+    visible pair)."""
     import oracle
     from attention_tcgen05_tmem_gb300 import flops, synth
 
@@ -182,21 +184,23 @@ def cpu_sample(ws, target_s: float, inputs=None):
         r0 = w.Sq - R
         t0 = time.perf_counter()
         oracle.fwd(q, k, v, w.mask, t, rows=(r0, w.Sq), **kw)
+        t1 = time.perf_counter()
         oracle.bwd(q, k, v, do, w.mask, t, rows=(r0, w.Sq), **kw)
-        dt = time.perf_counter() - t0
-        return dt, 14.0 * w.D * hq * pairs(r0)
+        t2 = time.perf_counter()
+        return t2 - t0, 14.0 * w.D * hq * pairs(r0), t1 - t0, t2 - t1
 
     R = min(w.Sq, 8)
-    dt, f = run(R)
+    dt, f, dtf, dtb = run(R)
     for _ in range(3):
         if dt >= 0.5 * target_s or R >= w.Sq:
             break
         R = int(min(w.Sq, max(2 * R, R * target_s / max(dt, 1e-3))))
-        dt, f = run(R)
+        dt, f, dtf, dtb = run(R)
     desc = (f"fp64 oracle fwd+bwd on {w.name}: {w.B} batch x {hq} of {w.Hq} q heads "
             f"({groups} kv-head groups), last {R} of {w.Sq} query rows, {f / 1e9:.1f} GFLOP "
             f"mask-aware, {dt:.1f} s")
-    return f / dt / 1e12, desc, threads
+    per_pass = {"fwd": f * 4 / 14 / max(dtf, 1e-9) / 1e12, "bwd": f * 10 / 14 / max(dtb, 1e-9) / 1e12}
+    return f / dt / 1e12, desc, threads, per_pass
 
 
 # --------------------------------------------------------------- GPU arm
@@ -641,13 +645,15 @@ def main():
         for name in names:
             ws = table[name]
             F = sum(flops.flops_fwd_bwd(w) for w in ws)
-            per, desc, threads = [], "", 1
+            per, per_f, per_b, desc, threads = [], [], [], "", 1
             from attention_tcgen05_tmem_gb300 import synth
             x = synth.make_inputs(ws[-1])
             for i in range(args.warmup + args.steps):
-                tf, desc, threads = cpu_sample(ws, 4.0, x)
+                tf, desc, threads, pp = cpu_sample(ws, 4.0, x)
                 if i >= args.warmup:
                     per.append(tf)
+                    per_f.append(pp["fwd"])
+                    per_b.append(pp["bwd"])
             value = statistics.median(per)
             line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
                     "n_gpus": n_gpus, "steps": args.steps, "warmup": args.warmup,
@@ -655,7 +661,9 @@ def main():
                     "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                     "config": describe(name, ws, args.out, n_gpus),
                     "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads,
-                                     "kind": "oracle", "sample": desc},
+                                     "kind": "oracle", "sample": desc,
+                                     "fwd_value": statistics.median(per_f),
+                                     "bwd_value": statistics.median(per_b)},
                     "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                             "d2h_bytes_per_step": 0}}
             print(json.dumps(line), flush=True)
@@ -718,9 +726,9 @@ def main():
             line["e2e"] = {"value": job_value(F, K, r["e2e_ms"], n_gpus), "unit": UNIT,
                            "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]}
         if rank == 0 and n_gpus == 1 and not args.no_cpu_baseline:
-            tf, desc, threads = cpu_sample(ws, args.cpu_seconds)
+            tf, desc, threads, pp = cpu_sample(ws, args.cpu_seconds)
             line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": threads, "kind": "oracle",
-                                    "sample": desc}
+                                    "sample": desc, "fwd_value": pp["fwd"], "bwd_value": pp["bwd"]}
         if rank == 0:
             print(json.dumps(line), flush=True)
     if dist:
