@@ -106,3 +106,34 @@ def test_loss_full_size_sampled():
     _close("grad", logits.reshape(N, w.V)[torch.from_numpy(rows).to(dev)].cpu(), ref_grad)
     mean = (x["mask"].reshape(-1).double() * row_loss.cpu().double()).sum().item() / N
     assert abs(loss.item() - mean) <= 1e-6 * abs(mean)
+
+
+@pytest.mark.gpu
+def test_loss_extreme_logits():
+    """Logits of magnitude ~250 (exp of them overflows fp32 without the running
+    max) and one-hot targets: the forward's online max / sum and the backward's
+    exp(x - lse) stay finite and match the oracle."""
+    dev = device()
+    w = synth.LossWorkload("loss_extreme", 1, 64, 5000)
+    x = synth.make_loss_inputs(w)
+    x["logits"] = x["logits"] * 100.0
+    hot = torch.zeros_like(x["target"])
+    idx = torch.arange(w.T) * 37 % w.V
+    hot[0, torch.arange(w.T), idx] = 1.0
+    x["target"] = hot
+    logits = x["logits"].to(dev).contiguous()
+    target, mask = x["target"].to(dev), x["mask"].to(dev)
+    loss, row_loss, row_lse, row_tsum = binding.logsoftmax_loss(logits, target, mask)
+    binding.logsoftmax_loss_bwd_raw(logits, target, mask.reshape(-1), row_lse, row_tsum)
+    torch.cuda.synchronize()
+    assert torch.isfinite(logits).all() and torch.isfinite(row_loss).all()
+    ref_loss, ref_row, ref_lse = sl.forward(x["logits"], x["target"], x["mask"])
+    ref_grad = sl.backward(x["logits"], x["target"], x["mask"])
+    # exp(x - lse) with |x|, |lse| ~ 900 in fp32: lse (and x log2(e)) carry an absolute
+    # error of about one fp32 ulp of |x| (2^-24 |x| ~ 5e-5), which exp turns into the
+    # same relative error of the gradient; the bar adds four such ulps
+    rtol = RTOL + 4 * 2.0 ** -24 * float(x["logits"].abs().max())
+    _close("loss", [loss.item()], [ref_loss])
+    _close("row_lse", row_lse.cpu(), ref_lse)
+    _close("row_loss", row_loss.cpu(), ref_row, rtol)
+    _close("grad", logits.cpu(), ref_grad, rtol)
