@@ -269,6 +269,69 @@ def test_growing_scores_rescale_often(w):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("D", [64, 128])
+def test_additive_mask_hides_whole_rows_and_keys(D):
+    """A per-batch additive mask that hides entire query rows (O = 0, LSE = 0,
+    dQ = 0 exactly: the rows see no key) and entire keys (dK = dV = 0 exactly),
+    over several tiles and a ragged tail."""
+    dev = device()
+    B, H, Sq, Skv = 2, 2, 300, 270
+    w = W("hide", B, H, H, Sq, Skv, D, "full", seed=15)
+    x = synth.make_inputs(w)
+    g = torch.Generator().manual_seed(15)
+    m = (0.5 * torch.randn(B, Sq, Skv, generator=g)).to(torch.bfloat16)
+    hidden_rows = {0: [0, 129, 299], 1: [7, 200]}
+    hidden_keys = {0: [5, 128, 269], 1: [0, 131]}
+    for b_, rows in hidden_rows.items():
+        m[b_, rows, :] = float("-inf")
+    for b_, keys in hidden_keys.items():
+        m[b_, :, keys] = float("-inf")
+    pad = -Skv % 8
+    am = torch.zeros(B, Sq, Skv + pad, dtype=torch.bfloat16, device=dev)[:, :, :Skv]
+    am.copy_(m.to(dev))
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
+    o, lse = binding.fwd(q, k, v, "full", out="fp32", add_mask=am)
+    dq, dk, dv = binding.bwd(q, k, v, o, lse, do, "full", add_mask=am)
+    binding.device_status()
+    ro, rl = oracle.fwd(x["q"], x["k"], x["v"], "full", add_mask=m)
+    rdq, rdk, rdv = oracle.bwd(x["q"], x["k"], x["v"], x["dout"], "full", add_mask=m)
+    compare("O", o, ro)
+    compare("LSE", lse, rl, atol=LSE_ATOL, rel_l2=1e-3)
+    compare("dQ", dq, rdq)
+    compare("dK", dk, rdk)
+    compare("dV", dv, rdv)
+    for b_, rows in hidden_rows.items():
+        assert torch.all(o[b_, :, rows] == 0) and torch.all(lse[b_, :, rows] == 0)
+        assert torch.all(dq[b_, :, rows] == 0)
+    for b_, keys in hidden_keys.items():
+        assert torch.all(dk[b_, :, keys] == 0) and torch.all(dv[b_, :, keys] == 0)
+
+
+@pytest.mark.gpu
+def test_scores_in_the_thousands():
+    """q and k scaled by 20: scores reach about 2000, each row's weights are close
+    to one-hot and the running max jumps by far more than the rescale threshold."""
+    dev = device()
+    w = W("huge", 1, 4, 2, 384, 384, 128, "causal", seed=16)
+    x = synth.make_inputs(w)
+    x["q"] = (x["q"].float() * 20).to(torch.bfloat16)
+    x["k"] = (x["k"].float() * 20).to(torch.bfloat16)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
+    o, lse = binding.fwd(q, k, v, "causal", out="fp32")
+    dq, dk, dv = binding.bwd(q, k, v, o, lse, do, "causal")
+    binding.device_status()
+    ro, rl = oracle.fwd(x["q"], x["k"], x["v"], "causal")
+    rdq, rdk, rdv = oracle.bwd(x["q"], x["k"], x["v"], x["dout"], "causal")
+    assert float(np.abs(rl).max()) > 1000  # the scores really are large
+    compare("O", o, ro, stress=True)
+    # |LSE| up to ~2100: fp32 keeps it to ~2^-24 |LSE| ~ 1.3e-4, inside the 1e-3 bar
+    compare("LSE", lse, rl, atol=LSE_ATOL, rel_l2=1e-3)
+    compare("dQ", dq, rdq, stress=True)
+    compare("dK", dk, rdk, stress=True)
+    compare("dV", dv, rdv, stress=True)
+
+
+@pytest.mark.gpu
 def test_zero_keys_give_uniform_weights():
     # K = 0: every visible key has the same weight; O = mean of visible V rows
     dev = device()
