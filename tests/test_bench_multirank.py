@@ -51,3 +51,18 @@ def test_max_over_ranks_and_job_value_gloo_world2():
 
 def test_single_rank_needs_no_process_group():
     assert bench.max_over_ranks([3.0, 4.0], None) == [3.0, 4.0]
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    """Under torchrun with N > 1 the reference arm (the CPU oracle) runs and prints on
+    rank 0 only; every other rank exits 0 at once, without output or work."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, WORLD_SIZE="2", RANK="1", LOCAL_RANK="1",
+               MASTER_ADDR="127.0.0.1", MASTER_PORT="29555")
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--gpus", "2", "--steps", "1", "--warmup", "3"],
+                       env=env, cwd=root, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == ""
