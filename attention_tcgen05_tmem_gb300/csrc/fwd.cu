@@ -13,8 +13,9 @@
 //   warps 4-7  softmax for query tile 1
 //   warp  8    TMA producer: Q0, Q1 once, then K_j, V_j into a slot ring
 //   warp  9    tcgen05 issuer (one thread) and TMEM owner
-// Tensor memory (512 columns x 128 lanes of 32 bit), D = 128:
-//   [0,128) S0 / P0   [128,256) S1 / P1   [256,384) O0   [384,512) O1
+// Tensor memory (512 columns x 128 lanes of 32 bit), two S buffers:
+//   [0,128) S0 / P0   [128,256) S1 / P1   [256,256+D) O0   [256+D,256+2D) O1
+// (all 512 columns at D = 128)
 // P (bf16, two per column) overwrites the first 64 columns of its S tile and
 // is the A operand of O += P V straight from tensor memory.
 //
