@@ -19,7 +19,8 @@
 //             then adds the TTT suffix-diagonal terms and writes c dQ once.
 //   4. TTT:   the keys of appended segments (one diagonal each) get
 //             dV = sum_g p dO and dK = c sum_g dS q, summed over the group's
-//             q heads in ascending order, from a per-row warp pass.
+//             q heads in ascending order; one warp per key row r serves the
+//             key i*Sq + r of every segment i, reading each q and dO row once.
 //
 // Tensor-core kernels use 10 warps: 0-7 elementwise (two warpgroups split the
 // 128 columns of each S / dP tile; thread = TMEM lane = row), 8 TMA producer,
