@@ -140,6 +140,26 @@ def test_step_host_arena_size(lib):
             == 2 * (_up(2 * 4) + _up((99 * 104 + 100) * 2)) + mask_ws)
 
 
+def test_plain_c_client(lib, tmp_path):
+    """The header is plain C: a C99 program includes it, links the library and
+    calls the host-side entry points (validation, sizes, error messages)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    here = os.path.dirname(os.path.abspath(__file__))
+    root = os.path.dirname(here)
+    libdir = os.path.dirname(binding.LIB_PATH)
+    exe = str(tmp_path / "c_abi_client")
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(root, "include"),
+                    os.path.join(here, "c_abi_client.c"), "-o", exe, "-L", libdir,
+                    "-lattn_train", "-Wl,-rpath," + libdir], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    assert "c abi ok" in r.stdout
+
+
 def test_size_limits(lib):
     # the mask arithmetic's unbounded extent is 2^30: longer sequences are refused
     p = binding.problem(1, 1, 1, 1 << 30, 128, 16, "full")
