@@ -372,3 +372,31 @@ def test_inputs_are_seeded_and_bf16():
         assert torch.equal(a[key], b[key])
     assert not torch.equal(a["q"], a["k"][:, :, : w.Sq])
     assert a["q"].shape == (1, 2, 128, 64)
+
+
+@pytest.mark.parametrize("mask,t,Sq,Skv", [("causal", 0, 40, 40), ("full", 0, 33, 50),
+                                            ("ttt", 2, 20, 60)])
+def test_row_restricted_oracle(mask, t, Sq, Skv):
+    """rows=(r0, r1) restricts the oracle to those query rows: the forward's rows
+    equal the full forward's; the backward's dQ rows equal the full dQ's, and its
+    dK/dV equal the full backward with dO zeroed outside the rows (a zero dO row
+    has dP = 0 and Delta = 0, so its dS and its dV terms vanish)."""
+    g = np.random.default_rng(17)
+    q = g.standard_normal((1, 4, Sq, 16))
+    k = g.standard_normal((1, 2, Skv, 16))
+    v = g.standard_normal((1, 2, Skv, 16))
+    do = g.standard_normal((1, 4, Sq, 16))
+    r0, r1 = Sq // 3, Sq - 2
+    o, lse = oracle.fwd(q, k, v, mask, t)
+    o_r, lse_r = oracle.fwd(q, k, v, mask, t, rows=(r0, r1))
+    np.testing.assert_array_equal(o_r[:, :, r0:r1], o[:, :, r0:r1])
+    np.testing.assert_array_equal(lse_r[:, :, r0:r1], lse[:, :, r0:r1])
+    assert not o_r[:, :, :r0].any() and not o_r[:, :, r1:].any()
+    dq, _, _ = oracle.bwd(q, k, v, do, mask, t)
+    dq_r, dk_r, dv_r = oracle.bwd(q, k, v, do, mask, t, rows=(r0, r1))
+    np.testing.assert_allclose(dq_r[:, :, r0:r1], dq[:, :, r0:r1], rtol=0, atol=1e-13)
+    do_band = np.zeros_like(do)
+    do_band[:, :, r0:r1] = do[:, :, r0:r1]
+    _, dk_b, dv_b = oracle.bwd(q, k, v, do_band, mask, t)
+    np.testing.assert_allclose(dk_r, dk_b, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dv_r, dv_b, rtol=0, atol=1e-13)
