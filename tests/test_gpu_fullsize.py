@@ -50,7 +50,7 @@ def test_long_causal_gqa_full_size():
 
 @pytest.mark.gpu
 @pytest.mark.timeout(1800)
-@pytest.mark.parametrize("t", [1, 6])
+@pytest.mark.parametrize("t", [1, 3, 6])
 def test_eagle3_ttt_full_size(t):
     run_sampled(synth.TTT_STEPS[t], groups=(0,))
 
