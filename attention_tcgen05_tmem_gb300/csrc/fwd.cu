@@ -439,8 +439,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (tr) ATTN_TR(2 + x, 1, j);
       tc_fence_after();
       uint32_t sr[128];  // S row as raw fp32 bits; columns k0 .. k0+127
-      tmem_ld32x2(tS + 0, tS + 32, *reinterpret_cast<uint32_t(*)[64]>(&sr[0]));
-      tmem_ld32x2(tS + 64, tS + 96, *reinterpret_cast<uint32_t(*)[64]>(&sr[64]));
+      tmem_ld64x2(tS + 0, tS + 64, sr);
 
       if constexpr (W) {
         if constexpr (M) {
