@@ -466,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tr) ATTN_TR(2 + wg, 1, it);
       tc_fence_after();
       uint32_t raw[64];
-      tmem_ld32x2(tS, tS + 32, raw);
+      if constexpr (D <= 64) tmem_ld64(tS, raw); else tmem_ld32x2(tS, tS + 32, raw);
       // key row kv sees query columns [clo, chi] of the tile; rows past Sq have
       // -lse2 = -inf.  Masked scores go to -inf (exponential 0) in a pass of its own,
       // so that the exponential loop of full tiles carries no per-element select.
@@ -510,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = mbar_wait_warp(dp_full, (uint32_t)it & 1u, ctl))) break;
       if (tr) ATTN_TR(2 + wg, 3, it);
       tc_fence_after();
-      tmem_ld32x2(tdP, tdP + 32, raw);
+      if constexpr (D <= 64) tmem_ld64(tdP, raw); else tmem_ld32x2(tdP, tdP + 32, raw);
       // dS = P (dP - Delta); packed pairs measure faster except at D = 128, where
       // they cost registers the kernel does not have to spare
 #pragma unroll

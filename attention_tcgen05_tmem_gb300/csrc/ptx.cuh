@@ -222,10 +222,20 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, uint32_t (
       : "r"(ta), "r"(tb)
       : "memory");
 }
+// One x64 load and its wait: a 64-column row in one instruction (dK/dV at
+// D <= 64, measured 1-2% faster there than an x32 pair; dQ and D = 128 dK/dV
+// measured faster with x32 pairs).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : ATTN_R8(0), ATTN_R8(8), ATTN_R8(16), ATTN_R8(24), ATTN_R8(32), ATTN_R8(40), ATTN_R8(48), ATTN_R8(56)
+      : "r"(taddr)
+      : "memory");
+}
 // Two x64 loads back to back, one wait: a 128-column row in two instructions
 // (the forward's score rows; measured 2-4% faster there than four x32 loads
-// with two waits, while the backward's 64-column rows keep x32 pairs, which
-// measured faster for them).
+// with two waits).
 __device__ __forceinline__ void tmem_ld64x2(uint32_t ta, uint32_t tb, uint32_t (&r)[128]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%128];\n\t"
