@@ -152,14 +152,14 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------- CPU oracle
-def cpu_sample(ws, target_s: float, inputs=None):
+def cpu_sample(ws, target_s: float, inputs=None, rows=None):
     """Time the fp64 oracle (forward + backward) on a bounded sample of the
     workload's first (or only) shape: the q heads of the first kv-head
     groups (at least as many q heads as host threads) and the last R query
     rows (those with the most visible keys), R grown until the run takes
     about target_s seconds.  Returns (TFLOP/s, description, threads, per pass)
-    with per pass = {"fwd": TFLOP/s, "bwd": TFLOP/s} (4 D and 10 D FLOP per
-    visible pair)."""
+    with per pass = {"fwd": TFLOP/s, "bwd": TFLOP/s, "rows": R} (4 D and 10 D
+    FLOP per visible pair).  rows=R skips the search and runs R rows once."""
     import oracle
     from attention_tcgen05_tmem_gb300 import flops, synth
 
@@ -189,18 +189,27 @@ def cpu_sample(ws, target_s: float, inputs=None):
         t2 = time.perf_counter()
         return t2 - t0, 14.0 * w.D * hq * pairs(r0), t1 - t0, t2 - t1
 
-    R = min(w.Sq, 8)
-    dt, f, dtf, dtb = run(R)
-    for _ in range(3):
-        if dt >= 0.5 * target_s or R >= w.Sq:
-            break
-        R = int(min(w.Sq, max(2 * R, R * target_s / max(dt, 1e-3))))
+    if rows is not None:
+        R = min(w.Sq, int(rows))
         dt, f, dtf, dtb = run(R)
+    else:
+        R = min(w.Sq, 8)
+        dt, f, dtf, dtb = run(R)
+        for _ in range(3):
+            if dt >= 0.5 * target_s or R >= w.Sq:
+                break
+            R = int(min(w.Sq, max(2 * R, R * target_s / max(dt, 1e-3))))
+            dt, f, dtf, dtb = run(R)
     desc = (f"fp64 oracle fwd+bwd on {w.name}: {w.B} batch x {hq} of {w.Hq} q heads "
             f"({groups} kv-head groups), last {R} of {w.Sq} query rows, {f / 1e9:.1f} GFLOP "
             f"mask-aware, {dt:.1f} s")
-    per_pass = {"fwd": f * 4 / 14 / max(dtf, 1e-9) / 1e12, "bwd": f * 10 / 14 / max(dtb, 1e-9) / 1e12}
+    per_pass = {"fwd": f * 4 / 14 / max(dtf, 1e-9) / 1e12, "bwd": f * 10 / 14 / max(dtb, 1e-9) / 1e12,
+                "rows": R}
     return f / dt / 1e12, desc, threads, per_pass
+
+
+# Seconds the reference arm (the CPU oracle) aims to spend over all its steps.
+REF_BUDGET_S = 150.0
 
 
 # --------------------------------------------------------------- GPU arm
@@ -477,25 +486,26 @@ def loss_bytes(w):
     return n * V * 4 * 2 + n * (4 + 12) + n * V * 4 * 3 + n * (4 + 8)
 
 
-def loss_cpu_sample(w, x, target_s):
-    """The fp64 oracle on the first R rows (R grown to about target_s s);
-    returns (GB/s of the same algorithmic bytes per row, description)."""
+def loss_cpu_sample(w, x, target_s, rows=None):
+    """The fp64 oracle on the first R rows (R grown to about target_s s, or
+    rows=R fixed); returns (GB/s of the same algorithmic bytes per row,
+    description, R)."""
     from oracle import softmax_loss as sl
     N, V = w.rows, w.V
     lg = x["logits"].reshape(N, V)
     tg = x["target"].reshape(N, V)
     mk = x["mask"].reshape(N)
-    R = 8
+    R = 8 if rows is None else min(N, int(rows))
     while True:
         t0 = time.perf_counter()
         sl.forward(lg[:R], tg[:R], mk[:R])
         sl.backward(lg[:R], tg[:R], mk[:R])
         dt = time.perf_counter() - t0
-        if dt >= 0.5 * target_s or R >= N:
+        if rows is not None or dt >= 0.5 * target_s or R >= N:
             break
         R = int(min(N, max(2 * R, R * target_s / max(dt, 1e-3))))
     gbs = loss_bytes(w) * R / N / dt / 1e9
-    return gbs, f"fp64 oracle fwd+bwd on the first {R} of {N} rows of {w.name}, {dt:.1f} s"
+    return gbs, f"fp64 oracle fwd+bwd on the first {R} of {N} rows of {w.name}, {dt:.1f} s", R
 
 
 def run_loss(args, w, rank, local_rank, dist, n_gpus, peaks, peak_src):
@@ -597,7 +607,7 @@ def run_loss(args, w, rank, local_rank, dist, n_gpus, peaks, peak_src):
                        "h2d_bytes_per_step": sum(t.numel() * 4 for t in pin.values()),
                        "d2h_bytes_per_step": out_grad.numel() * 4 + 4}
     if rank == 0 and n_gpus == 1 and not args.no_cpu_baseline:
-        gbs, desc = loss_cpu_sample(w, x, args.cpu_seconds)
+        gbs, desc, _ = loss_cpu_sample(w, x, args.cpu_seconds)
         line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
                                 "sample": desc}
     if rank == 0:
@@ -622,13 +632,18 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return 0
+        # the whole reference run stays near REF_BUDGET_S seconds: each step times the
+        # oracle on a sample sized once per workload (calibrated outside the steps)
+        n_lines = max(1, len(loss_names) + len(names))
+        step_s = max(0.2, min(4.0, REF_BUDGET_S / n_lines / (args.warmup + args.steps)))
         for name in loss_names:
             from attention_tcgen05_tmem_gb300 import synth
             w = losses[name]
             x = synth.make_loss_inputs(w)
             per, desc = [], ""
+            _, _, R = loss_cpu_sample(w, x, step_s)
             for i in range(args.warmup + args.steps):
-                gbs, desc = loss_cpu_sample(w, x, 2.0)
+                gbs, desc, _ = loss_cpu_sample(w, x, step_s, rows=R)
                 if i >= args.warmup:
                     per.append(gbs)
             value = statistics.median(per)
@@ -648,8 +663,9 @@ def main():
             per, per_f, per_b, desc, threads = [], [], [], "", 1
             from attention_tcgen05_tmem_gb300 import synth
             x = synth.make_inputs(ws[-1])
+            R = cpu_sample(ws, step_s, x)[3]["rows"]
             for i in range(args.warmup + args.steps):
-                tf, desc, threads, pp = cpu_sample(ws, 4.0, x)
+                tf, desc, threads, pp = cpu_sample(ws, step_s, x, rows=R)
                 if i >= args.warmup:
                     per.append(tf)
                     per_f.append(pp["fwd"])
