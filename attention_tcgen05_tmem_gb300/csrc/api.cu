@@ -2,8 +2,8 @@
 // maps, workspace carving, launch sequencing and error reporting.  Validation
 // runs entirely on the host before anything is enqueued; an unsupported or
 // malformed call returns a status and never falls back to another path
-// (HOT-Step flash-attn-training, section 2: a silent fallback is
-// indistinguishable from a pass, so unsupported shapes must fail hard).
+// (HOT-Step flash-attn-training, section 2: a silent fallback cannot be told
+// apart from a working kernel, so unsupported shapes must fail hard).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>

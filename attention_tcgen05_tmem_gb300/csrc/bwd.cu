@@ -2,9 +2,9 @@
 //
 // The backward recomputes the weights from the saved LSE (CS336 README,
 // "Flash Attention (Triton)": P is recomputed from L) and never stores the
-// S x S score matrix.  It is atomic-free with fixed schedules, so results are
-// bitwise reproducible (HOT-Step flash-attn-training, section 1: "no fp
-// atomics, fixed schedules"):
+// S x S score matrix.  It uses no atomics and a fixed schedule, so results are
+// bitwise reproducible (HOT-Step flash-attn-training, section 1, asks the same
+// of its backward: no floating-point atomics, a fixed order of accumulation):
 //
 //   1. prep:  Delta[q] = sum_d dO[q,d] O[q,d]               (fp32, from bf16)
 //   2. dK/dV: one CTA per (b, kv head, 128-key tile) owns its dK and dV rows.

@@ -15,7 +15,7 @@ __device__ __forceinline__ const __nv_bfloat16* row_ptr(const View& v, int b, in
   return reinterpret_cast<const __nv_bfloat16*>(v.ptr) + b * v.sb + h * v.sh + s * v.ss;
 }
 
-// Additive mask (HOT-Step section 3: any additive [S_kv, S] mask).  The raw
+// Additive mask (HOT-Step section 3: an arbitrary additive [S_kv, S] mask).  The raw
 // scores s enter the exponent as s * scale * log2(e), so M is folded in as
 // s + M / scale (M = -inf gives -inf).
 __device__ __forceinline__ float bf16_bits(uint32_t h) { return __uint_as_float(h << 16); }

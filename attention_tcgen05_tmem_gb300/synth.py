@@ -95,8 +95,8 @@ VARLEN_GQA = Workload("varlen_causal_gqa_B4_Hq32_Hkv4_S8192_D128", 4, 32, 4, 819
 VARLEN_TTT = Workload("varlen_eagle3_ttt_step2_B2_Hq32_Hkv8_S8192_D128", 2, 32, 8, 8192, 3 * 8192,
                       128, "ttt", 2, 6, seq_lengths=(8192, 5000))
 
-# Full self-attention with an additive bias table (HOT-Step section 3: the ops
-# take any additive mask; the DiT trainer passes its masks that way).
+# Full self-attention with an additive bias table (HOT-Step section 3: its ops
+# accept an arbitrary additive mask, the form in which its DiT trainer passes masks).
 DIT_ADDMASK = Workload("dit_addmask_self_B2_H16_S4096_D64", 2, 16, 16, 4096, 4096, 64, "full", 0,
                        4, add_mask=True)
 

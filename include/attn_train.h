@@ -29,14 +29,14 @@
  *                     appended segment) plus key i*Sq + q of each appended
  *                     segment i = 1..t (one diagonal entry each).
  *   ATTN_MASK_WINDOW  the band q - window_left <= kv <= q + window_right (the
- *                     HOT-Step page's windowed self-attention, section 4);
+ *                     HOT-Step page's self-attention over a window, section 4);
  *                     (w, 0) is a causal sliding window, (w, w) a symmetric one.
  * Per-batch key lengths (the padding terms of the eagle3 mask_mod): with
  * seq_lengths set, keys kv >= seq_lengths[b] of batch entry b are invisible
  * (for TTT: segment-0 keys kv >= seq_lengths[b], and the suffix diagonals of
  * rows q >= seq_lengths[b]); their dK and dV are 0.
- * Additive mask (HOT-Step section 3: the ops take any additive mask [S_kv, S],
- * or [S_kv, S, 1, B] broadcast): with add_mask set, the scores of the pairs
+ * Additive mask (HOT-Step section 3: its ops accept an arbitrary additive mask
+ * shaped [S_kv, S], or [S_kv, S, 1, B] with broadcast): with add_mask set, the scores of the pairs
  * the mask kind admits become scale * q.k + M[b][q][kv] (M = -inf hides the
  * pair); one M for all heads.  Not with ATTN_MASK_TTT.
  *

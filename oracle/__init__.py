@@ -13,7 +13,7 @@ arrays.  Every function follows the plain definition of attention:
   or(causal_mask, suffix_mask), read with shift_left = t (the number of
   appended TTT segments), Q_LEN = Sq and KV_LEN = (t+1) Sq; its padding terms
   take optional per-batch key lengths ``seq_lengths``.
-* HOT-Step flash-attn-training, section 4 ("windowed self" attention): the
+* HOT-Step flash-attn-training, section 4 (self-attention over a window): the
   window mask, read as the band q - left <= kv <= q + right; section 3: an
   optional additive mask [B or 1, Sq, Skv] added to the scaled scores
   (-inf hides a pair), shared by every head.

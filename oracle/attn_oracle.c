@@ -23,11 +23,11 @@
  * the causal part, kv % Q_LEN < seq_lengths[b] in the suffix part); without
  * lengths every key is inside.  The same key-length bound applies to the
  * full, causal and window masks.  The window mask (the band of the HOT-Step
- * page's "windowed self" attention, section 4, read as q - left <= kv <=
+ * page's self-attention over a window, section 4, read as q - left <= kv <=
  * q + right) takes its two extents from the caller.
  *
- * Additive mask (HOT-Step section 3: the ops take "any additive mask"
- * [S_kv, S], or [S_kv, S, 1, B] broadcast): an optional M[b][q][kv] added to
+ * Additive mask (HOT-Step section 3: its ops accept an arbitrary additive
+ * mask shaped [S_kv, S], or [S_kv, S, 1, B] with broadcast): an optional M[b][q][kv] added to
  * the scaled scores of the pairs the mask kind admits; M = -inf hides the
  * pair.  One M per batch entry (or one for all), shared by every head.
  *

@@ -1,5 +1,6 @@
 """Pins for the oracle's additive mask (HOT-Step flash-attn-training, section
-3: the ops take "any additive mask" [S_kv, S] or [S_kv, S, 1, B] broadcast):
+3: its ops accept an arbitrary additive mask shaped [S_kv, S], or [S_kv, S, 1, B]
+with broadcast):
 torch fp64 sdpa with a float attn_mask and autograd (per-batch and broadcast
 masks, -inf entries, GQA, combined with the causal kind), the closed form of a
 constant bias (softmax unchanged, LSE shifted by the bias), and rows that the

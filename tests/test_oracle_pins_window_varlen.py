@@ -1,6 +1,6 @@
 """Pins for the oracle's window mask and per-batch key lengths.
 
-The window mask is the band of the HOT-Step page's "windowed self" attention
+The window mask is the band of the HOT-Step page's self-attention over a window
 (section 4), read as q - left <= kv <= q + right; the key lengths are the
 padding terms of the SpecForge post's eagle3 mask_mod ("Flex Attention":
 kv < seq_lengths[b] in the causal part, kv % Q_LEN < seq_lengths[b] in the
