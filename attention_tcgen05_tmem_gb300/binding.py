@@ -342,12 +342,14 @@ def bwd(q, k, v, o, lse, dout, mask="causal", ttt_step=0, scale=None, stream=Non
 def mask_pattern(Sq, Skv, mask, ttt_step=0, device="cuda", with_tiles=True, window=None,
                  seq_length=None):
     """Device view of the mask for one batch entry of key length seq_length
-    (None = every key): (bits[2, Sq, Skv] uint8, tiles or None)."""
+    (None = every key): (bits[6, Sq, Skv] uint8, tiles or None); planes 0-2 are
+    the forward, dK/dV and dQ schedules the kernels run for this problem,
+    planes 3-5 the same passes in the general form."""
     import torch
     lens = None if seq_length is None else torch.tensor([seq_length], dtype=torch.int32,
                                                         device=device)
     p = problem(1, 1, 1, Sq, Skv, 64, mask, ttt_step, window=window, seq_lengths=lens)
-    bits = torch.zeros(2, Sq, Skv, dtype=torch.uint8, device=device)
+    bits = torch.zeros(6, Sq, Skv, dtype=torch.uint8, device=device)
     tiles = None
     if with_tiles:
         kv_main = Sq if p.mask == 2 else Skv

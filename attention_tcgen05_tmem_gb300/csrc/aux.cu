@@ -1,7 +1,7 @@
-// aux.cu -- test-only kernels: the device view of the mask (both the row-side
-// schedule used by the forward and dQ passes and the column-side schedule used
-// by the dK/dV pass), a one-tile tcgen05 descriptor probe, and a bounded-wait
-// self-test that times out on purpose (nothing ever arrives on its barrier).
+// aux.cu -- test-only kernels: the device view of the mask (the forward, dK/dV
+// and dQ schedules, through the scheduling calls the kernels make), a one-tile
+// tcgen05 descriptor probe, and a bounded-wait self-test that times out on
+// purpose (nothing ever arrives on its barrier).
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -14,49 +14,22 @@
 namespace attn {
 namespace {
 
-// bits[0][q][kv]: pair visited and unmasked by the row-side schedule
-// bits[1][q][kv]: same for the column-side schedule
-// Both include the TTT suffix diagonals exactly as the kernels address them
+// bits[p][q][kv], six planes of Sq x Skv: planes 0-2 the forward, dK/dV and
+// dQ schedules in the form the kernels run for this problem (one-sided unless
+// needs_general_mask), planes 3-5 the same three in the general form.  Every
+// plane includes the TTT suffix diagonals exactly as the kernels address them
 // (key row i*Sq + q, i = 1..t).  tiles[qt][kt] = tile class of the tiled part.
 // With per-batch key lengths this is the view of batch entry 0.
-__global__ void mask_pattern_kernel(const Dims d, uint8_t* bits, uint8_t* tiles) {
+__global__ void mask_pattern_kernel(const Dims d, bool general, uint8_t* bits, uint8_t* tiles) {
   const MaskGeom g = with_len(d.geom, d.seqlens, 0);
   const int64_t n = (int64_t)d.Sq * d.Skv;
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
        idx += (int64_t)gridDim.x * blockDim.x) {
     const int q = (int)(idx / d.Skv);
     const int kv = (int)(idx % d.Skv);
-    uint8_t row_side = 0, col_side = 0;
-    if (kv < g.kv_main) {
-      const int kt = kv / kBN, k0 = kt * kBN;
-      // row side: the forward pairs query tiles; its key range covers both
-      const int qp0 = (q / (2 * kBM)) * 2 * kBM;
-      const int qt0 = (q / kBM) * kBM;
-      int f0, fn, q0t, qn;
-      kv_tiles_for_rows(g, qp0, 2 * kBM, &f0, &fn);
-      kv_tiles_for_rows(g, qt0, kBM, &q0t, &qn);
-      const bool fwd_visits = kt >= f0 && kt < f0 + fn;
-      const bool dq_visits = kt >= q0t && kt < q0t + qn;
-      int clo, chi;
-      col_range(g, q, k0, &clo, &chi);
-      const bool unmasked = tile_is_full(g, qt0, k0) || (kv - k0 >= clo && kv - k0 <= chi);
-      row_side = (fwd_visits && dq_visits && unmasked) ? 1 : 0;
-      // column side: query tiles of the key tile's query range
-      int qlo, qhi;
-      q_range_for_kv(g, k0, &qlo, &qhi);
-      const bool visits = qhi > qlo && q / kBM >= qlo / kBM && q / kBM < cdiv(qhi, kBM);
-      int rlo, rhi;
-      row_range_for_kv(g, kv, qt0, &rlo, &rhi);
-      const bool keep = tile_is_full(g, qt0, k0) || (q - qt0 >= rlo && q - qt0 <= rhi);
-      col_side = (visits && keep) ? 1 : 0;
-    } else if (g.ttt > 0) {
-      const int64_t rel = (int64_t)kv - q;
-      const bool diag = kv >= d.Sq && rel > 0 && rel % d.Sq == 0 && rel / d.Sq <= g.ttt &&
-                        q < g.kv_len;
-      row_side = col_side = diag ? 1 : 0;
-    }
-    bits[idx] = row_side;
-    bits[n + idx] = col_side;
+    uint8_t vis[6];
+    sched_pattern_pair(g, q, kv, general, vis);
+    for (int p = 0; p < 6; ++p) bits[p * n + idx] = vis[p];
   }
   if (tiles != nullptr) {
     const int nqt = cdiv(d.Sq, kBM), nkt = cdiv(g.kv_main, kBN);
@@ -196,7 +169,7 @@ cudaError_t launch_mask_pattern(const Dims& d, uint8_t* bits, uint8_t* tiles, cu
   int64_t blocks = (n + 255) / 256;
   if (blocks > 4096) blocks = 4096;
   if (blocks < 1) blocks = 1;
-  mask_pattern_kernel<<<(unsigned)blocks, 256, 0, s>>>(d, bits, tiles);
+  mask_pattern_kernel<<<(unsigned)blocks, 256, 0, s>>>(d, needs_general_mask(d), bits, tiles);
   return cudaGetLastError();
 }
 

@@ -257,16 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // this batch entry's geometry; query tiles qt_begin .. qt_begin + n_q - 1 see the key tile
   const MaskGeom g = W ? with_len(d.geom, d.seqlens, b) : d.geom;
   int qt_begin, n_q;
-  if constexpr (W) {
-    int q_lo, q_hi;
-    q_range_for_kv(g, k0, &q_lo, &q_hi);
-    qt_begin = q_lo / kBM;
-    n_q = q_hi > q_lo ? cdiv(q_hi, kBM) - qt_begin : 0;
-  } else {
-    qt_begin = upper_q_begin(g, k0) / kBM;
-    n_q = cdiv(d.Sq, kBM) - qt_begin;
-    if (n_q < 0) n_q = 0;
-  }
+  sched_q_tiles<W>(g, k0, &qt_begin, &n_q);
   const int N = n_q * d.G;
 
   const int warp = warp_id();
@@ -470,22 +461,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // key row kv sees query columns [clo, chi] of the tile; rows past Sq have
       // -lse2 = -inf.  Masked scores go to -inf (exponential 0) in a pass of its own,
       // so that the exponential loop of full tiles carries no per-element select.
-      if constexpr (W) {
-        if constexpr (M) {
-          if (addm) apply_bias_row<64>(raw, mreg, inv_scale);
-        }
-        if (!in_range(full_q, q0)) {
-          int clo, chi;
-          row_range_for_kv(g, kv, q0 + 64 * wg, &clo, &chi);
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (c < clo || c > chi) raw[c] = __float_as_uint(-INFINITY);
-        }
-      } else if (!upper_tile_full(g, q0, k0)) {
-        const int cmin = upper_q_begin(g, kv) - q0 - 64 * wg;
+      if constexpr (M) {
+        if (addm) apply_bias_row<64>(raw, mreg, inv_scale);
+      }
+      if (sched_col_tile_masked<W>(g, full_q, q0, k0)) {
+        int clo, chi;
+        sched_col_rows<W>(g, kv, q0 + 64 * wg, &clo, &chi);
 #pragma unroll
         for (int c = 0; c < 64; ++c)
-          if (c < cmin) raw[c] = __float_as_uint(-INFINITY);
+          if (c < clo || c > chi) raw[c] = __float_as_uint(-INFINITY);
       }
       float p[64];
 #pragma unroll
@@ -649,9 +633,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q0 = qt * kBM;
   // this batch entry's geometry; key tiles kt0 .. kt0 + n_kv - 1
   const MaskGeom g = W ? with_len(d.geom, d.seqlens, b) : d.geom;
-  int kt0 = 0, n_kv;
-  if constexpr (W) kv_tiles_for_rows(g, q0, kBM, &kt0, &n_kv);
-  else n_kv = cdiv(upper_kv_end(g, q0, kBM), kBN);
+  int kt0, n_kv;
+  sched_kv_tiles<W>(g, q0, kBM, &kt0, &n_kv);
 
   const int warp = warp_id();
   const int lane = lane_id();
@@ -844,22 +827,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32x2(tS, tS + 32, rs);
       // masked scores to -inf (their exponential is 0) in a pass of its own, so that
       // the exponential loop of full tiles carries no per-element select
-      if constexpr (W) {
-        if constexpr (M) {
-          if (addm) apply_bias_row<64>(rs, mreg, inv_scale);
-        }
-        if (!in_range(full_k, k0)) {
-          int clo, chi;
-          col_range(g, q, k0 + 64 * wg, &clo, &chi);
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (c < clo || c > chi) rs[c] = __float_as_uint(-INFINITY);
-        }
-      } else if (!upper_tile_full(g, q0, k0)) {
-        const int lim = upper_col_limit(g, q, k0) - 64 * wg;
+      if constexpr (M) {
+        if (addm) apply_bias_row<64>(rs, mreg, inv_scale);
+      }
+      if (sched_row_tile_masked<W>(g, full_k, q0, k0)) {
+        int clo, chi;
+        sched_row_cols<W>(g, q, k0 + 64 * wg, &clo, &chi);
 #pragma unroll
         for (int c = 0; c < 64; ++c)
-          if (c > lim) rs[c] = __float_as_uint(-INFINITY);
+          if (c < clo || c > chi) rs[c] = __float_as_uint(-INFINITY);
       }
       float p[64];
 #pragma unroll

@@ -198,9 +198,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int q0 = qp * 2 * kBM;
   // this batch entry's geometry; key tiles kt0 .. kt0 + n_kv - 1
   const MaskGeom g = W ? with_len(d.geom, d.seqlens, b) : d.geom;
-  int kt0 = 0, n_kv;
-  if constexpr (W) kv_tiles_for_rows(g, q0, 2 * kBM, &kt0, &n_kv);
-  else n_kv = cdiv(upper_kv_end(g, q0, 2 * kBM), kBN);
+  int kt0, n_kv;
+  sched_kv_tiles<W>(g, q0, 2 * kBM, &kt0, &n_kv);
 
   const int warp = warp_id();
   const int lane = lane_id();
@@ -441,24 +440,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       uint32_t sr[128];  // S row as raw fp32 bits; columns k0 .. k0+127
       tmem_ld64x2(tS + 0, tS + 64, sr);
 
-      if constexpr (W) {
-        if constexpr (M) {
-          if (q < d.Sq)
-            add_bias_row<128>(sr, d.addm + b * d.addm_sb + (int64_t)q * d.addm_sq, k0, d.Skv,
-                              inv_scale);
-        }
-        if (!in_range(full_k, k0)) {
-          int clo, chi;
-          col_range(g, q, k0, &clo, &chi);
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c < clo || c > chi) sr[c] = __float_as_uint(neg_inf());
-        }
-      } else if (!upper_tile_full(g, qt0, k0)) {
-        const int lim = upper_col_limit(g, q, k0);
+      if constexpr (M) {
+        if (q < d.Sq)
+          add_bias_row<128>(sr, d.addm + b * d.addm_sb + (int64_t)q * d.addm_sq, k0, d.Skv,
+                            inv_scale);
+      }
+      if (sched_row_tile_masked<W>(g, full_k, qt0, k0)) {
+        int clo, chi;
+        sched_row_cols<W>(g, q, k0, &clo, &chi);
 #pragma unroll
         for (int c = 0; c < 128; ++c)
-          if (c > lim) sr[c] = __float_as_uint(neg_inf());
+          if (c < clo || c > chi) sr[c] = __float_as_uint(neg_inf());
       }
       // row max over 8 independent chains of three-input max (a single chain of
       // 127 dependent max operations is latency-bound)

@@ -173,8 +173,10 @@ __host__ __device__ inline bool in_range(const FullRange& r, int x) { return x >
 // The one-sided forms: masks without a lower key bound (full, causal, TTT) and
 // without per-batch key lengths (kv_len == kv_main).  The kernels are
 // instantiated for this case of their own, so that the general window and
-// length arithmetic costs the common masks nothing; they agree with the
-// general functions above whenever lo is unbounded and kv_len == kv_main.
+// length arithmetic costs the common masks nothing.  Both forms must select
+// exactly the visible pairs; the mask export below evaluates each of them as
+// the kernels do, and the tests compare every plane with the visibility
+// predicate bit for bit.
 __host__ __device__ inline int upper_kv_end(const MaskGeom& g, int q0, int rows) {
   int64_t last_q = (int64_t)q0 + rows - 1;
   if (last_q > g.Sq - 1) last_q = g.Sq - 1;
@@ -197,6 +199,161 @@ __host__ __device__ inline int upper_col_limit(const MaskGeom& g, int q, int k0)
 __host__ __device__ inline int upper_q_begin(const MaskGeom& g, int kv) {
   if (g.kind == kMaskFull) return 0;
   return (int)clamp64((int64_t)kv - g.hi, 0, g.Sq);
+}
+
+// ---- The schedules the attention kernels run ----------------------------
+// Every decision a kernel takes about which tiles to visit and which scores
+// to hide goes through these functions, and so does the test-only export of
+// the mask pattern, so that the export shows exactly what the kernels compute.
+// W selects the general form (window mask, per-batch key lengths, additive
+// mask); without it the one-sided form (full, causal, TTT).
+
+// Key tiles [*kt0, *kt0 + *n) visited by query rows [q0, q0 + rows): the
+// forward (rows = 2 kBM, a query-tile pair) and dQ (rows = kBM).
+template <bool W>
+__host__ __device__ inline void sched_kv_tiles(const MaskGeom& g, int q0, int rows, int* kt0,
+                                               int* n) {
+  if constexpr (W) {
+    kv_tiles_for_rows(g, q0, rows, kt0, n);
+  } else {
+    *kt0 = 0;
+    *n = cdiv(upper_kv_end(g, q0, rows), kBN);
+  }
+}
+
+// Query tiles [*qt0, *qt0 + *n) that the dK/dV pass visits for the key tile at k0.
+template <bool W>
+__host__ __device__ inline void sched_q_tiles(const MaskGeom& g, int k0, int* qt0, int* n) {
+  if constexpr (W) {
+    int lo, hi;
+    q_range_for_kv(g, k0, &lo, &hi);
+    *qt0 = lo / kBM;
+    *n = hi > lo ? cdiv(hi, kBM) - *qt0 : 0;
+  } else {
+    *qt0 = upper_q_begin(g, k0) / kBM;
+    const int m = cdiv(g.Sq, kBM) - *qt0;
+    *n = m < 0 ? 0 : m;
+  }
+}
+
+// Row side (forward, dQ): whether the key tile at k0 needs per-column masking
+// for the query tile at qt0; full_k = full_keys_for_rows(g, qt0) (read by the
+// general form only, so the kernels can keep it in uniform registers).
+template <bool W>
+__host__ __device__ inline bool sched_row_tile_masked(const MaskGeom& g, const FullRange& full_k,
+                                                      int qt0, int k0) {
+  if constexpr (W) return !in_range(full_k, k0);
+  else return !upper_tile_full(g, qt0, k0);
+}
+// Row side, masked tile: columns c of the key block starting at k0 that query
+// q sees are *clo <= c <= *chi.
+template <bool W>
+__host__ __device__ inline void sched_row_cols(const MaskGeom& g, int q, int k0, int* clo,
+                                               int* chi) {
+  if constexpr (W) {
+    col_range(g, q, k0, clo, chi);
+  } else {
+    *clo = 0;
+    *chi = upper_col_limit(g, q, k0);
+  }
+}
+
+// Column side (dK/dV): whether the query tile at q0 needs per-row masking for
+// the key tile at k0; full_q = full_rows_for_keys(g, k0) (general form only).
+template <bool W>
+__host__ __device__ inline bool sched_col_tile_masked(const MaskGeom& g, const FullRange& full_q,
+                                                      int q0, int k0) {
+  if constexpr (W) return !in_range(full_q, q0);
+  else return !upper_tile_full(g, q0, k0);
+}
+// Column side, masked tile: query columns c of the block starting at q0 that
+// key row kv is seen by are *clo <= c <= *chi.
+template <bool W>
+__host__ __device__ inline void sched_col_rows(const MaskGeom& g, int kv, int q0, int* clo,
+                                               int* chi) {
+  if constexpr (W) {
+    row_range_for_kv(g, kv, q0, clo, chi);
+  } else {
+    *clo = upper_q_begin(g, kv) - q0;
+    *chi = kBM;
+  }
+}
+
+// The three schedules at one (q, kv) pair of the tiled part (kv < kv_main),
+// through the same sched_* calls the kernels make (for the test-only mask
+// export): vis[0] the forward (a pair of query tiles,
+// whole 128-column key tiles), vis[1] the dK/dV pass (key tile fixed, 64-row
+// query halves), vis[2] the dQ pass (64-column key halves).
+template <bool W>
+__host__ __device__ inline void sched_pattern_at(const MaskGeom& g, int q, int kv, uint8_t vis[3]) {
+  const int kt = kv / kBN, k0 = kt * kBN;
+  const int qt0 = (q / kBM) * kBM;
+  // forward: the CTA of query tiles [qp0, qp0 + 2 kBM)
+  {
+    const int qp0 = (q / (2 * kBM)) * 2 * kBM;
+    int kt0, n;
+    sched_kv_tiles<W>(g, qp0, 2 * kBM, &kt0, &n);
+    bool keep = kt >= kt0 && kt < kt0 + n;
+    if (keep && sched_row_tile_masked<W>(g, full_keys_for_rows(g, qt0), qt0, k0)) {
+      int clo, chi;
+      sched_row_cols<W>(g, q, k0, &clo, &chi);
+      keep = kv - k0 >= clo && kv - k0 <= chi;
+    }
+    vis[0] = keep ? 1 : 0;
+  }
+  // dK/dV: the CTA of key tile k0; warpgroup wg holds query columns q0 + 64 wg ..
+  {
+    int qtb, n;
+    sched_q_tiles<W>(g, k0, &qtb, &n);
+    bool keep = q / kBM >= qtb && q / kBM < qtb + n;
+    if (keep && sched_col_tile_masked<W>(g, full_rows_for_keys(g, k0), qt0, k0)) {
+      const int wg = (q - qt0) / 64;
+      int clo, chi;
+      sched_col_rows<W>(g, kv, qt0 + 64 * wg, &clo, &chi);
+      const int c = q - qt0 - 64 * wg;
+      keep = c >= clo && c <= chi;
+    }
+    vis[1] = keep ? 1 : 0;
+  }
+  // dQ: the CTA of query tile qt0; warpgroup wg holds key columns k0 + 64 wg ..
+  {
+    int kt0, n;
+    sched_kv_tiles<W>(g, qt0, kBM, &kt0, &n);
+    bool keep = kt >= kt0 && kt < kt0 + n;
+    if (keep && sched_row_tile_masked<W>(g, full_keys_for_rows(g, qt0), qt0, k0)) {
+      const int wg = (kv - k0) / 64;
+      int clo, chi;
+      sched_row_cols<W>(g, q, k0 + 64 * wg, &clo, &chi);
+      const int c = kv - k0 - 64 * wg;
+      keep = c >= clo && c <= chi;
+    }
+    vis[2] = keep ? 1 : 0;
+  }
+}
+
+// One (q, kv) pair of the test-only mask export: vis[0..2] the forward, dK/dV
+// and dQ schedules in the form the kernels run (general or one-sided),
+// vis[3..5] the same in the general form.  Keys past the tiled part are the
+// TTT suffix diagonals, key row i*Sq + q of segment i = 1..t, visible for
+// rows below the key length, as the kernels' per-row diagonal passes address
+// them.
+__host__ __device__ inline void sched_pattern_pair(const MaskGeom& g, int q, int kv, bool general,
+                                                   uint8_t vis[6]) {
+  if (kv < g.kv_main) {
+    sched_pattern_at<true>(g, q, kv, vis + 3);
+    if (general) {
+      vis[0] = vis[3];
+      vis[1] = vis[4];
+      vis[2] = vis[5];
+    } else {
+      sched_pattern_at<false>(g, q, kv, vis);
+    }
+    return;
+  }
+  const int64_t rel = (int64_t)kv - q;
+  const bool diag = g.ttt > 0 && kv >= g.Sq && rel > 0 && rel % g.Sq == 0 &&
+                    rel / g.Sq <= g.ttt && q < g.kv_len;
+  for (int p = 0; p < 6; ++p) vis[p] = diag ? 1 : 0;
 }
 
 // Tile class for the test-only mask-pattern export: 0 empty, 1 partial, 2 full.

@@ -348,12 +348,18 @@ attn_status attn_train_set_wait_budget_ns(uint64_t ns);
 
 /* ---- test-only entry points ------------------------------------------- */
 
-/* Device evaluation of the mask as the kernels schedule it.  bits: device
- * buffer of 2 * Sq * Skv bytes; plane 0 = pairs the forward/dQ row schedule
- * visits unmasked, plane 1 = pairs the dK/dV column schedule keeps, TTT
- * suffix diagonals included.  tiles (may be NULL): ceil(Sq/128) x
- * ceil(kv_main/128) tile classes (0 empty, 1 partial, 2 full) of the tiled
- * part, kv_main = Sq for TTT else Skv.  Must equal the visibility predicate. */
+/* Device evaluation of the mask as the kernels schedule it, through the same
+ * tile-range and masking calls the kernels make.  bits: device buffer of
+ * 6 * Sq * Skv bytes, six [Sq, Skv] planes of 0/1 = pair visited and not
+ * masked: plane 0 the forward, plane 1 the dK/dV pass, plane 2 the dQ pass,
+ * each in the form the kernels run for this problem (the one-sided form for
+ * full, causal and TTT masks without key lengths or additive mask, else the
+ * general form); planes 3-5 the same three passes in the general form.  TTT
+ * suffix diagonals are included as the kernels address them.  tiles (may be
+ * NULL): ceil(Sq/128) x ceil(kv_main/128) tile classes (0 empty, 1 partial,
+ * 2 full) of the tiled part, kv_main = Sq for TTT else Skv.  Every plane must
+ * equal the visibility predicate (SpecForge post, "Flex Attention",
+ * eagle3 mask_mod).  With seq_lengths set: the view of batch entry 0. */
 attn_status attn_train_mask_pattern(const attn_problem* p, uint8_t* bits, uint8_t* tiles,
                                     void* stream);
 
