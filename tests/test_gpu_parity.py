@@ -61,6 +61,9 @@ CASES = [
     W("ttt_t0", 1, 4, 2, 256, 256, 128, "ttt", 0),
     W("ttt_t1_ragged", 1, 4, 2, 300, 600, 128, "ttt", 1),
     W("ttt_t3", 1, 4, 1, 257, 1028, 128, "ttt", 3),
+    W("ttt_t4", 1, 4, 2, 200, 1000, 128, "ttt", 4),
+    W("ttt_t5", 1, 4, 2, 200, 1200, 128, "ttt", 5),
+    W("ttt_t5_ragged_d64", 1, 4, 1, 333, 1998, 64, "ttt", 5),
     W("ttt_t6_d64", 1, 2, 1, 200, 1400, 64, "ttt", 6),
     W("ttt_t2_tiny", 1, 2, 1, 5, 15, 32, "ttt", 2),
     # window masks: causal sliding, symmetric, one-sided ahead, narrow (rows that see
