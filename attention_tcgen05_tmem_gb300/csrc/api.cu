@@ -246,10 +246,13 @@ size_t ws_bytes_for(const attn_problem* p) {
 }
 
 // ------------------------------------------- built-in scratch (no-alloc bwd)
-// Scratch for attn_train_bwd_noalloc: the backward's only scratch is the
-// fp32 Delta row statistic, B * Hq * Sq floats.  4 MiB covers 1,048,576 rows
-// (the long GQA workload needs 524,288).  It lives in the module image, so
-// every GPU that loads this library holds it until the process exits.
+// Scratch for attn_train_bwd_noalloc: the backward's whole workspace
+// (ws_bytes_for: Delta, B * Hq * Sq floats; at TTT step t also 2 t floats per
+// row for the suffix diagonals; with an additive mask its bf16 transpose) must
+// fit in 4 MiB.  That is 1,048,576 rows without TTT diagonals or mask (the long
+// GQA workload needs 524,288) and about 1,048,576 / (1 + 2t) rows at TTT step t.
+// It lives in the module image, so every GPU that loads this library holds it
+// until the process exits.
 constexpr size_t kNoAllocScratchBytes = (size_t)4 << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -414,11 +417,10 @@ attn_status attn_train_bwd_noalloc(const attn_problem* p, attn_tensor q, attn_te
   if (st != ATTN_OK) return st;
   if (need > kNoAllocScratchBytes)
     return fail(ATTN_ERR_WORKSPACE,
-                "attn_train_bwd_noalloc: this problem needs %zu bytes of scratch (B*Hq*Sq = %lld "
-                "rows) but the built-in scratch holds %zu bytes (%zu rows); call attn_train_bwd "
-                "with a caller-provided workspace instead",
-                need, (long long)p->B * p->Hq * p->Sq, kNoAllocScratchBytes,
-                kNoAllocScratchBytes / sizeof(float));
+                "attn_train_bwd_noalloc: this problem's backward workspace is %zu bytes but the "
+                "built-in scratch holds %zu bytes; call attn_train_bwd with a caller-provided "
+                "workspace instead",
+                need, kNoAllocScratchBytes);
   void* scratch = nullptr;
   if ((st = noalloc_scratch(&scratch)) != ATTN_OK) return st;
   return attn_train_bwd(p, q, k, v, o, dout, lse, dq, dk, dv, scratch, kNoAllocScratchBytes,

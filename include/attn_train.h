@@ -196,10 +196,18 @@ attn_status attn_train_bwd_passes(const attn_problem* p, unsigned passes, attn_t
  * results as attn_train_bwd minus the workspace pair; it allocates nothing
  * (no cudaMalloc, cudaFree or allocating library call).
  *
- * Its scratch (the fp32 Delta row statistic) is a 4 MiB array compiled into
- * the library as device memory, held by every GPU that loads the library
- * until the process exits.  Limit: B * Hq * Sq <= 1,048,576; larger problems
- * return ATTN_ERR_WORKSPACE with a message (use attn_train_bwd then).
+ * Its scratch -- the backward's whole workspace, attn_train_workspace_size
+ * bytes: the fp32 Delta row statistic (B * Hq * Sq * 4 bytes), for a TTT step
+ * t > 0 the suffix diagonals' weights and score gradients (2 * t * B * Hq *
+ * Sq * 4 bytes more), with an additive mask its bf16 transpose -- lives in a
+ * 4 MiB array compiled into the library as device memory, held by every GPU
+ * that loads the library until the process exits.  Limit:
+ * attn_train_workspace_size(p) <= 4 MiB (4,194,304 bytes), i.e. up to
+ * 1,048,576 query rows B * Hq * Sq for the full, causal and window masks
+ * without an additive mask, and about 1,048,576 / (1 + 2t) rows at TTT step t
+ * (each part is rounded up to 256 bytes).  Larger problems return
+ * ATTN_ERR_WORKSPACE with a message giving the bytes needed (use
+ * attn_train_bwd then).
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
  * capture.  Every call on a device shares the one array and each call
