@@ -311,14 +311,37 @@ def set_wait_budget_ns(ns: int):
 
 
 # ------------------------------------------------------------ conveniences
+def canary() -> bool:
+    """ATTN_TRAIN_CANARY=1: the conveniences below fill the outputs they
+    allocate with NaN and the workspace with 0xff bytes (NaN as fp32) instead of
+    leaving them uninitialised, so that an element a kernel fails to write shows
+    up as NaN rather than as a plausible stale value (a debugging aid; the test
+    suite turns it on)."""
+    return os.environ.get("ATTN_TRAIN_CANARY", "0") == "1"
+
+
+def _alloc(shape, dtype, device):
+    import torch
+    if canary():
+        return torch.full(shape, float("nan"), dtype=dtype, device=device)
+    return torch.empty(shape, dtype=dtype, device=device)
+
+
+def _alloc_workspace(nbytes, device):
+    import torch
+    if canary():
+        return torch.full((nbytes,), 0xFF, dtype=torch.uint8, device=device)
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
 def fwd(q, k, v, mask="causal", ttt_step=0, scale=None, stream=None, out="bf16", window=None,
         seq_lengths=None, add_mask=None):
     """Allocates O (bf16 or fp32) and LSE with torch, runs the forward;
     returns (o, lse)."""
     import torch
     p = problem_for(q, k, mask, ttt_step, scale, out, window, seq_lengths, add_mask)
-    o = torch.empty(q.shape, dtype=_torch_out_dtype(out), device=q.device)
-    lse = torch.empty(q.shape[0], q.shape[1], q.shape[2], dtype=torch.float32, device=q.device)
+    o = _alloc(q.shape, _torch_out_dtype(out), q.device)
+    lse = _alloc((q.shape[0], q.shape[1], q.shape[2]), torch.float32, q.device)
     fwd_raw(p, q, k, v, o, lse, stream)
     return o, lse
 
@@ -330,11 +353,11 @@ def bwd(q, k, v, o, lse, dout, mask="causal", ttt_step=0, scale=None, stream=Non
     import torch
     out = "fp32" if o.dtype == torch.float32 else "bf16"
     p = problem_for(q, k, mask, ttt_step, scale, out, window, seq_lengths, add_mask)
-    dq = torch.empty(q.shape, dtype=o.dtype, device=q.device)
-    dk = torch.empty(k.shape, dtype=o.dtype, device=q.device)
-    dv = torch.empty(v.shape, dtype=o.dtype, device=q.device)
+    dq = _alloc(q.shape, o.dtype, q.device)
+    dk = _alloc(k.shape, o.dtype, q.device)
+    dv = _alloc(v.shape, o.dtype, q.device)
     if workspace is None:
-        workspace = torch.empty(workspace_size(p), dtype=torch.uint8, device=q.device)
+        workspace = _alloc_workspace(workspace_size(p), q.device)
     bwd_raw(p, q, k, v, o, dout, lse, dq, dk, dv, workspace, stream)
     return dq, dk, dv
 

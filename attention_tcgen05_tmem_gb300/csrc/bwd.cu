@@ -225,7 +225,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t T_DP = DB ? 256 : 128;
   constexpr uint32_t T_DV = DB ? 384 : 256;
   extern __shared__ uint8_t smem_raw[];
-  if (*reinterpret_cast<volatile uint32_t*>(a.ctl.err) != 0) return;
 
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
@@ -254,6 +253,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hk = bh % d.Hkv;
   const int b = bh / d.Hkv;
   const int k0 = kt * kBN;
+  if (*reinterpret_cast<volatile uint32_t*>(a.ctl.err) != 0) {
+    // sticky device error: no work; NaN over this CTA's dK and dV rows
+    const int nrows = min(kBN, d.geom.kv_main - k0);
+    poison_rows(a.dk, b, hk, k0, nrows, D, d.out_f32 != 0);
+    poison_rows(a.dv, b, hk, k0, nrows, D, d.out_f32 != 0);
+    return;
+  }
   // this batch entry's geometry; query tiles qt_begin .. qt_begin + n_q - 1 see the key tile
   const MaskGeom g = W ? with_len(d.geom, d.seqlens, b) : d.geom;
   int qt_begin, n_q;
@@ -545,6 +551,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (store) store16(a.dk, b, hk, kv, c0, vals, d.scale, f32);
       }
+    } else if (kv < g.kv_main) {
+      // a wait of this CTA ran out of budget: NaN instead of a partial result
+      poison_row(a.dv, b, hk, kv, 16 * wg, 32, D, d.out_f32 != 0);
+      poison_row(a.dk, b, hk, kv, 16 * wg, 32, D, d.out_f32 != 0);
     }
   }
 
@@ -594,7 +604,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // computed as soon as dP(j) has been read and S(j+1) long before it is needed.
   constexpr int T_S = 0, T_DP = 256, T_DQ = 384;
   extern __shared__ uint8_t smem_raw[];
-  if (*reinterpret_cast<volatile uint32_t*>(a.ctl.err) != 0) return;
 
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
@@ -631,6 +640,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = bh / d.Hq;
   const int hk = h / d.G;
   const int q0 = qt * kBM;
+  if (*reinterpret_cast<volatile uint32_t*>(a.ctl.err) != 0) {
+    // sticky device error: no work; NaN over this CTA's dQ rows
+    poison_rows(a.dq, b, h, q0, min(kBM, d.Sq - q0), D, d.out_f32 != 0);
+    return;
+  }
   // this batch entry's geometry; key tiles kt0 .. kt0 + n_kv - 1
   const MaskGeom g = W ? with_len(d.geom, d.seqlens, b) : d.geom;
   int kt0, n_kv;
@@ -930,6 +944,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (qin) store16(a.dq, b, h, q, c0, acc, d.scale, d.out_f32 != 0);
       }
+    } else if (qin) {
+      // a wait of this CTA ran out of budget: NaN instead of a partial result
+      poison_row(a.dq, b, h, q, 16 * wg, 32, D, d.out_f32 != 0);
     }
   }
 

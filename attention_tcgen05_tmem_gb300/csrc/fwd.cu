@@ -165,8 +165,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   constexpr uint32_t O_COL = TB ? 384u : 256u;   // first O accumulator column
   extern __shared__ uint8_t smem_raw[];
 
-  if (*reinterpret_cast<volatile uint32_t*>(a.ctl.err) != 0) return;  // sticky device error
-
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* q_full = bars;
@@ -196,6 +194,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int b = bh / d.Hq;
   const int hk = h / d.G;
   const int q0 = qp * 2 * kBM;
+  if (*reinterpret_cast<volatile uint32_t*>(a.ctl.err) != 0) {
+    // sticky device error: no work; NaN over this CTA's O and LSE rows
+    const int nrows = min(2 * kBM, d.Sq - q0);
+    poison_rows(a.o, b, h, q0, nrows, D, d.out_f32 != 0);
+    for (int i = threadIdx.x; i < nrows; i += blockDim.x)
+      a.lse[((int64_t)b * d.Hq + h) * d.Sq + q0 + i] = nan_f32();
+    return;
+  }
   // this batch entry's geometry; key tiles kt0 .. kt0 + n_kv - 1
   const MaskGeom g = W ? with_len(d.geom, d.seqlens, b) : d.geom;
   int kt0, n_kv;
@@ -608,6 +614,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const float lse = (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * 0.69314718055994531f : 0.f;
         a.lse[((int64_t)b * d.Hq + h) * d.Sq + q] = lse;
       }
+    } else if (q < d.Sq) {
+      // a wait of this CTA ran out of budget: NaN instead of a partial result
+      poison_row(a.o, b, h, q, 0, 16, D, d.out_f32 != 0);
+      a.lse[((int64_t)b * d.Hq + h) * d.Sq + q] = nan_f32();
     }
   }
 

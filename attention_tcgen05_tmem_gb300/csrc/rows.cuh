@@ -150,4 +150,30 @@ __device__ __forceinline__ void store16(const View& v, int b, int h, int64_t s, 
   }
 }
 
+// Skipped work is made visible: a CTA that computes nothing (the device error
+// word was already set when it started) or gave up part-way (one of its waits
+// ran out of budget) writes NaN where its results would go, so that stale
+// memory can never pass for a result.
+__device__ __forceinline__ float nan_f32() { return __int_as_float(0x7fc00000); }
+
+// NaN over columns c_begin, c_begin + step, ... (16-column chunks) of one row.
+__device__ __forceinline__ void poison_row(const View& v, int b, int h, int64_t s, int c_begin,
+                                           int c_step, int D, bool f32) {
+  float x[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) x[e] = nan_f32();
+  for (int c0 = c_begin; c0 < D; c0 += c_step) store16(v, b, h, s, c0, x, 1.f, f32);
+}
+
+// NaN over rows [s0, s0 + n) of an output view, by all threads of the CTA.
+__device__ __forceinline__ void poison_rows(const View& v, int b, int h, int64_t s0, int n, int D,
+                                            bool f32) {
+  const int chunks = D / 16;
+  float x[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) x[e] = nan_f32();
+  for (int i = threadIdx.x; i < n * chunks; i += blockDim.x)
+    store16(v, b, h, s0 + i / chunks, (i % chunks) * 16, x, 1.f, f32);
+}
+
 }  // namespace attn

@@ -7,6 +7,10 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+# outputs and workspaces that the binding allocates start as NaN, so that an
+# element no kernel writes fails the parity checks instead of passing as stale memory
+os.environ.setdefault("ATTN_TRAIN_CANARY", "1")
+
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built library")

@@ -371,3 +371,35 @@ def test_device_wait_timeout_is_reported_and_cleared():
     # the word is cleared: the library works again
     run_both(synth.TINY, check_bwd=False)
     del dev
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("out", ["fp32", "bf16"])
+def test_skipped_work_leaves_nan_not_stale_memory(out):
+    """While the device error word is set, every attention kernel returns
+    without computing.  Its outputs must then read NaN -- not whatever the
+    buffers held before -- also for a caller that does not ask
+    attn_train_device_status first.  Clearing the word makes the library work
+    again."""
+    dev = device()
+    w = W("skip_gqa_ragged", 2, 4, 2, 333, 333, 128, "causal", seed=9)
+    x = synth.make_inputs(w)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
+    p = binding.problem(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.mask, 0, 0.0, out)
+    odt = torch.float32 if out == "fp32" else torch.bfloat16
+    # buffers holding finite stale values
+    o, dq = (torch.full(q.shape, 7.0, dtype=odt, device=dev) for _ in range(2))
+    dk, dv = (torch.full(k.shape, 7.0, dtype=odt, device=dev) for _ in range(2))
+    lse = torch.full((w.B, w.Hq, w.Sq), 7.0, dtype=torch.float32, device=dev)
+    ws = torch.zeros(binding.workspace_size(p), dtype=torch.uint8, device=dev)
+    binding.selftest_wait_timeout()  # sets the device error word
+    binding.fwd_raw(p, q, k, v, o, lse)
+    binding.bwd_raw(p, q, k, v, o, do, lse, dq, dk, dv, ws)
+    torch.cuda.synchronize(dev)
+    for name, t in (("O", o), ("LSE", lse), ("dQ", dq), ("dK", dk), ("dV", dv)):
+        assert torch.isnan(t).all(), f"{name}: skipped work left non-NaN values"
+    with pytest.raises(binding.AttnError) as ei:
+        binding.device_status()
+    assert ei.value.status == 6
+    run_both(w, out=out)  # the word is cleared: correct results again
+
