@@ -67,6 +67,9 @@ def parse_args():
     ap.add_argument("--all", action="store_true", help="one line per workload of the pages")
     ap.add_argument("--out", choices=["fp32", "bf16"], default="fp32",
                     help="dtype of O, dQ, dK, dV (fp32 is the parity-gated configuration)")
+    ap.add_argument("--repeats", type=int, default=3,
+                    help="timed regions per workload (interleaved across workloads); the "
+                         "line reports the median region and the spread")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-chunk", type=int, default=0,
@@ -270,103 +273,126 @@ class Case:
                 evs[2 + i].record(stream)
 
 
-def run_ours(args, ws, local_rank, dist):
-    import torch
+class Runner:
+    """One workload on one GPU: device buffers, the timed device-only region
+    (K steps of kernels with CUDA events between them) and the end-to-end
+    region through the host-memory session.  Each region can be run several
+    times; main() interleaves the repeats across workloads."""
 
-    from attention_tcgen05_tmem_gb300 import binding, synth
-    from attention_tcgen05_tmem_gb300 import build as lib_build
+    def __init__(self, args, ws, local_rank, dist):
+        import torch
 
-    lib_build.build()
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    stream = torch.cuda.current_stream(dev)
-    cases = [Case(w, dev, args.out, binding, synth) for w in ws]
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > 129 MB L2
+        from attention_tcgen05_tmem_gb300 import binding, synth
+        from attention_tcgen05_tmem_gb300 import build as lib_build
 
-    for _ in range(max(args.warmup, 3)):
-        for c in cases:
-            c.step(stream)
-    torch.cuda.synchronize(dev)
-    binding.device_status()
-
-    K = args.steps
-    evsets = [[[torch.cuda.Event(enable_timing=True) for _ in range(len(c.names) + 1)]
-               for c in cases] for _ in range(K)]
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    with ClockSampler(gpu_index_for(local_rank)) as clk:
-        for i in range(K):
-            flush.zero_()  # evict L2 between steps (outside the events)
-            for c, evs in zip(cases, evsets[i]):
-                c.step(stream, evs)
+        lib_build.build()
+        self.args, self.ws, self.dist, self.local_rank = args, ws, dist, local_rank
+        self.binding = binding
+        self.dev = dev = torch.device("cuda", local_rank)
+        torch.cuda.set_device(dev)
+        self.stream = torch.cuda.current_stream(dev)
+        self.cases = [Case(w, dev, args.out, binding, synth) for w in ws]
+        self.flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > 129 MB L2
+        self.hosts = None
+        self.h2d = self.d2h = 0
+        self.launches_per_step = sum(c.launches for c in self.cases)
+        for _ in range(max(args.warmup, 3)):
+            for c in self.cases:
+                c.step(self.stream)
         torch.cuda.synchronize(dev)
-    if dist:
-        dist.barrier()
-    binding.device_status()
-    per_kernel = {}
-    total_ms = 0.0
-    for i in range(K):
-        for c, evs in zip(cases, evsets[i]):
-            total_ms += evs[0].elapsed_time(evs[-1])
-            for j, n in enumerate(c.names):
-                per_kernel[n] = per_kernel.get(n, 0.0) + evs[j].elapsed_time(evs[j + 1])
-    clocks = clk.summary()
+        binding.device_status()
 
-    e2e_ms, h2d, d2h = None, 0, 0
-    if not args.no_e2e:
+    def timed(self):
+        """K steps, L2 flushed between steps outside the events; returns the
+        summed event time of the steps, per-kernel sums and the clocks seen."""
+        import torch
+        K, dev, dist = self.args.steps, self.dev, self.dist
+        evsets = [[[torch.cuda.Event(enable_timing=True) for _ in range(len(c.names) + 1)]
+                   for c in self.cases] for _ in range(K)]
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        with ClockSampler(gpu_index_for(self.local_rank)) as clk:
+            for i in range(K):
+                self.flush.zero_()  # evict L2 between steps (outside the events)
+                for c, evs in zip(self.cases, evsets[i]):
+                    c.step(self.stream, evs)
+            torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+        self.binding.device_status()
+        per_kernel, total_ms = {}, 0.0
+        for i in range(K):
+            for c, evs in zip(self.cases, evsets[i]):
+                total_ms += evs[0].elapsed_time(evs[-1])
+                for j, n in enumerate(c.names):
+                    per_kernel[n] = per_kernel.get(n, 0.0) + evs[j].elapsed_time(evs[j + 1])
+        total_ms, = max_over_ranks([total_ms], dist, dev)
+        return {"total_ms": total_ms, "per_kernel_ms": per_kernel, "clocks": clk.summary()}
+
+    def _open_sessions(self):
         # end to end through the C ABI's host-memory session (attn_train_host_session_*):
         # every step copies q, k, v, dO (and key lengths / mask) in from pinned host
         # buffers and O, LSE, dQ, dK, dV out; the copies overlap the kernels of the
         # same and the neighbouring steps, and the timed region ends after the last
         # step's copies (join + synchronize)
-        hosts = []
-        for c in cases:
+        import torch
+        b, args = self.binding, self.args
+        self.hosts = []
+        for c in self.cases:
             w = c.w
             pin = {n: c.x[n].pin_memory()
                    for n in ("q", "k", "v", "dout", "seq_lengths", "add_mask") if n in c.x}
             outs = {n: torch.empty(getattr(c, n).shape, dtype=getattr(c, n).dtype).pin_memory()
                     for n in ("o", "lse", "dq", "dk", "dv")}
-            hp = binding.problem(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.mask, w.ttt_step, 0.0,
-                                 args.out, w.window, pin.get("seq_lengths"), pin.get("add_mask"),
-                                 host=True)
+            hp = b.problem(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.mask, w.ttt_step, 0.0, args.out,
+                           w.window, pin.get("seq_lengths"), pin.get("add_mask"), host=True)
             io = {"q": pin["q"], "k": pin["k"], "v": pin["v"], "dout": pin["dout"], **outs}
-            arena = torch.empty(binding.step_host_arena_size(hp, args.e2e_chunk),
-                                dtype=torch.uint8, device=dev)
-            hosts.append((binding.HostSession(hp, arena, args.e2e_chunk), io))
-            h2d += sum(t.numel() * t.element_size() for t in pin.values())
-            d2h += sum(t.numel() * t.element_size() for t in outs.values())
+            arena = torch.empty(b.step_host_arena_size(hp, args.e2e_chunk), dtype=torch.uint8,
+                                device=self.dev)
+            self.hosts.append((b.HostSession(hp, arena, args.e2e_chunk), io))
+            self.h2d += sum(t.numel() * t.element_size() for t in pin.values())
+            self.d2h += sum(t.numel() * t.element_size() for t in outs.values())
+        self._e2e_steps(2)  # warm-up
 
-        def e2e_step():
-            for sess, io in hosts:
-                sess.step(io, stream.cuda_stream)
+    def _e2e_steps(self, n):
+        for _ in range(n):
+            for sess, io in self.hosts:
+                sess.step(io, self.stream.cuda_stream)
+        for sess, _ in self.hosts:
+            sess.join(self.stream.cuda_stream)
 
-        for _ in range(2):
-            e2e_step()
-        for sess, _ in hosts:
-            sess.join(stream.cuda_stream)
+    def e2e(self):
+        """Milliseconds for K end-to-end steps (at most 20 run; scaled to K)."""
+        import torch
+        if self.hosts is None:
+            self._open_sessions()
+        dev, dist, K = self.dev, self.dist, self.args.steps
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if dist:
             dist.barrier()
         torch.cuda.synchronize(dev)
         Ke = max(3, min(K, 20))
-        e0.record(stream)
-        for _ in range(Ke):
-            e2e_step()
-        for sess, _ in hosts:
-            sess.join(stream.cuda_stream)
-        e1.record(stream)
+        e0.record(self.stream)
+        self._e2e_steps(Ke)
+        e1.record(self.stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = e0.elapsed_time(e1) / Ke * K
-        binding.device_status()
-        for sess, _ in hosts:
-            sess.close()
+        self.binding.device_status()
+        ms, = max_over_ranks([e0.elapsed_time(e1) / Ke * K], dist, dev)
+        return ms
 
-    total_ms, e2e_max = max_over_ranks([total_ms, e2e_ms or 0.0], dist, dev)
-    return {"K": K, "total_ms": total_ms, "e2e_ms": e2e_max if e2e_ms else None,
-            "per_kernel_ms": per_kernel, "clocks": clocks, "h2d": h2d, "d2h": d2h,
-            "launches_per_step": sum(c.launches for c in cases)}
+    def close(self):
+        for sess, _ in self.hosts or []:
+            sess.close()
+        self.hosts = None
+
+
+def median_run(runs):
+    """The repeat with the median total time (its per-kernel times and clocks
+    go with it)."""
+    order = sorted(range(len(runs)), key=lambda i: runs[i]["total_ms"])
+    return runs[order[(len(order) - 1) // 2]]
 
 
 def max_over_ranks(values, dist, device="cpu"):
@@ -455,6 +481,32 @@ def theoretical_peak(value_per_gpu, clocks, device):
     peak = sms * mhz * 1e6 * BF16_FLOP_PER_CLK_SM / 1e12
     return {"theoretical": value_per_gpu / peak, "theoretical_tflops": peak,
             "theoretical_basis": f"{sms} SMs x {mhz:.0f} MHz x {BF16_FLOP_PER_CLK_SM} FLOP/clk"}
+
+
+def clock_peak_tflops(clocks, device):
+    """SMs x the median SM clock sampled under load x the per-SM dense bf16
+    rate: the tensor peak at the clock the kernels actually ran at."""
+    import torch
+    mhz = (clocks or {}).get("sm_mhz")
+    if not mhz:
+        return None
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    return sms * mhz * 1e6 * BF16_FLOP_PER_CLK_SM / 1e12
+
+
+def merge_clocks(samples):
+    """Clock records of several timed regions as one: the median of their
+    median SM clocks, the highest max clock and power, every throttle reason
+    seen in any of them."""
+    got = [c for c in samples if c.get("sm_mhz") is not None]
+    if not got:
+        return samples[0] if samples else {"sm_mhz": None, "reasons": ["unsampled"], "samples": 0}
+    pw = [c["power_w_max"] for c in got if c.get("power_w_max") is not None]
+    return {"sm_mhz": statistics.median(c["sm_mhz"] for c in got),
+            "sm_max_mhz": max(c["sm_max_mhz"] for c in got),
+            "reasons": sorted(set().union(*(c["reasons"] for c in got))),
+            "power_w_max": max(pw) if pw else None,
+            "samples": sum(c["samples"] for c in got)}
 
 
 def describe(name, ws, out, n_gpus):
@@ -698,11 +750,26 @@ def main():
     peak_hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     for name in loss_names:
         run_loss(args, losses[name], rank, local_rank, dist, n_gpus, peaks, peak_src)
+    # every timed region runs args.repeats times, the repeats interleaved across
+    # workloads (arm drift between invocations shows as spread, not as bias)
+    runners = {name: Runner(args, table[name], local_rank, dist) for name in names}
+    runs = {name: [] for name in names}
+    e2es = {name: [] for name in names}
+    for _ in range(args.repeats):
+        for name in names:
+            runs[name].append(runners[name].timed())
+    if not args.no_e2e:
+        for _ in range(args.repeats):
+            for name in names:
+                e2es[name].append(runners[name].e2e())
+    for name in names:
+        runners[name].close()
     for name in names:
         ws = table[name]
         F = sum(flops.flops_fwd_bwd(w) for w in ws)
-        r = run_ours(args, ws, local_rank, dist)
-        K = r["K"]
+        K = args.steps
+        r = median_run(runs[name])
+        clocks = merge_clocks([x["clocks"] for x in runs[name]])
         value = job_value(F, K, r["total_ms"], n_gpus)
         pk = r["per_kernel_ms"]
         dom = max(pk, key=lambda n: pk[n])
@@ -713,14 +780,23 @@ def main():
                     "unit": "GB/s", "frac": ach / peak_hbm, "traffic": None,
                     "peak_kind": f"HBM copy, of {peak_src}"}
         else:
+            # the kernel is timed per launch (milliseconds) inside a short timed region,
+            # so the burst figure is its peak; the sustained one is given beside it,
+            # and frac_clock compares with SMs x the sampled SM clock x the dense rate
             ach = kernel_flops(ws, dom) / (dom_ms * 1e-3) / 1e12
-            roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak_sus,
-                    "unit": "TFLOP/s", "frac": ach / peak_sus, "traffic": None,
-                    "peak_kind": f"bf16 sustained, of {peak_src}"}
+            roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak_burst,
+                    "unit": "TFLOP/s", "frac": ach / peak_burst, "traffic": None,
+                    "peak_kind": f"bf16 burst, of {peak_src}",
+                    "peak_sustained": peak_sus, "frac_sustained": ach / peak_sus}
+            clk_peak = clock_peak_tflops(clocks, local_rank)
+            if clk_peak:
+                roof["frac_clock"] = ach / clk_peak
+                roof["clock_peak"] = clk_peak
         traffic = load_traffic(name, dom)
         if traffic is not None:
             roof["traffic"] = traffic
         alg_bytes = sum(flops.bytes_fwd(w) + flops.bytes_bwd(w) for w in ws)
+        totals = sorted(x["total_ms"] / K for x in runs[name])
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": n_gpus, "steps": K,
             "warmup": args.warmup, "ms_per_step": r["total_ms"] / K, "higher_is_better": True,
@@ -728,19 +804,27 @@ def main():
             "config": describe(name, ws, args.out, n_gpus),
             "pct_of_peak": {"bf16_burst": value / n_gpus / peak_burst,
                             "bf16_sustained": value / n_gpus / peak_sus, "source": peak_src,
-                            **theoretical_peak(value / n_gpus, r["clocks"], local_rank)},
+                            **theoretical_peak(value / n_gpus, clocks, local_rank)},
             "fwd_tflops": sum(flops.flops_fwd(w) for w in ws) / (pk["fwd"] / K * 1e-3) / 1e12,
             "bwd_tflops": sum(flops.flops_bwd(w) for w in ws) /
                           (sum(v for n, v in pk.items() if n != "fwd") / K * 1e-3) / 1e12,
             "hbm_gbs_algorithmic": alg_bytes / (r["total_ms"] / K * 1e-3) / 1e9,
             "kernel_ms": {n: v / K for n, v in pk.items()},
             "roofline": roof,
-            "gpu_launches": r["launches_per_step"] * K,
-            "clocks": r["clocks"],
+            "gpu_launches": runners[name].launches_per_step * K,
+            "clocks": clocks,
+            "repeats": {"n": len(totals), "steps_each": K,
+                        "ms_per_step": {"median": r["total_ms"] / K, "min": totals[0],
+                                        "max": totals[-1]}},
         }
-        if r["e2e_ms"]:
-            line["e2e"] = {"value": job_value(F, K, r["e2e_ms"], n_gpus), "unit": UNIT,
-                           "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]}
+        if e2es[name]:
+            e = sorted(e2es[name])
+            e_med = e[(len(e) - 1) // 2]
+            line["e2e"] = {"value": job_value(F, K, e_med, n_gpus), "unit": UNIT,
+                           "h2d_bytes_per_step": runners[name].h2d,
+                           "d2h_bytes_per_step": runners[name].d2h}
+            line["repeats"]["e2e_ms_per_step"] = {"median": e_med / K, "min": e[0] / K,
+                                                  "max": e[-1] / K}
         if rank == 0 and n_gpus == 1 and not args.no_cpu_baseline:
             tf, desc, threads, pp = cpu_sample(ws, args.cpu_seconds)
             line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": threads, "kind": "oracle",

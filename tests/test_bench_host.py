@@ -1,0 +1,32 @@
+"""Host-side logic of bench.py that needs no GPU: which repeat is reported and
+how the clock records of several timed regions combine."""
+import bench
+
+
+def test_median_run_picks_the_middle_repeat_with_its_kernel_times():
+    runs = [{"total_ms": 9.0, "per_kernel_ms": {"fwd": 3.0}},
+            {"total_ms": 7.0, "per_kernel_ms": {"fwd": 2.0}},
+            {"total_ms": 8.0, "per_kernel_ms": {"fwd": 2.5}}]
+    r = bench.median_run(runs)
+    assert r["total_ms"] == 8.0 and r["per_kernel_ms"]["fwd"] == 2.5
+    # an even count takes the lower middle
+    assert bench.median_run(runs[:2])["total_ms"] == 7.0
+
+
+def test_merge_clocks_keeps_every_throttle_reason():
+    a = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "power_w_max": 900.0,
+         "samples": 5}
+    b = {"sm_mhz": 1900.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"],
+         "power_w_max": 1300.0, "samples": 4}
+    c = {"sm_mhz": 2000.0, "sm_max_mhz": 2070.0, "reasons": ["hw_slowdown"],
+         "power_w_max": None, "samples": 6}
+    m = bench.merge_clocks([a, b, c])
+    assert m["sm_mhz"] == 2000.0 and m["sm_max_mhz"] == 2070.0
+    assert m["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    assert m["power_w_max"] == 1300.0 and m["samples"] == 15
+
+
+def test_merge_clocks_without_samples():
+    m = bench.merge_clocks([{"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"],
+                             "samples": 0}])
+    assert m["reasons"] == ["unsampled"]
