@@ -8,10 +8,13 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -39,6 +42,28 @@ attn_status cuda_fail(cudaError_t e, const char* what) {
 }
 
 std::atomic<uint64_t> g_budget_ns{2000000000ull};
+
+// ATTN_TRAIN_NVTX=1 (read once per process): every entry point that enqueues
+// kernels wraps each of its launches in an NVTX range named after the kernel
+// pass, for profilers' timelines.  Off by default; then a range costs one
+// branch on a cached flag.
+bool nvtx_on() {
+  static const bool on = [] {
+    const char* e = std::getenv("ATTN_TRAIN_NVTX");
+    return e != nullptr && e[0] == '1';
+  }();
+  return on;
+}
+
+struct NvtxRange {
+  bool on;
+  explicit NvtxRange(const char* name) : on(nvtx_on()) {
+    if (on) nvtxRangePushA(name);
+  }
+  ~NvtxRange() {
+    if (on) nvtxRangePop();
+  }
+};
 
 // ----------------------------------------------------- device error word
 __device__ uint32_t g_device_error;
@@ -329,6 +354,7 @@ attn_status attn_train_fwd(const attn_problem* p, attn_tensor q, attn_tensor k, 
   if ((st = make_map(&m.k, a.k, p->B, p->Hkv, p->Skv, p->D, "k")) != ATTN_OK) return st;
   if ((st = make_map(&m.v, a.v, p->B, p->Hkv, p->Skv, p->D, "v")) != ATTN_OK) return st;
   m.dout = m.q;
+  NvtxRange range("attn_train_fwd");
   cudaError_t e = attn::launch_fwd(a, m, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return ATTN_OK;
@@ -403,7 +429,19 @@ attn_status attn_train_bwd_passes(const attn_problem* p, unsigned passes, attn_t
   if ((st = make_map(&m.k, a.k, p->B, p->Hkv, p->Skv, p->D, "k")) != ATTN_OK) return st;
   if ((st = make_map(&m.v, a.v, p->B, p->Hkv, p->Skv, p->D, "v")) != ATTN_OK) return st;
   if ((st = make_map(&m.dout, a.dout, p->B, p->Hq, p->Sq, p->D, "dout")) != ATTN_OK) return st;
-  cudaError_t e = attn::launch_bwd(a, m, passes, static_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaSuccess;
+  if (nvtx_on()) {
+    // one range per pass, launched one at a time in the usual order
+    static const char* const names[4] = {"attn_train_bwd:prep", "attn_train_bwd:dkdv",
+                                         "attn_train_bwd:dq", "attn_train_bwd:ttt_suffix"};
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i) {
+      if ((passes & (1u << i)) == 0) continue;
+      NvtxRange range(names[i]);
+      e = attn::launch_bwd(a, m, 1u << i, static_cast<cudaStream_t>(stream));
+    }
+  } else {
+    e = attn::launch_bwd(a, m, passes, static_cast<cudaStream_t>(stream));
+  }
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   return ATTN_OK;
 }
@@ -460,6 +498,7 @@ attn_status attn_train_logsoftmax_loss_fwd(int64_t rows, int64_t V, const float*
     return fail(ATTN_ERR_ALIGNMENT, "row outputs and loss must be 4-byte aligned");
   attn::LossArgs a{rows, V, ld_logits, ld_target, logits, nullptr, target, mask,
                    row_loss, row_lse, row_tsum, loss, nullptr};
+  NvtxRange range("attn_train_logsoftmax_loss_fwd");
   cudaError_t e = attn::launch_logsoftmax_loss_fwd(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "log-softmax loss forward launch");
   return ATTN_OK;
@@ -479,6 +518,7 @@ attn_status attn_train_logsoftmax_loss_bwd(int64_t rows, int64_t V, float* logit
   attn::LossArgs a{rows, V, ld_logits, ld_target, logits, logits, target, mask,
                    nullptr, const_cast<float*>(row_lse), const_cast<float*>(row_tsum), nullptr,
                    grad_loss};
+  NvtxRange range("attn_train_logsoftmax_loss_bwd");
   cudaError_t e = attn::launch_logsoftmax_loss_bwd(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "log-softmax loss backward launch");
   return ATTN_OK;
