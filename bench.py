@@ -363,7 +363,8 @@ class Runner:
             sess.join(self.stream.cuda_stream)
 
     def e2e(self):
-        """Milliseconds for K end-to-end steps (at most 20 run; scaled to K)."""
+        """Milliseconds for K end-to-end steps (at most 20 run; scaled to K) and
+        the clocks sampled meanwhile."""
         import torch
         if self.hosts is None:
             self._open_sessions()
@@ -374,13 +375,14 @@ class Runner:
             dist.barrier()
         torch.cuda.synchronize(dev)
         Ke = max(3, min(K, 20))
-        e0.record(self.stream)
-        self._e2e_steps(Ke)
-        e1.record(self.stream)
-        torch.cuda.synchronize(dev)
+        with ClockSampler(gpu_index_for(self.local_rank)) as clk:
+            e0.record(self.stream)
+            self._e2e_steps(Ke)
+            e1.record(self.stream)
+            torch.cuda.synchronize(dev)
         self.binding.device_status()
         ms, = max_over_ranks([e0.elapsed_time(e1) / Ke * K], dist, dev)
-        return ms
+        return {"ms": ms, "clocks": clk.summary()}
 
     def close(self):
         for sess, _ in self.hosts or []:
@@ -818,13 +820,14 @@ def main():
                                         "max": totals[-1]}},
         }
         if e2es[name]:
-            e = sorted(e2es[name])
+            e = sorted(x["ms"] for x in e2es[name])
             e_med = e[(len(e) - 1) // 2]
             line["e2e"] = {"value": job_value(F, K, e_med, n_gpus), "unit": UNIT,
                            "h2d_bytes_per_step": runners[name].h2d,
                            "d2h_bytes_per_step": runners[name].d2h}
             line["repeats"]["e2e_ms_per_step"] = {"median": e_med / K, "min": e[0] / K,
                                                   "max": e[-1] / K}
+            line["e2e_clocks"] = merge_clocks([x["clocks"] for x in e2es[name]])
         if rank == 0 and n_gpus == 1 and not args.no_cpu_baseline:
             tf, desc, threads, pp = cpu_sample(ws, args.cpu_seconds)
             line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": threads, "kind": "oracle",
