@@ -211,6 +211,14 @@ struct DkdvLayout {
 // other masks take the one-sided form of the tile arithmetic.
 // W: general mask arithmetic (window, key lengths, additive mask); M (implies
 // W): an additive mask is present, in an instantiation of its own.
+// NaN over rows [k0, k0 + n) of dK and dV (a CTA that skips its work); kept
+// out of line so that it costs the kernel's register allocation nothing.
+__device__ __noinline__ void poison_key_rows(const BwdArgs& a, int b, int hk, int k0, int n,
+                                             int D) {
+  poison_rows(a.dk, b, hk, k0, n, D, a.d.out_f32 != 0);
+  poison_rows(a.dv, b, hk, k0, n, D, a.d.out_f32 != 0);
+}
+
 template <int D, bool W, bool M>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -255,9 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int k0 = kt * kBN;
   if (*reinterpret_cast<volatile uint32_t*>(a.ctl.err) != 0) {
     // sticky device error: no work; NaN over this CTA's dK and dV rows
-    const int nrows = min(kBN, d.geom.kv_main - k0);
-    poison_rows(a.dk, b, hk, k0, nrows, D, d.out_f32 != 0);
-    poison_rows(a.dv, b, hk, k0, nrows, D, d.out_f32 != 0);
+    poison_key_rows(a, b, hk, k0, min(kBN, d.geom.kv_main - k0), D);
     return;
   }
   // this batch entry's geometry; query tiles qt_begin .. qt_begin + n_q - 1 see the key tile
