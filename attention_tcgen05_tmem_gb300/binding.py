@@ -21,7 +21,8 @@ STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID", 2: "ATTN_ERR_UNSUPPORTED", 3: "AT
           4: "ATTN_ERR_WORKSPACE", 5: "ATTN_ERR_CUDA", 6: "ATTN_ERR_DEVICE_TIMEOUT"}
 
 # Entry points of include/attn_train.h (checked against the header by the tests).
-EXPORTS = ("attn_train_supports", "attn_train_workspace_size", "attn_train_fwd", "attn_train_bwd",
+EXPORTS = ("attn_train_supports", "attn_train_workspace_size", "attn_train_fwd",
+           "attn_train_fwd_workspace_size", "attn_train_fwd_ws", "attn_train_bwd",
            "attn_train_bwd_passes", "attn_train_bwd_noalloc", "attn_train_last_error", "attn_train_device_status", "attn_train_set_wait_budget_ns",
            "attn_train_mask_pattern", "attn_train_probe_mma", "attn_train_selftest_wait_timeout",
            "attn_train_logsoftmax_loss_fwd", "attn_train_logsoftmax_loss_bwd",
@@ -81,6 +82,8 @@ def load(path: str = LIB_PATH):
             "attn_train_supports": (st, [P]),
             "attn_train_workspace_size": (st, [P, ctypes.POINTER(ctypes.c_size_t)]),
             "attn_train_fwd": (st, [P, T, T, T, T, vp, vp]),
+            "attn_train_fwd_workspace_size": (st, [P, ctypes.POINTER(ctypes.c_size_t)]),
+            "attn_train_fwd_ws": (st, [P, T, T, T, T, vp, vp, ctypes.c_size_t, vp]),
             "attn_train_bwd": (st, [P, T, T, T, T, T, vp, T, T, T, vp, ctypes.c_size_t, vp]),
             "attn_train_bwd_passes": (st, [P, ctypes.c_uint, T, T, T, T, T, vp, T, T, T, vp,
                                            ctypes.c_size_t, vp]),
@@ -204,10 +207,26 @@ def workspace_size(p: Problem) -> int:
     return int(n.value)
 
 
+def fwd_workspace_size(p: Problem) -> int:
+    """attn_train_fwd_workspace_size: 0 unless the forward splits its key range
+    (small grids) on the current device."""
+    n = ctypes.c_size_t(0)
+    _check(load().attn_train_fwd_workspace_size(ctypes.byref(p), ctypes.byref(n)))
+    return int(n.value)
+
+
 def fwd_raw(p: Problem, q, k, v, o, lse, stream=None):
     """attn_train_fwd on caller-owned tensors (o, lse are written)."""
     _check(load().attn_train_fwd(ctypes.byref(p), view(q), view(k), view(v), view(o),
                                  ctypes.c_void_p(lse.data_ptr()), _stream(stream)))
+
+
+def fwd_ws_raw(p: Problem, q, k, v, o, lse, workspace, stream=None):
+    """attn_train_fwd_ws on caller-owned tensors; workspace None = no split."""
+    ws = ctypes.c_void_p(workspace.data_ptr() if workspace is not None else 0)
+    n = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().attn_train_fwd_ws(ctypes.byref(p), view(q), view(k), view(v), view(o),
+                                    ctypes.c_void_p(lse.data_ptr()), ws, n, _stream(stream)))
 
 
 def bwd_raw(p: Problem, q, k, v, o, dout, lse, dq, dk, dv, workspace, stream=None):
@@ -335,14 +354,19 @@ def _alloc_workspace(nbytes, device):
 
 
 def fwd(q, k, v, mask="causal", ttt_step=0, scale=None, stream=None, out="bf16", window=None,
-        seq_lengths=None, add_mask=None):
-    """Allocates O (bf16 or fp32) and LSE with torch, runs the forward;
-    returns (o, lse)."""
+        seq_lengths=None, add_mask=None, split=True):
+    """Allocates O (bf16 or fp32), LSE and, when the forward splits its key range
+    (attn_train_fwd_workspace_size > 0), its workspace with torch, runs the
+    forward; returns (o, lse).  split=False runs attn_train_fwd (no split)."""
     import torch
     p = problem_for(q, k, mask, ttt_step, scale, out, window, seq_lengths, add_mask)
     o = _alloc(q.shape, _torch_out_dtype(out), q.device)
     lse = _alloc((q.shape[0], q.shape[1], q.shape[2]), torch.float32, q.device)
-    fwd_raw(p, q, k, v, o, lse, stream)
+    n = fwd_workspace_size(p) if split else 0
+    if n > 0:
+        fwd_ws_raw(p, q, k, v, o, lse, _alloc_workspace(n, q.device), stream)
+    else:
+        fwd_raw(p, q, k, v, o, lse, stream)
     return o, lse
 
 

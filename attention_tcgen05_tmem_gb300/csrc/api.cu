@@ -18,6 +18,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "abi_internal.h"
 #include "attn_train.h"
 #include "kernels.h"
 
@@ -329,6 +330,39 @@ attn_status attn_train_workspace_size(const attn_problem* p, size_t* bytes) {
 
 attn_status attn_train_fwd(const attn_problem* p, attn_tensor q, attn_tensor k, attn_tensor v,
                            attn_tensor o, float* lse, void* stream) {
+  return attn_train_fwd_ws(p, q, k, v, o, lse, nullptr, 0, stream);
+}
+
+attn_status attn_train_fwd_workspace_size(const attn_problem* p, size_t* bytes) {
+  attn_status st = check_problem(p);
+  if (st != ATTN_OK) return st;
+  if (bytes == nullptr) return fail(ATTN_ERR_INVALID, "bytes is NULL");
+  *bytes = attn::fwd_split_plan(make_dims(p)).bytes();
+  return ATTN_OK;
+}
+
+attn_status attn_train_fwd_ws(const attn_problem* p, attn_tensor q, attn_tensor k, attn_tensor v,
+                              attn_tensor o, float* lse, void* workspace, size_t ws_bytes,
+                              void* stream) {
+  attn_status st = check_problem(p);
+  if (st != ATTN_OK) return st;
+  const int split = workspace != nullptr ? attn::fwd_split_plan(make_dims(p)).split : 0;
+  return attn::fwd_with_split(p, split, q, k, v, o, lse, workspace, ws_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace attn {
+
+int fwd_split_tiles(const attn_problem* p) { return fwd_split_plan(make_dims(p)).split; }
+
+size_t fwd_split_bytes(const attn_problem* p, int split) {
+  return fwd_split_with(make_dims(p), split).bytes();
+}
+
+attn_status fwd_with_split(const attn_problem* p, int split, attn_tensor q, attn_tensor k,
+                           attn_tensor v, attn_tensor o, float* lse, void* workspace,
+                           size_t ws_bytes, void* stream) {
   attn_status st = check_problem(p);
   if (st != ATTN_OK) return st;
   if ((st = check_tensor(q, p->B, p->Hq, p->Sq, p->D, "q")) != ATTN_OK) return st;
@@ -347,6 +381,23 @@ attn_status attn_train_fwd(const attn_problem* p, attn_tensor q, attn_tensor k, 
   a.v = to_view(v);
   a.o = to_view(o);
   a.lse = lse;
+  a.split = a.nchunk = 0;
+  a.part_o = nullptr;
+  a.part_ml = nullptr;
+  const attn::FwdSplit sp = attn::fwd_split_with(a.d, split);
+  if (sp.split > 0) {
+    // the key range split over several CTAs (small grids): partials in the workspace
+    if (workspace == nullptr) return fail(ATTN_ERR_WORKSPACE, "forward workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+      return fail(ATTN_ERR_ALIGNMENT, "workspace is not 256-byte aligned");
+    if (ws_bytes < sp.bytes())
+      return fail(ATTN_ERR_WORKSPACE, "forward workspace too small: %zu < %zu bytes", ws_bytes,
+                  sp.bytes());
+    a.split = sp.split;
+    a.nchunk = sp.nchunk;
+    a.part_o = static_cast<float*>(workspace);
+    a.part_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + sp.part_o_bytes);
+  }
   if ((st = device_error_word(&a.ctl.err)) != ATTN_OK) return st;
   a.ctl.budget_ns = g_budget_ns.load();
   attn::Maps m;
@@ -354,11 +405,15 @@ attn_status attn_train_fwd(const attn_problem* p, attn_tensor q, attn_tensor k, 
   if ((st = make_map(&m.k, a.k, p->B, p->Hkv, p->Skv, p->D, "k")) != ATTN_OK) return st;
   if ((st = make_map(&m.v, a.v, p->B, p->Hkv, p->Skv, p->D, "v")) != ATTN_OK) return st;
   m.dout = m.q;
-  NvtxRange range("attn_train_fwd");
+  NvtxRange range(a.split > 0 ? "attn_train_fwd:split" : "attn_train_fwd");
   cudaError_t e = attn::launch_fwd(a, m, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return ATTN_OK;
 }
+
+}  // namespace attn
+
+extern "C" {
 
 attn_status attn_train_bwd(const attn_problem* p, attn_tensor q, attn_tensor k, attn_tensor v,
                            attn_tensor o, attn_tensor dout, const float* lse, attn_tensor dq,

@@ -179,33 +179,48 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
 
   const Dims& d = a.d;
-  // ---- work decode: causal/TTT launch the longest query-tile pairs first
+  // ---- work decode: causal/TTT launch the longest query-tile pairs first; with a
+  // key-range split, CTA blockIdx.x takes chunk blockIdx.x % nchunk of its pair
+  const bool split = a.split > 0;
+  const int chunk = split ? (int)(blockIdx.x % (unsigned)a.nchunk) : 0;
+  const int bid = split ? (int)(blockIdx.x / (unsigned)a.nchunk) : (int)blockIdx.x;
   const int n_qp = cdiv(d.Sq, 2 * kBM);
   const int BH = d.B * d.Hq;
   int qp, bh;
   if (d.geom.kind == kMaskFull || d.geom.kind == kMaskWindow) {
-    qp = blockIdx.x % n_qp;
-    bh = blockIdx.x / n_qp;
+    qp = bid % n_qp;
+    bh = bid / n_qp;
   } else {
-    qp = n_qp - 1 - (int)(blockIdx.x / BH);
-    bh = blockIdx.x % BH;
+    qp = n_qp - 1 - bid / BH;
+    bh = bid % BH;
   }
   const int h = bh % d.Hq;
   const int b = bh / d.Hq;
   const int hk = h / d.G;
   const int q0 = qp * 2 * kBM;
   if (*reinterpret_cast<volatile uint32_t*>(a.ctl.err) != 0) {
-    // sticky device error: no work; NaN over this CTA's O and LSE rows
-    const int nrows = min(2 * kBM, d.Sq - q0);
-    poison_rows(a.o, b, h, q0, nrows, D, d.out_f32 != 0);
-    for (int i = threadIdx.x; i < nrows; i += blockDim.x)
-      a.lse[((int64_t)b * d.Hq + h) * d.Sq + q0 + i] = nan_f32();
+    // sticky device error: no work; NaN over this CTA's O and LSE rows (with a
+    // split, the merge pass writes them)
+    if (!split) {
+      const int nrows = min(2 * kBM, d.Sq - q0);
+      poison_rows(a.o, b, h, q0, nrows, D, d.out_f32 != 0);
+      for (int i = threadIdx.x; i < nrows; i += blockDim.x)
+        a.lse[((int64_t)b * d.Hq + h) * d.Sq + q0 + i] = nan_f32();
+    }
     return;
   }
   // this batch entry's geometry; key tiles kt0 .. kt0 + n_kv - 1
   const MaskGeom g = W ? with_len(d.geom, d.seqlens, b) : d.geom;
   int kt0, n_kv;
   sched_kv_tiles<W>(g, q0, 2 * kBM, &kt0, &n_kv);
+  if (split) {
+    // this CTA's chunk of the pair's key tiles; a chunk past the range has no work
+    // (the merge pass derives the pair's chunk count from the same range)
+    const int c0 = chunk * a.split;
+    if (c0 >= n_kv) return;
+    kt0 += c0;
+    n_kv = min(a.split, n_kv - c0);
+  }
 
   const int warp = warp_id();
   const int lane = lane_id();
@@ -532,7 +547,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (ok && n_kv > 0)
       ok = TB ? mbar_wait_warp(&o_last[x], 0u, ctl)
               : mbar_wait_warp(&o_done[x], (uint32_t)(n_kv - 1) & 1u, ctl);
-    if (ok) {
+    if (split) {
+      // partial result of this key chunk (never a TTT mask, n_kv > 0): the
+      // unnormalised O row and the running max and sum it is relative to
+      if (ok) {
+        tc_fence_after();
+        // partial rows are indexed by CTA: (blockIdx.x, row of the pair)
+        const int64_t slot = (int64_t)blockIdx.x * (2 * kBM) + x * kBM + r;
+        float* po = a.part_o + slot * D;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 16) {
+          uint32_t raw[16];
+          tmem_ld16(tO + c0, raw);
+          if (q < d.Sq) {
+#pragma unroll
+            for (int e = 0; e < 16; e += 4)
+              *reinterpret_cast<float4*>(po + c0 + e) =
+                  make_float4(__uint_as_float(raw[e]), __uint_as_float(raw[e + 1]),
+                              __uint_as_float(raw[e + 2]), __uint_as_float(raw[e + 3]));
+          }
+        }
+        if (q < d.Sq) a.part_ml[slot] = make_float2(m_run, l_run);
+      }
+    } else if (ok) {
       if (n_kv > 0) tc_fence_after();
       const bool qin = q < d.Sq;
       // suffix diagonals exist for rows inside the batch entry's key length
@@ -616,6 +653,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
     } else if (q < d.Sq) {
       // a wait of this CTA ran out of budget: NaN instead of a partial result
+      // (with a split, the merge pass sees the error word and writes NaN)
       poison_row(a.o, b, h, q, 0, 16, D, d.out_f32 != 0);
       a.lse[((int64_t)b * d.Hq + h) * d.Sq + q] = nan_f32();
     }
@@ -627,6 +665,70 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+// Merge pass of the split forward.  Chunk c of a row holds O_c (unnormalised),
+// its running max m_c and sum l_c, both in the log2 domain of the scaled scores
+// (P = 2^(c log2(e) s - m_c)); the chunks combine as
+//     m = max_c m_c,  l = sum_c l_c 2^(m_c - m),  O = sum_c O_c 2^(m_c - m) / l,
+// the same log-sum-exp merge as the online softmax, taken in chunk order so the
+// result is bitwise reproducible.  One thread per 16 columns of a query row.
+template <int D, bool W>
+__global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdArgs a) {
+  constexpr int TPR = D / 16;
+  const Dims& d = a.d;
+  const int64_t rows = (int64_t)d.B * d.Hq * d.Sq;
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t row = idx / TPR;
+  if (row >= rows) return;
+  const int c0 = (int)(idx % TPR) * 16;
+  const int q = (int)(row % d.Sq);
+  const int bh = (int)(row / d.Sq);
+  const int h = bh % d.Hq;
+  const int b = bh / d.Hq;
+  const bool f32 = d.out_f32 != 0;
+  if (*reinterpret_cast<volatile uint32_t*>(a.ctl.err) != 0) {
+    // a chunk was skipped or gave up: NaN, not a partial result
+    poison_row(a.o, b, h, q, c0, D, D, f32);
+    if (c0 == 0) a.lse[row] = nan_f32();
+    return;
+  }
+  const int n_qp = cdiv(d.Sq, 2 * kBM);
+  const int qp = q / (2 * kBM), rr = q % (2 * kBM);
+  const MaskGeom g = W ? with_len(d.geom, d.seqlens, b) : d.geom;
+  int kt0, n_kv;
+  sched_kv_tiles<W>(g, qp * 2 * kBM, 2 * kBM, &kt0, &n_kv);
+  const int nc = n_kv > 0 ? cdiv(n_kv, a.split) : 0;
+  // the forward's CTA of (pair, chunk 0): its work decode inverted
+  const int bid = (d.geom.kind == kMaskFull || d.geom.kind == kMaskWindow)
+                      ? bh * n_qp + qp
+                      : (n_qp - 1 - qp) * (d.B * d.Hq) + bh;
+  const int64_t slot0 = (int64_t)bid * a.nchunk;
+  float m = -INFINITY;
+  for (int c = 0; c < nc; ++c) m = fmaxf(m, a.part_ml[(slot0 + c) * (2 * kBM) + rr].x);
+  float l = 0.f;
+  float acc[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+  for (int c = 0; c < nc; ++c) {
+    const int64_t slot = (slot0 + c) * (2 * kBM) + rr;
+    const float2 ml = a.part_ml[slot];
+    if (ml.x == -INFINITY) continue;  // the row sees no key of this chunk
+    const float w = ex2_approx(ml.x - m);
+    l = fmaf(ml.y, w, l);
+    const float4* po = reinterpret_cast<const float4*>(a.part_o + slot * D + c0);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float4 v = po[e];
+      acc[4 * e] = fmaf(v.x, w, acc[4 * e]);
+      acc[4 * e + 1] = fmaf(v.y, w, acc[4 * e + 1]);
+      acc[4 * e + 2] = fmaf(v.z, w, acc[4 * e + 2]);
+      acc[4 * e + 3] = fmaf(v.w, w, acc[4 * e + 3]);
+    }
+  }
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  store16(a.o, b, h, q, c0, acc, inv, f32);
+  if (c0 == 0) a.lse[row] = l > 0.f ? (m + lg2_approx(l)) * 0.69314718055994531f : 0.f;
 }
 
 template <int D, bool W, bool M>
@@ -644,8 +746,12 @@ cudaError_t launch_fwd_dw(const FwdArgs& a, const Maps& m, cudaStream_t s) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   const int n_qp = cdiv(a.d.Sq, 2 * kBM);
-  const unsigned grid = (unsigned)(n_qp * a.d.B * a.d.Hq);
+  const int64_t pairs = (int64_t)n_qp * a.d.B * a.d.Hq;
+  const unsigned grid = (unsigned)(pairs * (a.split > 0 ? a.nchunk : 1));
   kern<<<grid, kFwdThreads, L::ALLOC, s>>>(m.q, m.k, m.v, a);
+  if ((e = cudaGetLastError()) != cudaSuccess || a.split == 0) return e;
+  const int64_t threads = (int64_t)a.d.B * a.d.Hq * a.d.Sq * (D / 16);
+  fwd_merge_kernel<D, W><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -657,6 +763,54 @@ cudaError_t launch_fwd_d(const FwdArgs& a, const Maps& m, cudaStream_t s) {
 }
 
 }  // namespace
+
+// Fewest key tiles a chunk of the split forward takes: a CTA's fixed costs (tensor
+// memory and barrier set-up, the Q load, pipeline fill, the epilogue) are worth
+// several key tiles.
+constexpr int kMinSplitTiles = 4;
+
+FwdSplit fwd_split_plan(const Dims& d) {
+  constexpr int num_sms = kPlanSMs;
+  FwdSplit sp;
+  if (d.geom.ttt > 0) return sp;  // TTT merges its diagonals per CTA
+  const int n_qp = cdiv(d.Sq, 2 * kBM);
+  const int64_t pairs = (int64_t)n_qp * d.B * d.Hq;
+  if (pairs >= num_sms) return sp;  // one CTA per pair already fills a wave
+  // key tiles of every pair (the bound without per-batch key lengths, which only
+  // shorten rows), and the whole launch's
+  int64_t total = 0;
+  int nmax = 0;
+  for (int qp = 0; qp < n_qp; ++qp) {
+    int kt0, n;
+    sched_kv_tiles<true>(d.geom, qp * 2 * kBM, 2 * kBM, &kt0, &n);
+    total += n;
+    if (n > nmax) nmax = n;
+  }
+  total *= (int64_t)d.B * d.Hq;
+  // about two chunks per SM, each at least kMinSplitTiles key tiles
+  int64_t split = (total + 2 * num_sms - 1) / (2 * num_sms);
+  if (split < kMinSplitTiles) split = kMinSplitTiles;
+  if (split >= nmax) return sp;
+  return fwd_split_with(d, (int)split);
+}
+
+FwdSplit fwd_split_with(const Dims& d, int split) {
+  FwdSplit sp;
+  if (split <= 0 || d.geom.ttt > 0) return sp;
+  const int n_qp = cdiv(d.Sq, 2 * kBM);
+  int nmax = 0;
+  for (int qp = 0; qp < n_qp; ++qp) {
+    int kt0, n;
+    sched_kv_tiles<true>(d.geom, qp * 2 * kBM, 2 * kBM, &kt0, &n);
+    if (n > nmax) nmax = n;
+  }
+  sp.split = split;
+  sp.nchunk = nmax > 0 ? cdiv(nmax, split) : 1;
+  const int64_t slots = (int64_t)n_qp * d.B * d.Hq * sp.nchunk * 2 * kBM;
+  sp.part_o_bytes = ((size_t)slots * d.D * 4 + 255) & ~(size_t)255;
+  sp.part_ml_bytes = ((size_t)slots * 8 + 255) & ~(size_t)255;
+  return sp;
+}
 
 cudaError_t launch_fwd(const FwdArgs& a, const Maps& m, cudaStream_t s) {
   switch (a.d.D) {

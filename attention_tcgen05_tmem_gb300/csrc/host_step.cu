@@ -23,6 +23,7 @@
 #include <cstdio>
 #include <new>
 
+#include "abi_internal.h"
 #include "attn_train.h"
 #include "kernels.h"
 
@@ -55,6 +56,7 @@ struct Plan {
   // offsets inside one slot and its size
   size_t s_q = 0, s_k = 0, s_v = 0, s_do = 0, s_o = 0, s_lse = 0, s_dq = 0, s_dk = 0, s_dv = 0;
   size_t slot = 0;
+  int fsplit = 0;  // the whole problem's forward split (chunk length in key tiles)
   // arena: static[2] (key lengths, mask) | chunk workspace | slot[2]
   size_t lens_off = 0, mask_off = 0, mask_bytes = 0, stat = 0, ws_off = 0, ws = 0, slot_off = 0;
   size_t total = 0;
@@ -124,8 +126,15 @@ attn_status make_plan(const attn_problem* p, int kv_heads_per_chunk, Plan* pl) {
   }
   P.stat = o;
   o = 2 * P.stat;
+  // one workspace region serves the forward's key-range split and the backward:
+  // the forward's merge pass has consumed its partials before the backward runs.
+  // Every chunk splits its forward like the whole problem would, so that the
+  // chunked results equal the whole problem's bit for bit.
   attn_problem cp = chunk_problem(dp, P.NB, P.U, dp.seq_lengths, dp.add_mask);
   if ((st = attn_train_workspace_size(&cp, &P.ws)) != ATTN_OK) return st;
+  P.fsplit = attn::fwd_split_tiles(&dp);
+  const size_t fws = attn::fwd_split_bytes(&cp, P.fsplit);
+  if (fws > P.ws) P.ws = fws;
   P.ws_off = o;
   o += up(P.ws);
   P.slot_off = o;
@@ -280,7 +289,8 @@ attn_status attn_host_session_s::enqueue_step(const attn_host_io* io, cudaStream
       void* ws = arena + pl.ws_off;
       STEP_CUDA(cudaStreamWaitEvent(cs, qkv[s], 0), "stream wait");
       if (chunk >= 2) STEP_CUDA(cudaStreamWaitEvent(cs, outd[s], 0), "stream wait");
-      if ((st = attn_train_fwd(&sp, q, k, v, o, lse, cs)) != ATTN_OK) return st;
+      if ((st = attn::fwd_with_split(&sp, pl.fsplit, q, k, v, o, lse, ws, pl.ws, cs)) != ATTN_OK)
+        return st;
       STEP_CUDA(cudaEventRecord(fwd[s], cs), "event record");
       STEP_CUDA(cudaStreamWaitEvent(cs, inp[s], 0), "stream wait");
       if ((st = attn_train_bwd_passes(&sp, ATTN_BWD_PREP | ATTN_BWD_DQ, q, k, v, o, dout, lse, dqv,

@@ -44,7 +44,34 @@ struct FwdArgs {
   View q, k, v, o;
   float* lse;  // [B, Hq, Sq]
   Ctl ctl;
+  // Split over key tiles (see FwdSplit): split = key tiles per chunk (0: one CTA
+  // per query-tile pair, writing O and LSE itself); nchunk = chunk slots per pair;
+  // part_o [B*Hq][n_qp][nchunk][2*kBM][D] and part_ml [same slots][2*kBM] (running
+  // max and sum) in the workspace.
+  int split, nchunk;
+  float* part_o;
+  float2* part_ml;
 };
+
+// The forward's key-range split for grids that would leave most SMs idle: each
+// query-tile pair's key tiles are cut into chunks of `split` tiles, one CTA per
+// (pair, chunk), and a merge pass combines the chunks' partial results in chunk
+// order.  split = 0: no split.
+struct FwdSplit {
+  int split = 0, nchunk = 0;
+  size_t part_o_bytes = 0, part_ml_bytes = 0;
+  size_t bytes() const { return part_o_bytes + part_ml_bytes; }
+};
+// Planned for kPlanSMs multiprocessors (a GB300's count): the plan only changes
+// scheduling, so it is a pure function of the problem (workspace sizes can be
+// computed without a device, and a device with another count still gets exact
+// results).
+constexpr int kPlanSMs = 152;
+FwdSplit fwd_split_plan(const Dims& d);
+// The layout of a split into chunks of `split` key tiles for this problem (split
+// <= 0 or a TTT mask: none); slices of a larger problem use the larger problem's
+// chunk length, so that their results equal its results bit for bit.
+FwdSplit fwd_split_with(const Dims& d, int split);
 
 struct BwdArgs {
   Dims d;

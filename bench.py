@@ -248,6 +248,9 @@ class Case:
         self.dk = torch.empty(self.k.shape, dtype=odt, device=dev)
         self.dv = torch.empty(self.v.shape, dtype=odt, device=dev)
         self.ws = torch.empty(binding.workspace_size(self.p), dtype=torch.uint8, device=dev)
+        # the forward's key-range split (small grids) and its workspace
+        nfw = binding.fwd_workspace_size(self.p)
+        self.fws = torch.empty(nfw, dtype=torch.uint8, device=dev) if nfw else None
         has_ttt = w.mask == "ttt" and w.ttt_step > 0
         self.passes = [("bwd_prep", binding.BWD_PREP), ("bwd_dkdv", binding.BWD_DKDV),
                        ("bwd_dq", binding.BWD_DQ)]
@@ -257,13 +260,13 @@ class Case:
         # kernels launched per step: a TTT forward adds its diagonal-scores pre-pass
         # when the t scores fit into an output row (t * 4 <= D * output element size)
         scores = has_ttt and w.ttt_step * 4 <= w.D * (4 if out == "fp32" else 2)
-        self.launches = len(self.names) + (1 if scores else 0)
+        self.launches = len(self.names) + (1 if scores else 0) + (1 if self.fws is not None else 0)
 
     def step(self, stream, evs=None):
         b = self.b
         if evs:
             evs[0].record(stream)
-        b.fwd_raw(self.p, self.q, self.k, self.v, self.o, self.lse, stream.cuda_stream)
+        b.fwd_ws_raw(self.p, self.q, self.k, self.v, self.o, self.lse, self.fws, stream.cuda_stream)
         if evs:
             evs[1].record(stream)
         for i, (_, m) in enumerate(self.passes):

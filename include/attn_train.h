@@ -152,9 +152,32 @@ attn_status attn_train_workspace_size(const attn_problem* p, size_t* bytes);
 
 /* Forward.  Inputs q [B,Hq,Sq,D], k and v [B,Hkv,Skv,D]; outputs o
  * [B,Hq,Sq,D] (bf16) and lse [B,Hq,Sq] (fp32, natural log).  Kernels: one
- * tcgen05 kernel (two 128-row query tiles per CTA). */
+ * tcgen05 kernel (two 128-row query tiles per CTA).  Same as
+ * attn_train_fwd_ws with no workspace. */
 attn_status attn_train_fwd(const attn_problem* p, attn_tensor q, attn_tensor k, attn_tensor v,
                            attn_tensor o, float* lse, void* stream);
+
+/* Bytes of device workspace attn_train_fwd_ws uses for this problem; 0 when
+ * the forward does not split.  The split (a scheduling choice; the pages'
+ * kernels launch one program per query block): when one CTA per pair of query
+ * tiles would not fill a GB300's 152 multiprocessors (few batch
+ * entries and heads, long rows), each pair's key tiles are cut into chunks, one
+ * CTA per chunk writes its unnormalised partial O rows and their running max
+ * and sum (fp32) into the workspace, and a merge pass combines the chunks in a
+ * fixed order by log-sum-exp (CS336 README, "Flash Attention (Triton)": the
+ * running max and normaliser of the online softmax) -- the same result up to
+ * rounding, bitwise reproducible.  Never for the TTT mask.  A pure function of
+ * the problem (no device needed). */
+attn_status attn_train_fwd_workspace_size(const attn_problem* p, size_t* bytes);
+
+/* Forward with a workspace: workspace NULL runs attn_train_fwd; otherwise it is
+ * a device buffer of at least attn_train_fwd_workspace_size bytes (256-byte
+ * aligned, contents ignored, ATTN_ERR_WORKSPACE when too small) and the forward
+ * splits its key range when that size is non-zero.  Kernels: the tcgen05
+ * forward and, when split, the merge pass. */
+attn_status attn_train_fwd_ws(const attn_problem* p, attn_tensor q, attn_tensor k, attn_tensor v,
+                              attn_tensor o, float* lse, void* workspace, size_t ws_bytes,
+                              void* stream);
 
 /* Backward.  Inputs q, k, v, o (the forward's output), dout [B,Hq,Sq,D] and
  * lse (the forward's); outputs dq [B,Hq,Sq,D], dk and dv [B,Hkv,Skv,D],

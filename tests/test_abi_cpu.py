@@ -257,3 +257,40 @@ def test_binding_raises_without_library(tmp_path):
             binding.load(str(tmp_path / "missing.so"))
         finally:
             binding._lib = binding._lib_saved
+
+
+def test_forward_split_workspace_sizes():
+    """attn_train_fwd_workspace_size is a pure function of the problem: non-zero
+    for small grids with long rows (the single-head sweep at S >= 1024), zero
+    for TTT masks and for grids that fill a GB300 (the long GQA workload)."""
+    from attention_tcgen05_tmem_gb300 import build as lib_build
+    lib_build.build()
+    from attention_tcgen05_tmem_gb300 import synth
+
+    def size(w):
+        p = binding.problem(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.mask, w.ttt_step, 0.0, "fp32")
+        return binding.fwd_workspace_size(p)
+
+    sweep = {w.name: size(w) for w in synth.SWEEP}
+    assert all(v == 0 for n, v in sweep.items() if "_S256_" in n)
+    assert all(v > 0 for n, v in sweep.items() if "_S256_" not in n)
+    # S = 4096, D = 64: 16 pairs x 8 heads, 4 chunks each of 256 rows x (64 + 2) floats
+    assert size(synth.by_name("sweep_causal_B8_H1_S4096_D64")) == 16 * 8 * 4 * 256 * 66 * 4
+    assert size(synth.LONG_GQA) == 0 and size(synth.DIT_CROSS) == 0
+    assert all(size(w) == 0 for w in synth.TTT_STEPS)
+
+
+def test_forward_split_workspace_checks():
+    """A too-short or misaligned forward workspace is refused on the host."""
+    from attention_tcgen05_tmem_gb300 import build as lib_build
+    lib_build.build()
+    lib = binding.load()
+    p = binding.problem(1, 1, 1, 4096, 4096, 64, "causal", 0, 0.0, "fp32")
+    n = binding.fwd_workspace_size(p)
+    t = binding.Tensor(0x1000, 1 << 24, 1 << 22, 64)
+    lse = ctypes.c_void_p(0x2000)
+    st = lib.attn_train_fwd_ws(ctypes.byref(p), t, t, t, t, lse, ctypes.c_void_p(0x10000), n - 256,
+                               None)
+    assert st == 4 and b"too small" in lib.attn_train_last_error()
+    st = lib.attn_train_fwd_ws(ctypes.byref(p), t, t, t, t, lse, ctypes.c_void_p(0x10010), n, None)
+    assert st == 3 and b"256-byte" in lib.attn_train_last_error()
