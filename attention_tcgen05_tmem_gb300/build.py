@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libattn_train.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
-SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "aux.cu", "loss.cu", "host_step.cu"]
+SOURCES = ["api.cu", "fwd.cu", "fwd_split.cu", "bwd.cu", "aux.cu", "loss.cu", "host_step.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]

@@ -110,6 +110,8 @@ cudaError_t launch_logsoftmax_loss_fwd(const LossArgs& a, cudaStream_t s);
 cudaError_t launch_logsoftmax_loss_bwd(const LossArgs& a, cudaStream_t s);
 
 cudaError_t launch_fwd(const FwdArgs& a, const Maps& m, cudaStream_t s);
+// The split forward (a.split > 0) and its merge pass (fwd_split.cu).
+cudaError_t launch_fwd_split(const FwdArgs& a, const Maps& m, cudaStream_t s);
 // passes: mask of 1 = Delta prep, 2 = dK/dV, 4 = dQ, 8 = TTT suffix keys
 cudaError_t launch_bwd(const BwdArgs& a, const Maps& m, unsigned passes, cudaStream_t s);
 cudaError_t launch_mask_pattern(const Dims& d, uint8_t* bits, uint8_t* tiles, cudaStream_t s);

@@ -294,3 +294,21 @@ def test_forward_split_workspace_checks():
     assert st == 4 and b"too small" in lib.attn_train_last_error()
     st = lib.attn_train_fwd_ws(ctypes.byref(p), t, t, t, t, lse, ctypes.c_void_p(0x10010), n, None)
     assert st == 3 and b"256-byte" in lib.attn_train_last_error()
+
+
+def test_forward_split_workspace_is_bounded_independently_of_s():
+    """The split plans about two chunks per SM, so whatever the sequence length
+    its partial results fill at most a few hundred 256-row slots (the bound
+    below is 768 slots of D + 2 floats per row: at most 101 MB at D = 128)."""
+    from attention_tcgen05_tmem_gb300 import build as lib_build
+    lib_build.build()
+    worst = 0
+    for mask in ("causal", "full"):
+        for D in (16, 64, 128):
+            for H in (1, 4, 16, 64):
+                for S in (512, 4096, 16384, 131072):
+                    for Skv in ((S,) if mask == "causal" else (S, 1 << 20)):
+                        p = binding.problem(1, H, H, S, Skv, D, mask, 0, 0.0, "fp32")
+                        n = binding.fwd_workspace_size(p)
+                        worst = max(worst, n / (256 * (D + 2) * 4))
+    assert 0 < worst <= 768

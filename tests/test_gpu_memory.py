@@ -2,7 +2,9 @@
 backward needs exactly the backward workspace (the fp32 Delta row statistic,
 B*Hq*Sq*4 bytes); the S x S score matrix is never stored (SpecForge post:
 Flex attention's memory saving in long-context training; CS336 README:
-naive attention's O(N^2) score matrix is what flash attention avoids)."""
+naive attention's O(N^2) score matrix is what flash attention avoids).  The
+forward here runs unsplit; the key-range split used for grids under one wave
+adds a workspace bounded independently of S (tests/test_abi_cpu.py)."""
 import pytest
 import torch
 
@@ -22,7 +24,7 @@ def test_extra_memory_is_the_workspace_and_linear_in_s():
         torch.cuda.empty_cache()
         torch.cuda.reset_peak_memory_stats()
         base = torch.cuda.memory_allocated()
-        o, lse = binding.fwd(q, k, v, "causal", out="fp32")
+        o, lse = binding.fwd(q, k, v, "causal", out="fp32", split=False)
         dq, dk, dv = binding.bwd(q, k, v, o, lse, do, "causal")
         torch.cuda.synchronize()
         binding.device_status()
