@@ -5,6 +5,8 @@ Flex attention's memory saving in long-context training; CS336 README:
 naive attention's O(N^2) score matrix is what flash attention avoids).  The
 forward here runs unsplit; the key-range split used for grids under one wave
 adds a workspace bounded independently of S (tests/test_abi_cpu.py)."""
+import gc
+
 import pytest
 import torch
 
@@ -20,6 +22,9 @@ def test_extra_memory_is_the_workspace_and_linear_in_s():
         w = synth.Workload(f"mem_S{S}", 1, 8, 1, S, S, 128, "causal", 0, 31)
         x = synth.make_inputs(w)
         q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
+        # tensors of earlier tests still awaiting collection must not be freed while
+        # this one measures
+        gc.collect()
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
         torch.cuda.reset_peak_memory_stats()

@@ -19,7 +19,7 @@ CASES = [
     W("split_causal_d64", 1, 1, 1, 4096, 4096, 64, "causal", seed=51),
     W("split_causal_gqa_d128", 1, 4, 2, 2000, 2000, 128, "causal", seed=52),
     W("split_full_cross_d128", 1, 2, 1, 300, 5000, 128, "full", seed=53),
-    W("split_window_d32", 1, 2, 1, 2000, 2000, 32, "window", seed=54, window=(700, 100)),
+    W("split_window_d32", 1, 2, 1, 2000, 2000, 32, "window", seed=54, window=(1500, 200)),
     W("split_varlen_d16", 2, 2, 2, 1500, 1500, 16, "causal", seed=55, seq_lengths=(1500, 0)),
     W("split_addmask_d64", 1, 1, 1, 1300, 1300, 64, "full", seed=56, add_mask=True),
 ]
