@@ -70,6 +70,9 @@ def parse_args():
     ap.add_argument("--repeats", type=int, default=3,
                     help="timed regions per workload (interleaved across workloads); the "
                          "line reports the median region and the spread")
+    ap.add_argument("--eager", action="store_true",
+                    help="time eager launches (CUDA events between kernels) instead of a "
+                         "CUDA-graph replay of each step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-chunk", type=int, default=0,
@@ -262,18 +265,80 @@ class Case:
         scores = has_ttt and w.ttt_step * 4 <= w.D * (4 if out == "fp32" else 2)
         self.launches = len(self.names) + (1 if scores else 0) + (1 if self.fws is not None else 0)
 
-    def step(self, stream, evs=None):
+    def step(self, stream, evs=None, mark=None):
+        """One forward + backward on `stream`; timing marks between the kernels:
+        torch events (evs) or a callable mark(i) (events inside a CUDA graph)."""
         b = self.b
-        if evs:
-            evs[0].record(stream)
+        if mark is None and evs:
+            mark = lambda i: evs[i].record(stream)  # noqa: E731
+        if mark:
+            mark(0)
         b.fwd_ws_raw(self.p, self.q, self.k, self.v, self.o, self.lse, self.fws, stream.cuda_stream)
-        if evs:
-            evs[1].record(stream)
+        if mark:
+            mark(1)
         for i, (_, m) in enumerate(self.passes):
             b.bwd_passes_raw(self.p, m, self.q, self.k, self.v, self.o, self.do, self.lse, self.dq,
                              self.dk, self.dv, self.ws, stream.cuda_stream)
-            if evs:
-                evs[2 + i].record(stream)
+            if mark:
+                mark(2 + i)
+
+
+def cuda_runtime():
+    """The CUDA runtime library the attention library loaded (so that events
+    and streams are handled by the same runtime instance), via ctypes."""
+    import ctypes
+    path = None
+    try:
+        with open("/proc/self/maps") as f:
+            for line in f:
+                if "libcudart.so" in line:
+                    path = line.split()[-1]
+                    break
+    except OSError:
+        pass
+    rt = ctypes.CDLL(path or "libcudart.so.13")
+    vp = ctypes.c_void_p
+    rt.cudaEventCreate.argtypes = [ctypes.POINTER(vp)]
+    rt.cudaEventRecordWithFlags.argtypes = [vp, vp, ctypes.c_uint]
+    rt.cudaEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), vp, vp]
+    rt.cudaEventDestroy.argtypes = [vp]
+    return rt
+
+
+class GraphEvents:
+    """Timing events stamped by every replay of a CUDA graph: event-record
+    nodes captured with cudaEventRecordExternal, so per-kernel times exclude
+    the host's launch gaps."""
+
+    EXTERNAL = 0x1
+
+    def __init__(self, rt, n):
+        import ctypes
+        self.rt, self.ev = rt, [ctypes.c_void_p() for _ in range(n)]
+        for e in self.ev:
+            self._check(rt.cudaEventCreate(ctypes.byref(e)), "cudaEventCreate")
+
+    @staticmethod
+    def _check(err, what):
+        if err != 0:
+            raise RuntimeError(f"{what} failed ({err})")
+
+    def record(self, i, stream_handle):
+        import ctypes
+        self._check(self.rt.cudaEventRecordWithFlags(self.ev[i], ctypes.c_void_p(stream_handle),
+                                                     self.EXTERNAL), "cudaEventRecordWithFlags")
+
+    def elapsed_ms(self, i, j):
+        import ctypes
+        ms = ctypes.c_float()
+        self._check(self.rt.cudaEventElapsedTime(ctypes.byref(ms), self.ev[i], self.ev[j]),
+                    "cudaEventElapsedTime")
+        return float(ms.value)
+
+    def close(self):
+        for e in self.ev:
+            self.rt.cudaEventDestroy(e)
+        self.ev = []
 
 
 class Runner:
@@ -304,12 +369,59 @@ class Runner:
                 c.step(self.stream)
         torch.cuda.synchronize(dev)
         binding.device_status()
+        self.graph, self.gevs, self.timing = None, None, "eager, CUDA events between kernels"
+        if not args.eager:
+            self._capture()
+
+    def _capture(self):
+        """The step as one CUDA graph, with timing events recorded inside it (small
+        problems are otherwise timed with the host's launch gaps between kernels)."""
+        import torch
+        try:
+            rt = cuda_runtime()
+            self.gevs = [GraphEvents(rt, len(c.names) + 1) for c in self.cases]
+            g = torch.cuda.CUDAGraph()
+            s = torch.cuda.Stream(self.dev)
+            s.wait_stream(self.stream)
+            with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
+                for c, gev in zip(self.cases, self.gevs):
+                    c.step(s, mark=lambda i, gev=gev: gev.record(i, s.cuda_stream))
+            for _ in range(2):
+                g.replay()
+            torch.cuda.synchronize(self.dev)
+            self.binding.device_status()
+            self.graph = g
+            self.timing = "CUDA graph replay per step, events recorded inside the graph"
+        except Exception as ex:  # noqa: BLE001 -- eager timing remains valid
+            for gev in self.gevs or []:
+                gev.close()
+            self.graph, self.gevs = None, None
+            self.timing = f"eager, CUDA events between kernels (graph capture failed: {ex!r})"[:200]
 
     def timed(self):
         """K steps, L2 flushed between steps outside the events; returns the
         summed event time of the steps, per-kernel sums and the clocks seen."""
         import torch
         K, dev, dist = self.args.steps, self.dev, self.dist
+        per_kernel, total_ms = {}, 0.0
+        if self.graph is not None:
+            if dist:
+                dist.barrier()
+            torch.cuda.synchronize(dev)
+            with ClockSampler(gpu_index_for(self.local_rank)) as clk:
+                for i in range(K):
+                    self.flush.zero_()  # evict L2 between steps (outside the events)
+                    self.graph.replay()
+                    torch.cuda.synchronize(dev)
+                    for c, gev in zip(self.cases, self.gevs):
+                        total_ms += gev.elapsed_ms(0, len(c.names))
+                        for j, n in enumerate(c.names):
+                            per_kernel[n] = per_kernel.get(n, 0.0) + gev.elapsed_ms(j, j + 1)
+            if dist:
+                dist.barrier()
+            self.binding.device_status()
+            total_ms, = max_over_ranks([total_ms], dist, dev)
+            return {"total_ms": total_ms, "per_kernel_ms": per_kernel, "clocks": clk.summary()}
         evsets = [[[torch.cuda.Event(enable_timing=True) for _ in range(len(c.names) + 1)]
                    for c in self.cases] for _ in range(K)]
         if dist:
@@ -324,7 +436,6 @@ class Runner:
         if dist:
             dist.barrier()
         self.binding.device_status()
-        per_kernel, total_ms = {}, 0.0
         for i in range(K):
             for c, evs in zip(self.cases, evsets[i]):
                 total_ms += evs[0].elapsed_time(evs[-1])
@@ -391,6 +502,9 @@ class Runner:
         for sess, _ in self.hosts or []:
             sess.close()
         self.hosts = None
+        for gev in self.gevs or []:
+            gev.close()
+        self.graph, self.gevs = None, None
 
 
 def median_run(runs):
@@ -806,7 +920,7 @@ def main():
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": n_gpus, "steps": K,
             "warmup": args.warmup, "ms_per_step": r["total_ms"] / K, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": describe(name, ws, args.out, n_gpus),
+            "config": dict(describe(name, ws, args.out, n_gpus), timing=runners[name].timing),
             "pct_of_peak": {"bf16_burst": value / n_gpus / peak_burst,
                             "bf16_sustained": value / n_gpus / peak_sus, "source": peak_src,
                             **theoretical_peak(value / n_gpus, clocks, local_rank)},
