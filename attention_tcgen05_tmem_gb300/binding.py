@@ -18,13 +18,15 @@ LIB_PATH = os.path.join(HERE, "libattn_train.so")
 
 MASKS = {"full": 0, "causal": 1, "ttt": 2, "window": 3}
 STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_ALIGNMENT",
-          4: "ATTN_ERR_WORKSPACE", 5: "ATTN_ERR_CUDA", 6: "ATTN_ERR_DEVICE_TIMEOUT"}
+          4: "ATTN_ERR_WORKSPACE", 5: "ATTN_ERR_CUDA", 6: "ATTN_ERR_DEVICE_TIMEOUT",
+          7: "ATTN_ERR_DEVICE_CHECK"}
 
 # Entry points of include/attn_train.h (checked against the header by the tests).
 EXPORTS = ("attn_train_supports", "attn_train_workspace_size", "attn_train_fwd",
            "attn_train_fwd_workspace_size", "attn_train_fwd_ws", "attn_train_bwd",
            "attn_train_bwd_passes", "attn_train_bwd_noalloc", "attn_train_last_error", "attn_train_device_status", "attn_train_set_wait_budget_ns",
            "attn_train_mask_pattern", "attn_train_probe_mma", "attn_train_selftest_wait_timeout",
+           "attn_train_selftest_debug_check",
            "attn_train_logsoftmax_loss_fwd", "attn_train_logsoftmax_loss_bwd",
            "attn_train_step_host_arena_size", "attn_train_step_host",
            "attn_train_host_session_create", "attn_train_host_session_step",
@@ -94,6 +96,7 @@ def load(path: str = LIB_PATH):
             "attn_train_mask_pattern": (st, [P, vp, vp, vp]),
             "attn_train_probe_mma": (st, [ctypes.c_int, ctypes.c_int, vp, vp, vp, vp]),
             "attn_train_selftest_wait_timeout": (st, [vp]),
+            "attn_train_selftest_debug_check": (st, [vp]),
             "attn_train_logsoftmax_loss_fwd": (st, [ctypes.c_int64, ctypes.c_int64, vp,
                                                     ctypes.c_int64, vp, ctypes.c_int64, vp,
                                                     vp, vp, vp, vp, vp]),
@@ -420,6 +423,12 @@ def probe_mma(mode: int, a, b, D: int):
 
 def selftest_wait_timeout():
     _check(load().attn_train_selftest_wait_timeout(_stream(None)))
+
+
+def selftest_debug_check():
+    """A device-side check that fails on purpose (libraries built with
+    -DATTN_DEBUG; AttnError ATTN_ERR_UNSUPPORTED otherwise)."""
+    _check(load().attn_train_selftest_debug_check(_stream(None)))
 
 
 # ------------------------------------------------- soft-target log-softmax loss

@@ -45,6 +45,7 @@ def up_to_date() -> bool:
 
 
 TRACE_LIB = os.path.join(HERE, "libattn_train_trace.so")
+DEBUG_LIB = os.path.join(HERE, "libattn_train_debug.so")
 
 
 def build_trace(force: bool = False) -> str:
@@ -53,18 +54,27 @@ def build_trace(force: bool = False) -> str:
     return build(force=force, trace=True)
 
 
+def build_debug(force: bool = False) -> str:
+    """Same library built with -DATTN_DEBUG (device-side checks of tile
+    coordinates, work items and workspace slots), as libattn_train_debug.so:
+    a bring-up aid, loaded explicitly (binding.load(DEBUG_LIB))."""
+    return build(force=force, debug=True)
+
+
 def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False,
-          trace: bool = False) -> str:
-    lib = TRACE_LIB if trace else LIB
+          trace: bool = False, debug: bool = False) -> str:
+    lib = TRACE_LIB if trace else DEBUG_LIB if debug else LIB
     if not force and os.path.exists(lib) and all(
             os.path.getmtime(f) <= os.path.getmtime(lib) for f in _deps()):
         return lib
-    bdir = BUILD_DIR + ("_trace" if trace else "")
+    bdir = BUILD_DIR + ("_trace" if trace else "_debug" if debug else "")
     os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_v else []
     if trace:
         extra.append("-DATTN_TRACE")
+    if debug:
+        extra.append("-DATTN_DEBUG")
 
     def compile_one(src: str) -> tuple[str, str]:
         obj = os.path.join(bdir, src.replace(".cu", ".o"))

@@ -21,6 +21,7 @@
 #include "abi_internal.h"
 #include "attn_train.h"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace {
 
@@ -595,6 +596,9 @@ attn_status attn_train_device_status(void* stream) {
     const uint32_t zero = 0;
     e = cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+    if ((word & 0xffu) == attn::kErrDebugCheck)
+      return fail(ATTN_ERR_DEVICE_CHECK, "a device-side check of the ATTN_DEBUG build failed "
+                  "at site %u", word >> 8);
     return fail(ATTN_ERR_DEVICE_TIMEOUT, "a device-side wait ran out of budget (code %u)", word);
   }
   return ATTN_OK;
@@ -634,6 +638,18 @@ attn_status attn_train_probe_mma(int mode, int D, const void* a, const void* b, 
   if ((st = make_map(&tb, vb, 1, 1, 128, D, "probe b")) != ATTN_OK) return st;
   cudaError_t e = attn::launch_probe(mode, D, ta, tb, a, c, ctl, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "probe launch");
+  return ATTN_OK;
+}
+
+attn_status attn_train_selftest_debug_check(void* stream) {
+  if (!attn::debug_checks_built())
+    return fail(ATTN_ERR_UNSUPPORTED, "this library was built without ATTN_DEBUG");
+  Ctl ctl;
+  attn_status st = device_error_word(&ctl.err);
+  if (st != ATTN_OK) return st;
+  ctl.budget_ns = g_budget_ns.load();
+  cudaError_t e = attn::launch_selftest_check(ctl, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "selftest launch");
   return ATTN_OK;
 }
 

@@ -151,6 +151,12 @@ __global__ void selftest_wait_kernel(Ctl cc) {
   mbar_wait_warp(&bar, 0, ctl);
 }
 
+// A device check that fails on purpose (ATTN_DEBUG builds; no memory access).
+__global__ void selftest_check_kernel(Ctl cc) {
+  (void)ATTN_CHECK(cc.err, threadIdx.x == 1u << 30, 99);
+  (void)cc;
+}
+
 template <int D>
 cudaError_t launch_probe_d(int mode, const CUtensorMap& ta, const CUtensorMap& tb,
                            const void* a_global, float* c, Ctl ctl, cudaStream_t s) {
@@ -182,6 +188,19 @@ cudaError_t launch_probe(int mode, int D, const CUtensorMap& ta, const CUtensorM
     case 128: return launch_probe_d<128>(mode, ta, tb, a_global, c, ctl, s);
     default: return cudaErrorInvalidValue;
   }
+}
+
+bool debug_checks_built() {
+#ifdef ATTN_DEBUG
+  return true;
+#else
+  return false;
+#endif
+}
+
+cudaError_t launch_selftest_check(Ctl ctl, cudaStream_t s) {
+  selftest_check_kernel<<<1, 32, 0, s>>>(ctl);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_selftest_wait(Ctl ctl, cudaStream_t s) {

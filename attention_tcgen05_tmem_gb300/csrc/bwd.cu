@@ -266,6 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     poison_key_rows(a, b, hk, k0, min(kBN, d.geom.kv_main - k0), D);
     return;
   }
+  // the work item must exist (ATTN_DEBUG)
+  if (!ATTN_CHECK(a.ctl.err, k0 < d.geom.kv_main && hk < d.Hkv && b < d.B, 7)) return;
   // this batch entry's geometry; query tiles qt_begin .. qt_begin + n_q - 1 see the key tile
   const MaskGeom g = W ? with_len(d.geom, d.seqlens, b) : d.geom;
   int qt_begin, n_q;
@@ -313,8 +315,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tq);
         tma_prefetch_desc(&tdo);
         mbar_arrive_expect_tx(kv_full, 2 * TG::TILE_BYTES);
-        TG::load(smem + L::K_OFF, &tk, kv_full, k0, hk, b);
-        TG::load(smem + L::V_OFF, &tv, kv_full, k0, hk, b);
+        TG::load(smem + L::K_OFF, &tk, kv_full, k0, hk, b, d.geom.kv_main, d.Hkv, d.B,
+                 a.ctl.err, 5);
+        TG::load(smem + L::V_OFF, &tv, kv_full, k0, hk, b, d.geom.kv_main, d.Hkv, d.B,
+                 a.ctl.err, 5);
       }
       int issued = 0;
       for (int it = 0; it < N; ++it) {
@@ -328,8 +332,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           mbar_arrive_expect_tx(&qdo_full[s], 2 * TG::TILE_BYTES);
           uint8_t* dst = smem + L::ST_OFF + s * L::STAGE_BYTES;
-          TG::load(dst, &tq, &qdo_full[s], q0, h, b);
-          TG::load(dst + TG::TILE_BYTES, &tdo, &qdo_full[s], q0, h, b);
+          TG::load(dst, &tq, &qdo_full[s], q0, h, b, d.Sq, d.Hq, d.B, a.ctl.err, 6);
+          TG::load(dst + TG::TILE_BYTES, &tdo, &qdo_full[s], q0, h, b, d.Sq, d.Hq, d.B,
+                   a.ctl.err, 6);
         }
         float* st = stats + s * 256;
         const int64_t rbase = ((int64_t)b * d.Hq + h) * d.Sq;
@@ -651,6 +656,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     poison_rows(a.dq, b, h, q0, min(kBM, d.Sq - q0), D, d.out_f32 != 0);
     return;
   }
+  // the work item must exist (ATTN_DEBUG)
+  if (!ATTN_CHECK(a.ctl.err, q0 < d.Sq && h < d.Hq && b < d.B, 10)) return;
   // this batch entry's geometry; key tiles kt0 .. kt0 + n_kv - 1
   const MaskGeom g = W ? with_len(d.geom, d.seqlens, b) : d.geom;
   int kt0, n_kv;
@@ -696,19 +703,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
       mbar_arrive_expect_tx(qdo_full, 2 * TG::TILE_BYTES);
-      TG::load(smem + L::Q_OFF, &tq, qdo_full, q0, h, b);
-      TG::load(smem + L::DO_OFF, &tdo, qdo_full, q0, h, b);
+      TG::load(smem + L::Q_OFF, &tq, qdo_full, q0, h, b, d.Sq, d.Hq, d.B, a.ctl.err, 8);
+      TG::load(smem + L::DO_OFF, &tdo, qdo_full, q0, h, b, d.Sq, d.Hq, d.B, a.ctl.err, 8);
       int k_issued = 0, v_issued = 0;
       for (int j = 0; j < n_kv; ++j) {
         if (!mbar_wait(&k_empty[j % NK], ((uint32_t)(j / NK) & 1u) ^ 1u, ctl)) break;
         mbar_arrive_expect_tx(&k_full[j % NK], TG::TILE_BYTES);
         TG::load(smem + L::K_OFF + (j % NK) * TG::TILE_BYTES, &tk, &k_full[j % NK],
-                 (kt0 + j) * kBN, hk, b);
+                 (kt0 + j) * kBN, hk, b, g.kv_main, d.Hkv, d.B, a.ctl.err, 9);
         k_issued = j + 1;
         if (!mbar_wait(&v_empty[j % NV], ((uint32_t)(j / NV) & 1u) ^ 1u, ctl)) break;
         mbar_arrive_expect_tx(&v_full[j % NV], TG::TILE_BYTES);
         TG::load(smem + L::V_OFF + (j % NV) * TG::TILE_BYTES, &tv, &v_full[j % NV],
-                 (kt0 + j) * kBN, hk, b);
+                 (kt0 + j) * kBN, hk, b, g.kv_main, d.Hkv, d.B, a.ctl.err, 9);
         v_issued = j + 1;
       }
       if (*abort_flag) {

@@ -214,6 +214,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     return;
   }
+  // the work item must exist (ATTN_DEBUG)
+  if (!ATTN_CHECK(a.ctl.err, q0 < d.Sq && h < d.Hq && b < d.B && (!split || chunk < a.nchunk), 3))
+    return;
   // this batch entry's geometry; key tiles kt0 .. kt0 + n_kv - 1
   const MaskGeom g = W ? with_len(d.geom, d.seqlens, b) : d.geom;
   int kt0, n_kv;
@@ -268,8 +271,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
       mbar_arrive_expect_tx(q_full, 2 * TG::TILE_BYTES);
-      TG::load(smem + L::Q_OFF, &tq, q_full, q0, h, b);
-      TG::load(smem + L::Q_OFF + TG::TILE_BYTES, &tq, q_full, q0 + kBM, h, b);
+      TG::load(smem + L::Q_OFF, &tq, q_full, q0, h, b, d.Sq, d.Hq, d.B, a.ctl.err, 1);
+      TG::load(smem + L::Q_OFF + TG::TILE_BYTES, &tq, q_full, q0 + kBM, h, b, d.Sq, d.Hq, d.B,
+               a.ctl.err, 1);
       int issued = 0;
       for (int j = 0; j < n_kv; ++j) {
         bool ok = true;
@@ -283,7 +287,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
           mbar_arrive_expect_tx(&kv_full[s], TG::TILE_BYTES);
           TG::load(smem + L::KV_OFF + s * TG::TILE_BYTES, w == 0 ? &tk : &tv, &kv_full[s],
-                   (kt0 + j) * kBN, hk, b);
+                   (kt0 + j) * kBN, hk, b, g.kv_main, d.Hkv, d.B, a.ctl.err, 2);
           issued = idx + 1;
         }
         if (!ok) break;
@@ -709,6 +713,8 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdArgs a) {
                       ? bh * n_qp + qp
                       : (n_qp - 1 - qp) * (d.B * d.Hq) + bh;
   const int64_t slot0 = (int64_t)bid * a.nchunk;
+  // the chunks read must be slots the forward wrote (ATTN_DEBUG)
+  if (!ATTN_CHECK(a.ctl.err, nc <= a.nchunk && bid < n_qp * d.B * d.Hq, 4)) return;
   float m = -INFINITY;
   for (int c = 0; c < nc; ++c) m = fmaxf(m, a.part_ml[(slot0 + c) * (2 * kBM) + rr].x);
   float l = 0.f;

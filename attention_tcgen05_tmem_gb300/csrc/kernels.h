@@ -121,6 +121,10 @@ cudaError_t launch_mask_pattern(const Dims& d, uint8_t* bits, uint8_t* tiles, cu
 cudaError_t launch_probe(int mode, int D, const CUtensorMap& ta, const CUtensorMap& tb,
                          const void* a_global, float* c, Ctl ctl, cudaStream_t s);
 cudaError_t launch_selftest_wait(Ctl ctl, cudaStream_t s);
+// Whether this library was built with -DATTN_DEBUG (device-side checks), and a
+// kernel whose check fails on purpose (only meaningful when it was).
+bool debug_checks_built();
+cudaError_t launch_selftest_check(Ctl ctl, cudaStream_t s);
 
 // Records `msg` as the calling thread's last error message (attn_train_last_error)
 // and returns `status`; for host code outside the C ABI's own translation unit.

@@ -19,7 +19,25 @@ namespace attn {
 enum DeviceError : uint32_t {
   kErrNone = 0,
   kErrWaitTimeout = 1,  // an mbarrier wait ran out of budget
+  kErrDebugCheck = 2,   // an ATTN_DEBUG device check failed; the site number in bits 8..
 };
+
+// Device-side checks of the build with -DATTN_DEBUG: tile coordinates against
+// the tensor's extents before every TMA load, output and workspace rows
+// before they are stored.  A failed check records kErrDebugCheck | site << 8
+// in the device error word (the first failure wins) and the guarded access is
+// skipped; waits that depended on a skipped copy then run out and the CTA
+// returns as on a timeout.  Without ATTN_DEBUG a check is the constant true:
+// the condition is not evaluated and the kernels are unchanged.
+#ifdef ATTN_DEBUG
+static __device__ __noinline__ bool attn_debug_fail(uint32_t* err, int site) {
+  atomicCAS(err, 0u, (uint32_t)kErrDebugCheck | ((uint32_t)site << 8));
+  return false;
+}
+#define ATTN_CHECK(err, cond, site) ((cond) ? true : ::attn::attn_debug_fail((err), (site)))
+#else
+#define ATTN_CHECK(err, cond, site) true
+#endif
 
 struct WaitCtl {
   uint32_t* err;          // global error word (0 = fine)

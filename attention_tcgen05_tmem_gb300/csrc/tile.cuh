@@ -67,6 +67,16 @@ struct TileGeom {
     for (int x = 0; x < NBOX; ++x)
       tma_load_4d(static_cast<char*>(dst) + x * BOX_BYTES, m, bar, x * BOXC, r0, h, b);
   }
+  // The same, with the ATTN_DEBUG check that the tile overlaps the first rows +
+  // 128 rows of the tensor (a pair's second query tile may lie just past its
+  // end, read as zeros) and that head and batch entry exist; the copy is
+  // skipped if not.
+  __device__ static void load(void* dst, const CUtensorMap* m, uint64_t* bar, int r0, int h,
+                              int b, int rows, int H, int B, uint32_t* err, int site) {
+    if (ATTN_CHECK(err, r0 >= 0 && r0 < rows + 128 && h >= 0 && h < H && b >= 0 && b < B, site))
+      load(dst, m, bar, r0, h, b);
+    (void)rows, (void)H, (void)B, (void)err, (void)site;
+  }
 };
 
 }  // namespace attn

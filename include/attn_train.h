@@ -94,7 +94,8 @@ typedef enum {
   ATTN_ERR_ALIGNMENT = 3,      /* pointer or stride breaks the 16-byte rule */
   ATTN_ERR_WORKSPACE = 4,      /* workspace missing or too small */
   ATTN_ERR_CUDA = 5,           /* a CUDA runtime/driver call failed */
-  ATTN_ERR_DEVICE_TIMEOUT = 6  /* a device-side wait ran out of budget */
+  ATTN_ERR_DEVICE_TIMEOUT = 6, /* a device-side wait ran out of budget */
+  ATTN_ERR_DEVICE_CHECK = 7    /* a device-side check of a -DATTN_DEBUG build failed */
 } attn_status;
 
 /* A [B, H, S, D] tensor view: D has stride 1, the other strides are in
@@ -369,7 +370,10 @@ const char* attn_train_last_error(void);
 
 /* Synchronizes `stream`, then reads and clears the device error word of the
  * current device.  Returns ATTN_ERR_DEVICE_TIMEOUT if a kernel recorded a wait
- * that ran out of budget since the last call. */
+ * that ran out of budget since the last call, ATTN_ERR_DEVICE_CHECK if a
+ * device-side check of a library built with -DATTN_DEBUG failed (tile
+ * coordinates outside a tensor, a work item or workspace slot that does not
+ * exist; the message names the check's site). */
 attn_status attn_train_device_status(void* stream);
 
 /* Per-wait budget of the device-side pipeline waits, in nanoseconds (default
@@ -404,6 +408,12 @@ attn_status attn_train_probe_mma(int mode, int D, const void* a, const void* b, 
 /* Launches a kernel whose bounded wait can never be satisfied, with a 50 ms
  * budget; attn_train_device_status() must then return ATTN_ERR_DEVICE_TIMEOUT. */
 attn_status attn_train_selftest_wait_timeout(void* stream);
+
+/* In a library built with -DATTN_DEBUG: launches a kernel whose device-side
+ * check fails on purpose (site 99, no memory access); attn_train_device_status()
+ * must then return ATTN_ERR_DEVICE_CHECK.  In a normal build: returns
+ * ATTN_ERR_UNSUPPORTED and launches nothing. */
+attn_status attn_train_selftest_debug_check(void* stream);
 
 #ifdef __cplusplus
 }

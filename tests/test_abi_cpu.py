@@ -314,3 +314,11 @@ def test_forward_split_workspace_is_bounded_independently_of_s():
                         n = binding.fwd_workspace_size(p)
                         worst = max(worst, n / (256 * (D + 2) * 4))
     assert 0 < worst <= 4 * 152
+
+
+def test_debug_selftest_is_refused_by_the_normal_build():
+    from attention_tcgen05_tmem_gb300 import build as lib_build
+    lib_build.build()
+    lib = binding.load()
+    assert lib.attn_train_selftest_debug_check(None) == 2
+    assert b"ATTN_DEBUG" in lib.attn_train_last_error()
