@@ -904,13 +904,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && n_kv > 0) ok = mbar_wait_warp(done, 0, ctl);
     if (ok) {
       if (n_kv > 0) tc_fence_after();
-      // this warpgroup's dQ columns: 16-wide chunks c0 = 16 wg, 16 wg + 32, ...
+      // this warpgroup's dQ columns: the contiguous half [cbeg, cend) (all of them
+      // for warpgroup 0 at D = 16)
+      constexpr int NCW = D >= 32 ? D / 2 : 16;
+      const int cbeg = wg * NCW, cend = min(D, cbeg + NCW);
       const uint32_t tq = tmem + lane_base + T_DQ;
       if (n_kv == 0 && g.ttt > 0) {  // accumulator never written by an MMA: start at zero
         uint32_t z[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) z[e] = 0u;
-        for (int c0 = 16 * wg; c0 < D; c0 += 32) tmem_st16(tq + c0, z);
+        for (int c0 = cbeg; c0 < cend; c0 += 16) tmem_st16(tq + c0, z);
         tmem_st_wait();
       }
       // TTT suffix diagonals: dQ += ds_i k_i with ds_i = p_i (dO . v_i - Delta) from the
@@ -920,7 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int u = 0; u < kDiagBatch; ++u)
           dsv[u] = (qin && i0 + u <= g.ttt) ? a.ttt_ds[rrow * g.ttt + (i0 + u - 1)] : 0.f;
-        for (int c0 = 16 * wg; c0 < D; c0 += 32) {
+        for (int c0 = cbeg; c0 < cend; c0 += 16) {
           uint32_t raw[16];
           tmem_ld16(tq + c0, raw);
 #pragma unroll
@@ -944,7 +947,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
       }
-      for (int c0 = 16 * wg; c0 < D; c0 += 32) {
+      // the warp's 32 rows of its half go through shared memory (every MMA has
+      // completed, so the Q and dO tiles are free) for coalesced global stores
+      const RowStage<NCW> stage{smem + L::Q_OFF + warp * (32 * NCW * 4), d.out_f32 != 0};
+      for (int c0 = cbeg; c0 < cend; c0 += 16) {
         float acc[16];
         if (n_kv > 0 || g.ttt > 0) {
           uint32_t raw[16];
@@ -955,7 +961,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e) acc[e] = 0.f;
         }
-        if (qin) store16(a.dq, b, h, q, c0, acc, d.scale, d.out_f32 != 0);
+        stage.put16(lane, c0 - cbeg, acc, d.scale);
+      }
+      __syncwarp();
+      if (cbeg < cend) {
+        const int row0 = q0 + quad * 32;
+        stage.copy_out(lane, a.dq, b, h, row0, min(32, max(0, d.Sq - row0)), cbeg);
       }
     } else if (qin) {
       // a wait of this CTA ran out of budget: NaN instead of a partial result

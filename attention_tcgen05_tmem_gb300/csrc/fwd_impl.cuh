@@ -563,19 +563,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_after();
         // partial rows are indexed by CTA: (blockIdx.x, row of the pair)
         const int64_t slot = (int64_t)blockIdx.x * (2 * kBM) + x * kBM + r;
-        float* po = a.part_o + slot * D;
+        // staged like the final O rows (see below), stored as dense fp32 rows
+        const RowStage<D> stage{smem + (x == 0 ? L::Q_OFF : L::KV_OFF) + quad * (32 * D * 4),
+                                true};
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 16) {
           uint32_t raw[16];
+          float vals[16];
           tmem_ld16(tO + c0, raw);
-          if (q < d.Sq) {
 #pragma unroll
-            for (int e = 0; e < 16; e += 4)
-              *reinterpret_cast<float4*>(po + c0 + e) =
-                  make_float4(__uint_as_float(raw[e]), __uint_as_float(raw[e + 1]),
-                              __uint_as_float(raw[e + 2]), __uint_as_float(raw[e + 3]));
-          }
+          for (int e = 0; e < 16; ++e) vals[e] = __uint_as_float(raw[e]);
+          stage.put16(lane, c0, vals, 1.f);
         }
+        __syncwarp();
+        const View part{a.part_o, 0, 0, D};
+        const int row0 = qt0 + quad * 32;
+        stage.copy_out(lane, part, 0, 0, slot - r + quad * 32, min(32, max(0, d.Sq - row0)), 0);
         if (q < d.Sq) a.part_ml[slot] = make_float2(m_run, l_run);
       }
     } else if (ok) {
@@ -642,6 +645,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
       const bool have_acc = n_kv > 0 || g.ttt > 0;
+      // the warp's 32 rows go through shared memory so that the global stores are
+      // coalesced: query tile 0 stages in the Q tiles (their last reader, S1 of the
+      // last key tile, was issued before PV0 of that tile, which has completed),
+      // query tile 1 in the K/V ring (free: its own last PV was the last MMA)
+      const RowStage<D> stage{smem + (x == 0 ? L::Q_OFF : L::KV_OFF) + quad * (32 * D * 4),
+                              d.out_f32 != 0};
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 16) {
         float vals[16];
@@ -654,8 +663,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e) vals[e] = 0.f;
         }
-        if (qin) store16(a.o, b, h, q, c0, vals, inv, d.out_f32 != 0);
+        stage.put16(lane, c0, vals, inv);
       }
+      __syncwarp();
+      const int row0 = qt0 + quad * 32;
+      stage.copy_out(lane, a.o, b, h, row0, min(32, max(0, d.Sq - row0)), 0);
       if (qin) {
         const float lse = (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * 0.69314718055994531f : 0.f;
         a.lse[((int64_t)b * d.Hq + h) * d.Sq + q] = lse;

@@ -150,6 +150,60 @@ __device__ __forceinline__ void store16(const View& v, int b, int h, int64_t s, 
   }
 }
 
+// Coalesced row stores for epilogues in which lane i of a warp holds row
+// row0 + i (the TMEM lane layout): storing straight from the lanes makes every
+// store instruction touch 32 rows.  Instead each lane puts its row -- NC
+// columns, fp32 or bf16 -- into a warp-private shared-memory staging area, and
+// the warp then copies rows out with each instruction covering consecutive
+// 16-byte chunks of one or two rows.  Chunk c of staged row r sits at chunk
+// position c ^ (r % CPR) (CPR = chunks per row, a power of two), so the lane
+// writes (fixed c, 32 rows) and the copy-out reads (fixed row, consecutive c)
+// both run at the minimum of four wavefronts per 512-byte instruction.
+template <int NC>
+struct RowStage {
+  uint8_t* base;  // 32 * NC * 4 bytes of shared memory, 16-byte aligned
+  bool f32;       // element type of the destination (fp32, else bf16)
+
+  __device__ int row_bytes() const { return NC * (f32 ? 4 : 2); }
+  // columns c0 .. c0 + 15 (c0 a multiple of 16, < NC) of this lane's row, times mul
+  __device__ void put16(int lane, int c0, const float* x, float mul) const {
+    const int rb = row_bytes(), cpr = rb / 16;
+    uint8_t* row = base + lane * rb;
+    if (f32) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = c0 / 4 + e;
+        *reinterpret_cast<float4*>(row + 16 * (c ^ (lane & (cpr - 1)))) =
+            make_float4(x[4 * e] * mul, x[4 * e + 1] * mul, x[4 * e + 2] * mul,
+                        x[4 * e + 3] * mul);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int c = c0 / 8 + e;
+        uint4 pkt;
+        pkt.x = pack_bf16x2(x[8 * e + 0] * mul, x[8 * e + 1] * mul);
+        pkt.y = pack_bf16x2(x[8 * e + 2] * mul, x[8 * e + 3] * mul);
+        pkt.z = pack_bf16x2(x[8 * e + 4] * mul, x[8 * e + 5] * mul);
+        pkt.w = pack_bf16x2(x[8 * e + 6] * mul, x[8 * e + 7] * mul);
+        *reinterpret_cast<uint4*>(row + 16 * (c ^ (lane & (cpr - 1)))) = pkt;
+      }
+    }
+  }
+  // rows 0 .. nrows-1 of the stage to rows row0 .. of the view (columns col0 ..
+  // col0 + NC - 1); call after every lane's put16 and a __syncwarp
+  __device__ void copy_out(int lane, const View& v, int b, int h, int64_t row0, int nrows,
+                           int col0) const {
+    const int rb = row_bytes(), cpr = rb / 16, es = f32 ? 4 : 2;
+    char* dst0 = reinterpret_cast<char*>(v.ptr) + (b * v.sb + h * v.sh + row0 * v.ss + col0) * es;
+    for (int k = lane; k < nrows * cpr; k += 32) {
+      const int r = k / cpr, c = k % cpr;
+      const uint4 val = *reinterpret_cast<const uint4*>(base + r * rb + 16 * (c ^ (r & (cpr - 1))));
+      *reinterpret_cast<uint4*>(dst0 + (int64_t)r * v.ss * es + 16 * c) = val;
+    }
+  }
+};
+
 // Skipped work is made visible: a CTA that computes nothing (the device error
 // word was already set when it started) or gave up part-way (one of its waits
 // ran out of budget) writes NaN where its results would go, so that stale
