@@ -22,13 +22,15 @@
 //             q heads in ascending order; one warp per key row r serves the
 //             key i*Sq + r of every segment i, reading each q and dO row once.
 //
-// Tensor-core kernels use 10 warps: 0-7 elementwise (two warpgroups split the
+// Tensor-core kernels use 12 warps: 0-7 elementwise (two warpgroups split the
 // 128 columns of each S / dP tile; thread = TMEM lane = row), 8 TMA producer,
-// 9 tcgen05 issuer.  P^T, dS^T and dS are written back to tensor memory as
-// bf16 and used as the A operand of the next MMA directly from there.
+// 9 tcgen05 issuer, 10-11 idle (their registers go to the elementwise warps).
+// P^T, dS^T and dS are written back to tensor memory as bf16 and used as the
+// A operand of the next MMA directly from there.
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -917,35 +919,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
       }
       // TTT suffix diagonals: dQ += ds_i k_i with ds_i = p_i (dO . v_i - Delta) from the
-      // prep pass, folded into the TMEM accumulator kDiagBatch diagonals at a time
-      for (int i0 = 1; i0 <= g.ttt; i0 += kDiagBatch) {
-        float dsv[kDiagBatch];
+      // prep pass.  The k rows of the warp's 32 query positions (this warpgroup's
+      // columns) are fetched two segments at a time into the warp's output staging
+      // area (every MMA has completed, so the Q and dO tiles are free) and folded
+      // into the TMEM accumulator in one pass per pair, in segment order.
+      if (g.ttt > 0 && cbeg < cend) {
+        const int row0 = q0 + quad * 32;
+        const int nvalid = max(0, min(32, d.Sq - row0));
+        uint8_t* fbase = smem + L::Q_OFF + warp * (32 * NCW * 4);
+        const RowFetch<NCW> fk[2] = {{fbase}, {fbase + 32 * NCW * 2}};
+        for (int i0 = 1; i0 <= g.ttt; i0 += 2) {
+          const int nseg = min(2, g.ttt - i0 + 1);
+          for (int u = 0; u < nseg; ++u)
+            fk[u].issue(lane, a.k, b, hk, (int64_t)(i0 + u) * d.Sq + row0, nvalid, cbeg);
+          cp_async_commit();
+          float dsv[2];
 #pragma unroll
-        for (int u = 0; u < kDiagBatch; ++u)
-          dsv[u] = (qin && i0 + u <= g.ttt) ? a.ttt_ds[rrow * g.ttt + (i0 + u - 1)] : 0.f;
-        for (int c0 = cbeg; c0 < cend; c0 += 16) {
-          uint32_t raw[16];
-          tmem_ld16(tq + c0, raw);
+          for (int u = 0; u < 2; ++u)
+            dsv[u] = (qin && u < nseg) ? a.ttt_ds[rrow * g.ttt + (i0 + u - 1)] : 0.f;
+          cp_async_wait_all();
+          __syncwarp();
+          for (int c0 = cbeg; c0 < cend; c0 += 16) {
+            uint32_t raw[16];
+            float vals[16];
+            tmem_ld16(tq + c0, raw);
 #pragma unroll
-          for (int u = 0; u < kDiagBatch; ++u) {
-            if (!(qin && i0 + u <= g.ttt)) continue;
-            const __nv_bfloat16* krow = row_ptr(a.k, b, hk, (int64_t)(i0 + u) * d.Sq + q) + c0;
+            for (int e = 0; e < 16; ++e) vals[e] = __uint_as_float(raw[e]);
+            if (qin) {
 #pragma unroll
-            for (int e = 0; e < 16; e += 8) {
-              const uint4 ka = *reinterpret_cast<const uint4*>(krow + e);
-              const __nv_bfloat162* kv2 = reinterpret_cast<const __nv_bfloat162*>(&ka);
-#pragma unroll
-              for (int f = 0; f < 4; ++f) {
-                const float2 kf = __bfloat1622float2(kv2[f]);
-                raw[e + 2 * f] = __float_as_uint(fmaf(dsv[u], kf.x, __uint_as_float(raw[e + 2 * f])));
-                raw[e + 2 * f + 1] =
-                    __float_as_uint(fmaf(dsv[u], kf.y, __uint_as_float(raw[e + 2 * f + 1])));
-              }
+              for (int u = 0; u < 2; ++u)
+                if (u < nseg) fk[u].axpy16(lane, (c0 - cbeg) / 16, dsv[u], vals);
             }
+#pragma unroll
+            for (int e = 0; e < 16; ++e) raw[e] = __float_as_uint(vals[e]);
+            tmem_st16(tq + c0, raw);
           }
-          tmem_st16(tq + c0, raw);
+          tmem_st_wait();
+          __syncwarp();  // every lane has read the pair before it is refilled
         }
-        tmem_st_wait();
       }
       // the warp's 32 rows of its half go through shared memory (every MMA has
       // completed, so the Q and dO tiles are free) for coalesced global stores
@@ -995,21 +1006,6 @@ struct SuffixVec {
 };
 
 template <int VEC>
-__device__ __forceinline__ void load_bf16_cols(const __nv_bfloat16* p, float* f) {
-  if constexpr (VEC == 4) {
-    const uint2 u = *reinterpret_cast<const uint2*>(p);
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-  } else if constexpr (VEC == 2) {
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
-    f[0] = a.x; f[1] = a.y;
-  } else {
-    f[0] = __bfloat162float(*p);
-  }
-}
-
-template <int VEC>
 __device__ __forceinline__ void store_cols(void* base, int64_t off, bool f32, const float* v) {
   if (f32) {
     float* o = reinterpret_cast<float*>(base) + off;
@@ -1036,11 +1032,42 @@ __device__ __forceinline__ void store_cols(void* base, int64_t off, bool f32, co
   }
 }
 
+// Raw bf16 columns of one lane (VEC = 4, 2 or 1), loaded in one instruction
+// and widened to fp32 only when used, so that the loads of several q heads can
+// be in flight together at little register cost.
+template <int VEC>
+struct RawCols {
+  using T = typename std::conditional<VEC == 4, uint2,
+                                      typename std::conditional<VEC == 2, uint32_t,
+                                                                uint16_t>::type>::type;
+  T v;
+  __device__ void load(const __nv_bfloat16* p) { v = *reinterpret_cast<const T*>(p); }
+  __device__ void widen(float* f) const {
+    if constexpr (VEC == 4) {
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+      f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    } else if constexpr (VEC == 2) {
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+      f[0] = a.x; f[1] = a.y;
+    } else {
+      f[0] = bf16_bits(v);
+    }
+  }
+};
+
 // CH: segments per pass over the q and dO rows (1, 2, 4 or 8, the smallest
 // that covers t up to 8), so that the accumulators' registers scale with t.
+// The q heads of the group are taken HB at a time: their q and dO rows and
+// their p / ds values (lane u holds segment i0 + u, handed to every lane by a
+// shuffle) are all requested before the first is used, so that each warp
+// keeps several rows of memory traffic in flight.  The sums still run over
+// the heads in ascending order, one fused multiply-add per head.
 template <int D, int CH>
 __global__ void __launch_bounds__(256) ttt_diag_bwd_kernel(const BwdArgs a) {
   constexpr int VEC = SuffixVec<D>::VEC, LANES = SuffixVec<D>::LANES;
+  constexpr int HB = CH >= 4 ? 4 : 2;  // fewer at small CH, where registers set the occupancy
+  static_assert(CH <= 32, "one lane per segment of a pass");
   const Dims& d = a.d;
   const int t = d.geom.ttt;
   const int64_t rows = (int64_t)d.B * d.Hkv * d.Sq;
@@ -1054,35 +1081,48 @@ __global__ void __launch_bounds__(256) ttt_diag_bwd_kernel(const BwdArgs a) {
   const int hk = (int)(bk % d.Hkv);
   const int b = (int)(bk / d.Hkv);
   for (int i0 = 1; i0 <= t; i0 += CH) {
+    const int nch = min(CH, t - i0 + 1);  // segments in this pass
     float dk[CH][VEC], dv[CH][VEC];
 #pragma unroll
     for (int u = 0; u < CH; ++u)
 #pragma unroll
       for (int e = 0; e < VEC; ++e) dk[u][e] = dv[u][e] = 0.f;
-    // p and ds of (query row r of q head h, diagonal i) come from the prep pass
-    for (int gq = 0; gq < d.G; ++gq) {
-      const int h = hk * d.G + gq;
-      const int64_t rrow = ((int64_t)b * d.Hq + h) * d.Sq + r;
-      float qv[VEC], gv[VEC];
-      if (act) {
-        load_bf16_cols<VEC>(row_ptr(a.q, b, h, r) + c0, qv);
-        load_bf16_cols<VEC>(row_ptr(a.dout, b, h, r) + c0, gv);
+    for (int g0 = 0; g0 < d.G; g0 += HB) {
+      RawCols<VEC> qr[HB], gr[HB];
+      float pl[HB], dsl[HB];
+#pragma unroll
+      for (int j = 0; j < HB; ++j) {
+        const int gq = g0 + j;
+        const bool hv = gq < d.G;
+        const int h = hk * d.G + gq;
+        const int64_t rrow = ((int64_t)b * d.Hq + h) * d.Sq + r;
+        if (hv && act) {
+          qr[j].load(row_ptr(a.q, b, h, r) + c0);
+          gr[j].load(row_ptr(a.dout, b, h, r) + c0);
+        }
+        // p and ds of (query row r of q head h, segment i0 + lane) from the prep pass
+        const bool pv = hv && lane < nch;
+        pl[j] = pv ? a.ttt_p[rrow * t + (i0 - 1 + lane)] : 0.f;
+        dsl[j] = pv ? a.ttt_ds[rrow * t + (i0 - 1 + lane)] : 0.f;
       }
-      float p[CH], ds[CH];
 #pragma unroll
-      for (int u = 0; u < CH; ++u) {
-        const bool ok = i0 + u <= t;
-        p[u] = ok ? a.ttt_p[rrow * t + (i0 + u - 1)] : 0.f;
-        ds[u] = ok ? a.ttt_ds[rrow * t + (i0 + u - 1)] : 0.f;
-      }
-      if (act) {
+      for (int j = 0; j < HB; ++j) {
+        if (g0 + j >= d.G) break;  // uniform over the warp
+        float qv[VEC], gv[VEC];
+        qr[j].widen(qv);
+        gr[j].widen(gv);
 #pragma unroll
-        for (int u = 0; u < CH; ++u)
+        for (int u = 0; u < CH; ++u) {
+          const float p = __shfl_sync(0xffffffffu, pl[j], u);
+          const float ds = __shfl_sync(0xffffffffu, dsl[j], u);
+          if (act && u < nch) {
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            dv[u][e] = fmaf(p[u], gv[e], dv[u][e]);
-            dk[u][e] = fmaf(ds[u], qv[e], dk[u][e]);
+            for (int e = 0; e < VEC; ++e) {
+              dv[u][e] = fmaf(p, gv[e], dv[u][e]);
+              dk[u][e] = fmaf(ds, qv[e], dk[u][e]);
+            }
           }
+        }
       }
     }
     if (act) {

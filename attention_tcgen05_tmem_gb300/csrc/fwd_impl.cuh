@@ -612,17 +612,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int i = 1; i <= g.ttt; ++i) m_star = fmaxf(m_star, diag_score(i));
         const float alpha = (m_run == neg_inf()) ? 0.f : ex2_approx(m_run - m_star);
         l_run *= alpha;
-        // pass 2: O = alpha O + sum_i w_i v_i, kDiagBatch diagonals per TMEM round trip
-        for (int i0 = 1; i0 <= g.ttt; i0 += kDiagBatch) {
-          float w[kDiagBatch];
+        // pass 2: O = alpha O + sum_i w_i v_i.  The v rows of the warp's 32 query
+        // positions are fetched two segments at a time into the warp's output
+        // staging area (coalesced copies, one round trip per pair) and folded
+        // into the TMEM accumulator in one pass per pair, in segment order.
+        const int row0 = qt0 + quad * 32;
+        const int nvalid = max(0, min(32, min(d.Sq, g.kv_len) - row0));
+        uint8_t* fbase = smem + (x == 0 ? L::Q_OFF : L::KV_OFF) + quad * (32 * D * 4);
+        const RowFetch<D> fv[2] = {{fbase}, {fbase + 32 * D * 2}};
+        for (int i0 = 1; i0 <= g.ttt; i0 += 2) {
+          const int nseg = min(2, g.ttt - i0 + 1);
+          for (int u = 0; u < nseg; ++u)
+            fv[u].issue(lane, a.v, b, hk, (int64_t)(i0 + u) * d.Sq + row0, nvalid, 0);
+          cp_async_commit();
+          float w[2];
 #pragma unroll
-          for (int u = 0; u < kDiagBatch; ++u) {
+          for (int u = 0; u < 2; ++u) {
             w[u] = 0.f;
-            if (qdiag && i0 + u <= g.ttt) {
+            if (qdiag && u < nseg) {
               w[u] = ex2_approx(diag_score(i0 + u) - m_star);
               l_run += w[u];
             }
           }
+          cp_async_wait_all();
+          __syncwarp();
           const float scale0 = (i0 == 1) ? alpha : 1.f;
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 16) {
@@ -631,15 +644,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             tmem_ld16(tO + c0, raw);
 #pragma unroll
             for (int e = 0; e < 16; ++e) vals[e] = __uint_as_float(raw[e]) * scale0;
+            if (qdiag) {
 #pragma unroll
-            for (int u = 0; u < kDiagBatch; ++u)
-              if (qdiag && i0 + u <= g.ttt)
-                axpy16(vals, w[u], row_ptr(a.v, b, hk, (int64_t)(i0 + u) * d.Sq + q) + c0);
+              for (int u = 0; u < 2; ++u)
+                if (u < nseg) fv[u].axpy16(lane, c0 / 16, w[u], vals);
+            }
 #pragma unroll
             for (int e = 0; e < 16; ++e) raw[e] = __float_as_uint(vals[e]);
             tmem_st16(tO + c0, raw);
           }
           tmem_st_wait();
+          __syncwarp();  // every lane has read the pair before it is refilled
         }
         m_run = m_star;
       }

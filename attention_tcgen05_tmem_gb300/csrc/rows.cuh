@@ -1,6 +1,7 @@
 // rows.cuh -- per-row helpers for epilogues and the TTT suffix passes:
-// row addressing in [B, H, S, D] views, bf16 row dot products (fp32
-// accumulate) and 16-column stores of fp32 results as fp32 or bf16.
+// row addressing in [B, H, S, D] views, the additive mask row, bf16 row dot
+// products (fp32 accumulate), 16-column stores of fp32 results as fp32 or
+// bf16, and coalesced row staging through shared memory in both directions.
 #pragma once
 #include <cstdint>
 
@@ -8,8 +9,6 @@
 #include "ptx.cuh"
 
 namespace attn {
-
-constexpr int kDiagBatch = 8;  // TTT suffix diagonals folded per epilogue pass
 
 __device__ __forceinline__ const __nv_bfloat16* row_ptr(const View& v, int b, int h, int64_t s) {
   return reinterpret_cast<const __nv_bfloat16*>(v.ptr) + b * v.sb + h * v.sh + s * v.ss;
@@ -110,21 +109,6 @@ __device__ __forceinline__ float dot_rows(const __nv_bfloat16* x, const __nv_bfl
   return acc;
 }
 
-// x[0..15] += w * row[0..15] (bf16 row).
-__device__ __forceinline__ void axpy16(float* x, float w, const __nv_bfloat16* row) {
-#pragma unroll
-  for (int e = 0; e < 16; e += 8) {
-    const uint4 ra = *reinterpret_cast<const uint4*>(row + e);
-    const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&ra);
-#pragma unroll
-    for (int f = 0; f < 4; ++f) {
-      const float2 rf = __bfloat1622float2(r2[f]);
-      x[e + 2 * f] = fmaf(w, rf.x, x[e + 2 * f]);
-      x[e + 2 * f + 1] = fmaf(w, rf.y, x[e + 2 * f + 1]);
-    }
-  }
-}
-
 // Store 16 fp32 values (times mul) at columns c0 .. c0+15 of an output row,
 // as fp32 or bf16.
 __device__ __forceinline__ void store16(const View& v, int b, int h, int64_t s, int c0,
@@ -200,6 +184,45 @@ struct RowStage {
       const int r = k / cpr, c = k % cpr;
       const uint4 val = *reinterpret_cast<const uint4*>(base + r * rb + 16 * (c ^ (r & (cpr - 1))));
       *reinterpret_cast<uint4*>(dst0 + (int64_t)r * v.ss * es + 16 * c) = val;
+    }
+  }
+};
+
+// The reverse direction, for epilogues that need other rows of the same 32
+// query positions (the TTT suffix segments' k or v rows): the warp fetches
+// rows row0 .. row0 + nvalid - 1 (bf16, columns col0 .. col0 + NC - 1) with
+// 16-byte asynchronous copies, each instruction covering consecutive chunks of
+// one or two rows, into a warp-private area where row r keeps its chunks
+// XOR-swizzled by r (the RowStage layout); lane r then reads its own row from
+// there.  Rows at or past nvalid are not fetched and must not be read.
+template <int NC>
+struct RowFetch {
+  static constexpr int RB = NC * 2;    // bytes per staged row
+  static constexpr int CPR = RB / 16;  // 16-byte chunks per row (a power of two)
+  uint8_t* base;                       // 32 * RB bytes of shared memory, 16-byte aligned
+
+  __device__ void issue(int lane, const View& v, int b, int h, int64_t row0, int nvalid,
+                        int col0) const {
+    const char* src0 = reinterpret_cast<const char*>(v.ptr) +
+                       (b * v.sb + h * v.sh + row0 * v.ss + col0) * 2;
+    for (int k = lane; k < nvalid * CPR; k += 32) {
+      const int r = k / CPR, c = k % CPR;
+      cp_async16(base + r * RB + 16 * (c ^ (r & (CPR - 1))), src0 + (int64_t)r * v.ss * 2 + 16 * c);
+    }
+  }
+  // x[0..15] += w * (columns 16 c2 .. 16 c2 + 15 of this lane's row)
+  __device__ void axpy16(int lane, int c2, float w, float* x) const {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int c = 2 * c2 + h;
+      const uint4 ra = *reinterpret_cast<const uint4*>(base + lane * RB + 16 * (c ^ (lane & (CPR - 1))));
+      const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&ra);
+#pragma unroll
+      for (int f = 0; f < 4; ++f) {
+        const float2 rf = __bfloat1622float2(r2[f]);
+        x[8 * h + 2 * f] = fmaf(w, rf.x, x[8 * h + 2 * f]);
+        x[8 * h + 2 * f + 1] = fmaf(w, rf.y, x[8 * h + 2 * f + 1]);
+      }
     }
   }
 };
