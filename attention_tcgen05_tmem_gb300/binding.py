@@ -28,8 +28,9 @@ EXPORTS = ("attn_train_supports", "attn_train_workspace_size", "attn_train_fwd",
            "attn_train_mask_pattern", "attn_train_probe_mma", "attn_train_selftest_wait_timeout",
            "attn_train_selftest_debug_check",
            "attn_train_logsoftmax_loss_fwd", "attn_train_logsoftmax_loss_bwd",
-           "attn_train_step_host_arena_size", "attn_train_step_host",
-           "attn_train_host_session_create", "attn_train_host_session_step",
+           "attn_train_step_host_arena_size", "attn_train_host_session_arena_size",
+           "attn_train_step_host", "attn_train_host_session_create",
+           "attn_train_host_session_create_slots", "attn_train_host_session_step",
            "attn_train_host_session_join", "attn_train_host_session_destroy")
 
 
@@ -109,6 +110,10 @@ def load(path: str = LIB_PATH):
                                           ctypes.c_size_t, vp]),
             "attn_train_host_session_create": (st, [P, ctypes.c_int, vp, ctypes.c_size_t,
                                                     ctypes.POINTER(vp)]),
+            "attn_train_host_session_arena_size": (st, [P, ctypes.c_int, ctypes.c_int,
+                                                        ctypes.POINTER(ctypes.c_size_t)]),
+            "attn_train_host_session_create_slots": (st, [P, ctypes.c_int, ctypes.c_int, vp,
+                                                          ctypes.c_size_t, ctypes.POINTER(vp)]),
             "attn_train_host_session_step": (st, [vp, ctypes.POINTER(HostIO), vp]),
             "attn_train_host_session_join": (st, [vp, vp]),
             "attn_train_host_session_destroy": (st, [vp]),
@@ -261,11 +266,19 @@ def bwd_noalloc_raw(p: Problem, q, k, v, o, dout, lse, dq, dk, dv, stream=None):
                                          view(dk), view(dv), _stream(stream)))
 
 
-def step_host_arena_size(p: Problem, kv_heads_per_chunk: int = 0) -> int:
-    """Device arena bytes attn_train_step_host needs (0 = automatic chunk)."""
+HOST_MAX_SLOTS = 16  # ATTN_HOST_MAX_SLOTS
+
+
+def step_host_arena_size(p: Problem, kv_heads_per_chunk: int = 0, slots: int = 2) -> int:
+    """Device arena bytes of attn_train_step_host (two slots) or of a host
+    session with `slots` slots (kv_heads_per_chunk 0 = one chunk per step)."""
     n = ctypes.c_size_t(0)
-    _check(load().attn_train_step_host_arena_size(ctypes.byref(p), int(kv_heads_per_chunk),
-                                                  ctypes.byref(n)))
+    if slots == 2:
+        _check(load().attn_train_step_host_arena_size(ctypes.byref(p), int(kv_heads_per_chunk),
+                                                      ctypes.byref(n)))
+    else:
+        _check(load().attn_train_host_session_arena_size(ctypes.byref(p), int(kv_heads_per_chunk),
+                                                         int(slots), ctypes.byref(n)))
     return int(n.value)
 
 
@@ -295,16 +308,24 @@ def step_host_raw(p: Problem, host: dict, arena, kv_heads_per_chunk: int = 0, st
 class HostSession:
     """attn_train_host_session_*: steps of one problem from host memory whose
     copies overlap the neighbouring steps' kernels.  Keep `p` (and its host
-    key lengths / mask tensors) and the arena alive while the session is used."""
+    key lengths / mask tensors) and the arena alive while the session is used.
+    `slots` (2 to HOST_MAX_SLOTS) device slots let the copies run that many
+    chunks minus one ahead of or behind the kernels; the arena must hold
+    step_host_arena_size(p, kv_heads_per_chunk, slots) bytes."""
 
-    def __init__(self, p: Problem, arena, kv_heads_per_chunk: int = 0):
+    def __init__(self, p: Problem, arena, kv_heads_per_chunk: int = 0, slots: int = 2):
+        self._h = ctypes.c_void_p(0)  # no session yet (close() is safe if creation fails)
         self._lib = load()
         self.p = p
         self.arena = arena
         h = ctypes.c_void_p(0)
-        _check(self._lib.attn_train_host_session_create(ctypes.byref(p), int(kv_heads_per_chunk),
-                                                        ctypes.c_void_p(arena.data_ptr()),
-                                                        arena.numel(), ctypes.byref(h)))
+        args = (ctypes.c_void_p(arena.data_ptr()), arena.numel(), ctypes.byref(h))
+        if slots == 2:
+            _check(self._lib.attn_train_host_session_create(ctypes.byref(p),
+                                                            int(kv_heads_per_chunk), *args))
+        else:
+            _check(self._lib.attn_train_host_session_create_slots(
+                ctypes.byref(p), int(kv_heads_per_chunk), int(slots), *args))
         self._h = h
 
     def step(self, host: dict, stream=None):

@@ -9,14 +9,15 @@
 //   copy-in   q, k, v, then dO of chunk c + 1 (while chunk c computes)
 //   compute   forward; backward prep + dQ; backward dK/dV (the caller's stream)
 //   copy-out  O and LSE during the backward, dQ during dK/dV, then dK, dV
-// The device copies of a chunk live in one of two arena slots; chunk c + 2
-// takes chunk c's slot once chunk c's compute has read its inputs and its
-// copy-out has read its outputs.  A session keeps the streams, events and
-// slot counter between steps, so the chunks of the next step continue the
-// alternation and its copy-in overlaps this step's compute.  Every chunk runs
-// the same kernels as the device-memory entry points on the sub-problem, and
-// no kernel mixes heads, so the results equal those of the unchunked call bit
-// for bit.
+// The device copies of a chunk live in one of n arena slots (n = 2 by
+// default); chunk c + n takes chunk c's slot once chunk c's compute has read
+// its inputs and its copy-out has read its outputs, so the copies may run up
+// to n - 1 chunks ahead of (inputs) or behind (outputs) the kernels.  A
+// session keeps the streams, events and slot counter between steps, so the
+// chunks of the next step continue the rotation and its copy-in overlaps this
+// step's compute.  Every chunk runs the same kernels as the device-memory
+// entry points on the sub-problem, and no kernel mixes heads, so the results
+// equal those of the unchunked call bit for bit.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -30,6 +31,7 @@
 namespace {
 
 constexpr size_t kAlign = 256;
+constexpr int kMaxSlots = ATTN_HOST_MAX_SLOTS;
 size_t up(size_t n) { return (n + kAlign - 1) & ~(kAlign - 1); }
 int cdiv(int a, int b) { return (a + b - 1) / b; }
 
@@ -56,8 +58,9 @@ struct Plan {
   // offsets inside one slot and its size
   size_t s_q = 0, s_k = 0, s_v = 0, s_do = 0, s_o = 0, s_lse = 0, s_dq = 0, s_dk = 0, s_dv = 0;
   size_t slot = 0;
+  int nslots = 2;  // chunk slots (and copies of the key lengths / mask)
   int fsplit = 0;  // the whole problem's forward split (chunk length in key tiles)
-  // arena: static[2] (key lengths, mask) | chunk workspace | slot[2]
+  // arena: static[nslots] (key lengths, mask) | chunk workspace | slot[nslots]
   size_t lens_off = 0, mask_off = 0, mask_bytes = 0, stat = 0, ws_off = 0, ws = 0, slot_off = 0;
   size_t total = 0;
 };
@@ -75,8 +78,10 @@ attn_problem chunk_problem(const attn_problem& p, int nb, int n, const int32_t* 
   return s;
 }
 
-attn_status make_plan(const attn_problem* p, int kv_heads_per_chunk, Plan* pl) {
+attn_status make_plan(const attn_problem* p, int kv_heads_per_chunk, int slots, Plan* pl) {
   if (p == nullptr) return err(ATTN_ERR_INVALID, "problem is NULL");
+  if (slots < 2 || slots > kMaxSlots)
+    return err(ATTN_ERR_INVALID, "slots must be in [2, ATTN_HOST_MAX_SLOTS]");
   // Validate the problem as it will run on the device: the key lengths and the
   // mask are copied to 256-byte aligned arena offsets, so their host addresses
   // need no alignment; a stand-in aligned address takes their place for the
@@ -91,6 +96,7 @@ attn_status make_plan(const attn_problem* p, int kv_heads_per_chunk, Plan* pl) {
     return err(ATTN_ERR_INVALID, "kv_heads_per_chunk exceeds Hkv");
 
   Plan& P = *pl;
+  P.nslots = slots;
   P.whole = kv_heads_per_chunk <= 0;
   P.NB = P.whole ? p->B : 1;
   P.U = P.whole ? p->Hkv : kv_heads_per_chunk;
@@ -125,7 +131,7 @@ attn_status make_plan(const attn_problem* p, int kv_heads_per_chunk, Plan* pl) {
     o += up(P.mask_bytes);
   }
   P.stat = o;
-  o = 2 * P.stat;
+  o = (size_t)slots * P.stat;
   // one workspace region serves the forward's key-range split and the backward:
   // the forward's merge pass has consumed its partials before the backward runs.
   // Every chunk splits its forward like the whole problem would, so that the
@@ -138,7 +144,7 @@ attn_status make_plan(const attn_problem* p, int kv_heads_per_chunk, Plan* pl) {
   P.ws_off = o;
   o += up(P.ws);
   P.slot_off = o;
-  o += 2 * P.slot;
+  o += (size_t)slots * P.slot;
   P.total = o;
   return ATTN_OK;
 }
@@ -155,43 +161,56 @@ attn_tensor dev_view(const void* ptr, int H, int S, int D) {
 }  // namespace
 
 // A session: the problem, its plan and arena, the two copy streams and the
-// events that order the slots.  Chunks take the slots alternately across
-// steps, so the next step's copy-in overlaps this step's compute.
+// events that order the slots.  Chunks take the slots in turn across steps,
+// so the next step's copy-in overlaps this step's compute.
 struct attn_host_session_s {
   attn_problem p{};
   Plan pl;
   char* arena = nullptr;
   cudaStream_t in = nullptr, out = nullptr;
   cudaEvent_t start = nullptr, stat = nullptr, end_in = nullptr, end_out = nullptr;
-  cudaEvent_t step_done[2] = {};  // compute of the last step that used static area i
-  cudaEvent_t qkv[2] = {}, inp[2] = {}, fwd[2] = {}, dq[2] = {}, bwd[2] = {}, outd[2] = {};
-  int64_t chunk = 0;    // chunks enqueued so far (slot = chunk % 2)
-  int64_t step = 0;     // steps enqueued so far (static area = step % 2)
+  // per slot (only the first pl.nslots exist): compute of the last step that
+  // used static area i; per chunk slot: its inputs copied (q, k, v / all),
+  // its forward, its dQ pass and its whole backward computed, its outputs copied
+  cudaEvent_t step_done[kMaxSlots] = {};
+  cudaEvent_t qkv[kMaxSlots] = {}, inp[kMaxSlots] = {}, fwd[kMaxSlots] = {},
+              dq[kMaxSlots] = {}, bwd[kMaxSlots] = {}, outd[kMaxSlots] = {};
+  int64_t chunk = 0;    // chunks enqueued so far (slot = chunk % nslots)
+  int64_t step = 0;     // steps enqueued so far (static area = step % nslots)
   bool failed = false;  // a step stopped part-way: the slot bookkeeping no longer
                         // matches what was enqueued, so no further step is accepted
 
+  template <typename F>
+  void each_event(F f) {
+    f(&start);
+    f(&stat);
+    f(&end_in);
+    f(&end_out);
+    for (int i = 0; i < pl.nslots; ++i) {
+      f(&step_done[i]);
+      f(&qkv[i]);
+      f(&inp[i]);
+      f(&fwd[i]);
+      f(&dq[i]);
+      f(&bwd[i]);
+      f(&outd[i]);
+    }
+  }
   cudaError_t create() {
     cudaError_t e;
     if ((e = cudaStreamCreateWithFlags(&in, cudaStreamNonBlocking)) != cudaSuccess) return e;
     if ((e = cudaStreamCreateWithFlags(&out, cudaStreamNonBlocking)) != cudaSuccess) return e;
-    for (cudaEvent_t* ev : events())
-      if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) return e;
-    return cudaSuccess;
-  }
-  struct EvList {
-    cudaEvent_t* v[18];
-    cudaEvent_t** begin() { return v; }
-    cudaEvent_t** end() { return v + 18; }
-  };
-  EvList events() {
-    return EvList{{&start, &stat, &end_in, &end_out, &step_done[0], &step_done[1], &qkv[0],
-                   &qkv[1], &inp[0], &inp[1], &fwd[0], &fwd[1], &dq[0], &dq[1], &bwd[0], &bwd[1],
-                   &outd[0], &outd[1]}};
+    e = cudaSuccess;
+    each_event([&](cudaEvent_t* ev) {
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    });
+    return e;
   }
   // A stream or event destroyed with work pending is released once that work completes.
   ~attn_host_session_s() {
-    for (cudaEvent_t* ev : events())
+    each_event([](cudaEvent_t* ev) {
       if (*ev != nullptr) cudaEventDestroy(*ev);
+    });
     if (in != nullptr) cudaStreamDestroy(in);
     if (out != nullptr) cudaStreamDestroy(out);
   }
@@ -229,11 +248,13 @@ attn_status attn_host_session_s::enqueue_step(const attn_host_io* io, cudaStream
   }
   // every step shares the chunk workspace: compute follows the previous step's
   // compute even when the caller passes another stream
-  const int par = (int)(step % 2);
-  if (step >= 1) STEP_CUDA(cudaStreamWaitEvent(cs, step_done[par ^ 1], 0), "stream wait");
-  // key lengths and mask: static area step % 2, free once step - 2 has been computed
+  const int ns = pl.nslots;
+  const int par = (int)(step % ns);
+  if (step >= 1)
+    STEP_CUDA(cudaStreamWaitEvent(cs, step_done[(step - 1) % ns], 0), "stream wait");
+  // key lengths and mask: static area step % n, free once step - n has been computed
   char* stat_area = arena + (size_t)par * pl.stat;
-  if (step >= 2) STEP_CUDA(cudaStreamWaitEvent(in, step_done[par], 0), "stream wait");
+  if (step >= ns) STEP_CUDA(cudaStreamWaitEvent(in, step_done[par], 0), "stream wait");
   if (P.seq_lengths != nullptr)
     STEP_CUDA(cudaMemcpyAsync(stat_area + pl.lens_off, P.seq_lengths, (size_t)P.B * 4, H2D, in),
               "key lengths copy-in");
@@ -250,7 +271,7 @@ attn_status attn_host_session_s::enqueue_step(const attn_host_io* io, cudaStream
       const int n = (P.Hkv - g0) < pl.U ? (P.Hkv - g0) : pl.U;
       const int hq_n = n * pl.G;
       const int nb = pl.NB;
-      const int s = (int)(chunk % 2);
+      const int s = (int)(chunk % ns);
       char* S = arena + pl.slot_off + (size_t)s * pl.slot;
       const int32_t* lens =
           P.seq_lengths ? reinterpret_cast<const int32_t*>(stat_area + pl.lens_off) + b : nullptr;
@@ -267,8 +288,8 @@ attn_status attn_host_session_s::enqueue_step(const attn_host_io* io, cudaStream
       const size_t nq = (size_t)nb * hq_n * P.Sq * P.D, nk = (size_t)nb * n * P.Skv * P.D;
       const size_t nl = (size_t)nb * hq_n * P.Sq;
 
-      // copy-in: the slot's inputs are free once chunk - 2 has been computed
-      if (chunk >= 2) STEP_CUDA(cudaStreamWaitEvent(in, bwd[s], 0), "stream wait");
+      // copy-in: the slot's inputs are free once chunk - n has been computed
+      if (chunk >= ns) STEP_CUDA(cudaStreamWaitEvent(in, bwd[s], 0), "stream wait");
       STEP_CUDA(cudaMemcpyAsync(S + pl.s_q, hq + eq * 2, nq * 2, H2D, in), "q copy-in");
       STEP_CUDA(cudaMemcpyAsync(S + pl.s_k, hk + ek * 2, nk * 2, H2D, in), "k copy-in");
       STEP_CUDA(cudaMemcpyAsync(S + pl.s_v, hv + ek * 2, nk * 2, H2D, in), "v copy-in");
@@ -276,7 +297,7 @@ attn_status attn_host_session_s::enqueue_step(const attn_host_io* io, cudaStream
       STEP_CUDA(cudaMemcpyAsync(S + pl.s_do, hdo + eq * 2, nq * 2, H2D, in), "dout copy-in");
       STEP_CUDA(cudaEventRecord(inp[s], in), "event record");
 
-      // compute: the slot's outputs are free once chunk - 2 has been copied out
+      // compute: the slot's outputs are free once chunk - n has been copied out
       const attn_tensor q = dev_view(S + pl.s_q, hq_n, P.Sq, P.D);
       const attn_tensor k = dev_view(S + pl.s_k, n, P.Skv, P.D);
       const attn_tensor v = dev_view(S + pl.s_v, n, P.Skv, P.D);
@@ -288,7 +309,7 @@ attn_status attn_host_session_s::enqueue_step(const attn_host_io* io, cudaStream
       float* lse = reinterpret_cast<float*>(S + pl.s_lse);
       void* ws = arena + pl.ws_off;
       STEP_CUDA(cudaStreamWaitEvent(cs, qkv[s], 0), "stream wait");
-      if (chunk >= 2) STEP_CUDA(cudaStreamWaitEvent(cs, outd[s], 0), "stream wait");
+      if (chunk >= ns) STEP_CUDA(cudaStreamWaitEvent(cs, outd[s], 0), "stream wait");
       if ((st = attn::fwd_with_split(&sp, pl.fsplit, q, k, v, o, lse, ws, pl.ws, cs)) != ATTN_OK)
         return st;
       STEP_CUDA(cudaEventRecord(fwd[s], cs), "event record");
@@ -359,23 +380,28 @@ attn_status check_arena(const Plan& pl, void* arena, size_t arena_bytes) {
 
 extern "C" {
 
-attn_status attn_train_step_host_arena_size(const attn_problem* p, int kv_heads_per_chunk,
-                                            size_t* bytes) {
+attn_status attn_train_host_session_arena_size(const attn_problem* p, int kv_heads_per_chunk,
+                                               int slots, size_t* bytes) {
   Plan pl;
-  attn_status st = make_plan(p, kv_heads_per_chunk, &pl);
+  attn_status st = make_plan(p, kv_heads_per_chunk, slots, &pl);
   if (st != ATTN_OK) return st;
   if (bytes == nullptr) return err(ATTN_ERR_INVALID, "bytes is NULL");
   *bytes = pl.total;
   return ATTN_OK;
 }
 
-attn_status attn_train_host_session_create(const attn_problem* p, int kv_heads_per_chunk,
-                                           void* arena, size_t arena_bytes,
-                                           attn_host_session* out) {
+attn_status attn_train_step_host_arena_size(const attn_problem* p, int kv_heads_per_chunk,
+                                            size_t* bytes) {
+  return attn_train_host_session_arena_size(p, kv_heads_per_chunk, 2, bytes);
+}
+
+attn_status attn_train_host_session_create_slots(const attn_problem* p, int kv_heads_per_chunk,
+                                                 int slots, void* arena, size_t arena_bytes,
+                                                 attn_host_session* out) {
   if (out == nullptr) return err(ATTN_ERR_INVALID, "out is NULL");
   *out = nullptr;
   Plan pl;
-  attn_status st = make_plan(p, kv_heads_per_chunk, &pl);
+  attn_status st = make_plan(p, kv_heads_per_chunk, slots, &pl);
   if (st != ATTN_OK) return st;
   if ((st = check_arena(pl, arena, arena_bytes)) != ATTN_OK) return st;
   attn_host_session_s* s = new (std::nothrow) attn_host_session_s();
@@ -390,6 +416,12 @@ attn_status attn_train_host_session_create(const attn_problem* p, int kv_heads_p
   }
   *out = s;
   return ATTN_OK;
+}
+
+attn_status attn_train_host_session_create(const attn_problem* p, int kv_heads_per_chunk,
+                                           void* arena, size_t arena_bytes,
+                                           attn_host_session* out) {
+  return attn_train_host_session_create_slots(p, kv_heads_per_chunk, 2, arena, arena_bytes, out);
 }
 
 attn_status attn_train_host_session_step(attn_host_session s, const attn_host_io* io,
@@ -423,7 +455,7 @@ attn_status attn_train_step_host(const attn_problem* p, const attn_host_io* io,
   if (st != ATTN_OK) {
     // report a malformed problem first, as the other entry points do
     Plan pl;
-    attn_status pst = make_plan(p, kv_heads_per_chunk, &pl);
+    attn_status pst = make_plan(p, kv_heads_per_chunk, 2, &pl);
     return pst != ATTN_OK ? pst : check_io(io);
   }
   attn_host_session s = nullptr;

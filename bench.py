@@ -37,6 +37,10 @@ METRIC = "attention fwd+bwd TFLOPS (mask-aware, bf16) and % of GB300 tensor peak
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TTT_ALL = "eagle3_ttt_steps0-6"
+# Host-device copies on GB300 (Grace host) pause for 20-80 ms about twice a
+# second; the end-to-end session gets enough slots to keep computing through
+# a pause this long
+E2E_RIDE_MS = 80.0
 
 
 def bench_workloads():
@@ -77,6 +81,11 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-chunk", type=int, default=0,
                     help="kv heads per chunk of the host-memory step (0 = automatic)")
+    ap.add_argument("--e2e-slots", type=int, default=0,
+                    help="device slots of the host-memory session (0 = enough for about "
+                         f"{E2E_RIDE_MS:.0f} ms of compute, at most 16)")
+    ap.add_argument("--e2e-seconds", type=float, default=1.0,
+                    help="length of each timed end-to-end region")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     return ap.parse_args()
@@ -363,6 +372,8 @@ class Runner:
         self.flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > 129 MB L2
         self.hosts = None
         self.h2d = self.d2h = 0
+        self.step_ms = None  # device-only time per step, once timed
+        self.e2e_slots = self.e2e_count = None
         self.launches_per_step = sum(c.launches for c in self.cases)
         for _ in range(max(args.warmup, 3)):
             for c in self.cases:
@@ -421,6 +432,7 @@ class Runner:
                 dist.barrier()
             self.binding.device_status()
             total_ms, = max_over_ranks([total_ms], dist, dev)
+            self.step_ms = total_ms / K
             return {"total_ms": total_ms, "per_kernel_ms": per_kernel, "clocks": clk.summary()}
         evsets = [[[torch.cuda.Event(enable_timing=True) for _ in range(len(c.names) + 1)]
                    for c in self.cases] for _ in range(K)]
@@ -442,7 +454,24 @@ class Runner:
                 for j, n in enumerate(c.names):
                     per_kernel[n] = per_kernel.get(n, 0.0) + evs[j].elapsed_time(evs[j + 1])
         total_ms, = max_over_ranks([total_ms], dist, dev)
+        self.step_ms = total_ms / K
         return {"total_ms": total_ms, "per_kernel_ms": per_kernel, "clocks": clk.summary()}
+
+    def _pick_slots(self, hps):
+        """Slots of the sessions: enough for E2E_RIDE_MS of compute (the device
+        step time measured by timed()), within a quarter of the free memory."""
+        import math
+
+        import torch
+        b, args = self.binding, self.args
+        if args.e2e_slots:
+            return args.e2e_slots
+        est = self.step_ms or 8.0
+        n = min(b.HOST_MAX_SLOTS, max(2, math.ceil(E2E_RIDE_MS / est) + 1))
+        free, _ = torch.cuda.mem_get_info(self.dev)
+        while n > 2 and sum(b.step_host_arena_size(hp, args.e2e_chunk, n) for hp in hps) > free / 4:
+            n -= 1
+        return n
 
     def _open_sessions(self):
         # end to end through the C ABI's host-memory session (attn_train_host_session_*):
@@ -451,8 +480,10 @@ class Runner:
         # same and the neighbouring steps, and the timed region ends after the last
         # step's copies (join + synchronize)
         import torch
+        import math
         b, args = self.binding, self.args
         self.hosts = []
+        staged = []
         for c in self.cases:
             w = c.w
             pin = {n: c.x[n].pin_memory()
@@ -462,34 +493,45 @@ class Runner:
             hp = b.problem(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.mask, w.ttt_step, 0.0, args.out,
                            w.window, pin.get("seq_lengths"), pin.get("add_mask"), host=True)
             io = {"q": pin["q"], "k": pin["k"], "v": pin["v"], "dout": pin["dout"], **outs}
-            arena = torch.empty(b.step_host_arena_size(hp, args.e2e_chunk), dtype=torch.uint8,
-                                device=self.dev)
-            self.hosts.append((b.HostSession(hp, arena, args.e2e_chunk), io))
+            staged.append((hp, io, pin))
             self.h2d += sum(t.numel() * t.element_size() for t in pin.values())
             self.d2h += sum(t.numel() * t.element_size() for t in outs.values())
-        self._e2e_steps(2)  # warm-up
+        self.e2e_slots = n = self._pick_slots([hp for hp, _, _ in staged])
+        for hp, io, pin in staged:
+            arena = torch.empty(b.step_host_arena_size(hp, args.e2e_chunk, n), dtype=torch.uint8,
+                                device=self.dev)
+            self.hosts.append((b.HostSession(hp, arena, args.e2e_chunk, n), io, pin))
+        # timed steps: about args.e2e_seconds of device time
+        est = self.step_ms or 8.0
+        self.e2e_count = max(3, min(1000, math.ceil(args.e2e_seconds * 1e3 / est)))
+        self._e2e_steps(2)  # first use of the sessions
 
     def _e2e_steps(self, n):
         for _ in range(n):
-            for sess, io in self.hosts:
+            for sess, io, _ in self.hosts:
                 sess.step(io, self.stream.cuda_stream)
-        for sess, _ in self.hosts:
+        for sess, _, _ in self.hosts:
             sess.join(self.stream.cuda_stream)
 
     def e2e(self):
-        """Milliseconds for K end-to-end steps (at most 20 run; scaled to K) and
-        the clocks sampled meanwhile."""
+        """Milliseconds for K end-to-end steps (e2e_count steps run, about a
+        second, scaled to K) and the clocks sampled meanwhile.  The sampler
+        starts first and the warm-up steps (one per slot) run right before the
+        timed ones: the first copies after an idle host link are slow, and the
+        link pauses about twice a second under load, so the region neither
+        starts cold nor is short enough to miss or catch a pause by chance."""
         import torch
         if self.hosts is None:
             self._open_sessions()
         dev, dist, K = self.dev, self.dist, self.args.steps
-        torch.cuda.synchronize(dev)
+        Ke = self.e2e_count
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        if dist:
-            dist.barrier()
         torch.cuda.synchronize(dev)
-        Ke = max(3, min(K, 20))
         with ClockSampler(gpu_index_for(self.local_rank)) as clk:
+            self._e2e_steps(max(3, self.e2e_slots))  # warm-up (outside the events)
+            torch.cuda.synchronize(dev)
+            if dist:
+                dist.barrier()
             e0.record(self.stream)
             self._e2e_steps(Ke)
             e1.record(self.stream)
@@ -499,7 +541,7 @@ class Runner:
         return {"ms": ms, "clocks": clk.summary()}
 
     def close(self):
-        for sess, _ in self.hosts or []:
+        for sess, _, _ in self.hosts or []:
             sess.close()
         self.hosts = None
         for gev in self.gevs or []:
@@ -941,7 +983,9 @@ def main():
             e_med = e[(len(e) - 1) // 2]
             line["e2e"] = {"value": job_value(F, K, e_med, n_gpus), "unit": UNIT,
                            "h2d_bytes_per_step": runners[name].h2d,
-                           "d2h_bytes_per_step": runners[name].d2h}
+                           "d2h_bytes_per_step": runners[name].d2h,
+                           "steps_timed": runners[name].e2e_count,
+                           "slots": runners[name].e2e_slots}
             line["repeats"]["e2e_ms_per_step"] = {"median": e_med / K, "min": e[0] / K,
                                                   "max": e[-1] / K}
             line["e2e_clocks"] = merge_clocks([x["clocks"] for x in e2es[name]])

@@ -262,15 +262,16 @@ attn_status attn_train_bwd_noalloc(const attn_problem* p, attn_tensor q, attn_te
  * serializes them.
  *
  * arena: caller-owned device buffer of at least
- * attn_train_step_host_arena_size bytes, 256-byte aligned, contents ignored.
- * It holds two slots of chunk buffers (see below), two copies of the key
- * lengths and mask, and the backward's workspace; the library allocates no
- * device memory.
+ * attn_train_step_host_arena_size bytes (attn_train_host_session_arena_size
+ * for a session with more slots), 256-byte aligned, contents ignored.  It
+ * holds the slots of chunk buffers (two by default; see below), as many
+ * copies of the key lengths and mask, and the backward's workspace; the
+ * library allocates no device memory.
  *
  * Pipelining.  A step is one chunk (kv_heads_per_chunk <= 0: the whole
  * problem), or chunks of kv_heads_per_chunk kv heads (1 to Hkv, with their
  * Hq/Hkv query heads each) of one batch entry; GQA groups are independent
- * problems and contiguous slices of the host arrays.  Chunks take the two
+ * problems and contiguous slices of the host arrays.  Chunks take the
  * slots in turn, also across the steps of a session.  Per chunk, on three
  * streams: its inputs are copied in while the previous chunk computes; O and
  * LSE are copied out during its backward; the backward runs Delta prep and dQ
@@ -280,6 +281,18 @@ attn_status attn_train_bwd_noalloc(const attn_problem* p, attn_tensor q, attn_te
  * step at the price of fuller kernel tails.  No kernel mixes heads, so the
  * results equal those of attn_train_fwd + attn_train_bwd on the whole problem
  * bit for bit.
+ *
+ * Slots.  A slot holds the device copies of one chunk's inputs and outputs.
+ * With n slots, chunk c's copy-in may start once chunk c - n has been
+ * computed, and chunk c's kernels may start once chunk c - n has been copied
+ * out: the copies can run up to n - 1 chunks ahead of (inputs) or behind
+ * (outputs) the kernels.  Two slots suffice while the host link delivers at
+ * a steady rate.  More slots let the kernels ride through pauses of the host
+ * copies: on GB300 (Grace host) copies of a few hundred MB were measured to
+ * stall for 20-80 ms about twice a second, in either direction, on one or
+ * two streams; n slots absorb a pause of about (n - 1) chunks of compute,
+ * and the copies then catch up at the rate by which they are faster than
+ * the kernels.  Results do not depend on n.
  *
  * Streams.  Compute is enqueued on `stream`; the copies run on two streams of
  * the session.  The first step waits for the work already on `stream` (the
@@ -303,10 +316,18 @@ typedef struct {
 
 typedef struct attn_host_session_s* attn_host_session;
 
+/* Largest slot count of a host-memory session. */
+#define ATTN_HOST_MAX_SLOTS 16
+
 /* Arena bytes for this problem and chunk size (kv_heads_per_chunk <= 0: one
- * chunk for the whole step). */
+ * chunk for the whole step), with two slots. */
 attn_status attn_train_step_host_arena_size(const attn_problem* p, int kv_heads_per_chunk,
                                             size_t* bytes);
+/* The same for a session of `slots` slots (2 to ATTN_HOST_MAX_SLOTS; other
+ * values return ATTN_ERR_INVALID).  Each slot adds the device copies of one
+ * chunk's inputs and outputs and one copy of the key lengths and mask. */
+attn_status attn_train_host_session_arena_size(const attn_problem* p, int kv_heads_per_chunk,
+                                               int slots, size_t* bytes);
 
 /* One step: create a session, enqueue the step, join `stream`, release the
  * session.  The outputs are valid once `stream` has been synchronized. */
@@ -320,6 +341,12 @@ attn_status attn_train_step_host(const attn_problem* p, const attn_host_io* io,
 attn_status attn_train_host_session_create(const attn_problem* p, int kv_heads_per_chunk,
                                            void* arena, size_t arena_bytes,
                                            attn_host_session* out);
+/* A session with `slots` slots (2 to ATTN_HOST_MAX_SLOTS) over an arena of
+ * at least attn_train_host_session_arena_size(p, kv_heads_per_chunk, slots)
+ * bytes; attn_train_host_session_create is the two-slot form. */
+attn_status attn_train_host_session_create_slots(const attn_problem* p, int kv_heads_per_chunk,
+                                                 int slots, void* arena, size_t arena_bytes,
+                                                 attn_host_session* out);
 /* Enqueues one step (copy-in, forward, backward, copy-out).  Arguments are
  * checked before anything is enqueued; a failure after that (a CUDA error)
  * leaves the session unusable: later steps return ATTN_ERR_INVALID, and the

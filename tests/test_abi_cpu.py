@@ -140,6 +140,25 @@ def test_step_host_arena_size(lib):
             == 2 * (_up(2 * 4) + _up((99 * 104 + 100) * 2)) + mask_ws)
 
 
+def test_host_session_arena_size_grows_by_one_slot_per_slot(lib):
+    """n slots: n chunk slots and n copies of the key lengths and mask; the
+    two-slot form equals attn_train_step_host_arena_size."""
+    lens = torch.tensor([100, 50], dtype=torch.int32)
+    am = torch.zeros(100, 104, dtype=torch.bfloat16)[:, :100]
+    p = binding.problem(2, 4, 2, 100, 100, 64, "full", seq_lengths=lens, add_mask=am, out="fp32",
+                        host=True)
+    nq, nk, nl = 2 * 100 * 64, 100 * 64, 2 * 100  # one kv head of one batch entry
+    slot = 2 * _up(nq * 2) + 2 * _up(nk * 2) + 2 * _up(nq * 4) + 2 * _up(nk * 4) + _up(nl * 4)
+    stat = _up(2 * 4) + _up((99 * 104 + 100) * 2)
+    two = binding.step_host_arena_size(p, 1)
+    assert binding.step_host_arena_size(p, 1, 2) == two
+    for n in (3, 8, binding.HOST_MAX_SLOTS):
+        assert binding.step_host_arena_size(p, 1, n) == two + (n - 2) * (slot + stat)
+    for bad in (0, 1, binding.HOST_MAX_SLOTS + 1):
+        with pytest.raises(binding.AttnError, match="slots"):
+            binding.step_host_arena_size(p, 1, bad)
+
+
 def test_plain_c_client(lib, tmp_path):
     """The header is plain C: a C99 program includes it, links the library and
     calls the host-side entry points (validation, sizes, error messages)."""

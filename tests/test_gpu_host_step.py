@@ -92,14 +92,38 @@ def test_step_host_back_to_back_calls_reuse_arena():
         assert torch.equal(got2[n], ref2[n]), n
 
 
-@pytest.mark.parametrize("chunk", [0, 1])
+@pytest.mark.parametrize("slots,chunk", [(2, 0), (2, 1), (4, 0), (4, 1)])
 @pytest.mark.parametrize("w", [CASES[0], CASES[3], CASES[4]], ids=lambda w: w.name)
-def test_session_steps_overlap_and_match(w, chunk):
-    """A session of three steps on different inputs with one join at the end:
-    the copies of each step overlap its neighbours' kernels and share the arena's
-    two slots, yet every step's outputs equal the device path's."""
+def test_session_steps_overlap_and_match(w, chunk, slots):
+    """A session of several steps on different inputs with one join at the end:
+    the copies of each step overlap its neighbours' kernels and rotate through
+    the arena's slots (more steps than slots, so every slot is reused), yet
+    every step's outputs equal the device path's."""
+    _session_matches(w, chunk, slots, 3 if slots == 2 else slots + 2)
+
+
+def test_session_with_the_most_slots():
+    """ATTN_HOST_MAX_SLOTS slots, eight chunks per step (two batch entries of
+    four kv heads): six steps (48 chunks) wrap the slot rotation twice."""
+    _session_matches(CASES[3].with_(B=2, seq_lengths=(384, 130)), 1, binding.HOST_MAX_SLOTS, 6)
+
+
+def test_session_rejects_slot_counts_outside_the_range():
     dev = torch.device("cuda:0")
-    xs = [synth.make_inputs(w, seed=w.seed + 100 * i) for i in range(3)]
+    w = CASES[0]
+    p = binding.problem(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.mask, host=True)
+    arena = torch.empty(binding.step_host_arena_size(p, 0, 3), dtype=torch.uint8, device=dev)
+    for bad in (1, binding.HOST_MAX_SLOTS + 1):
+        with pytest.raises(binding.AttnError, match="slots"):
+            binding.HostSession(p, arena, 0, bad)
+    # an arena sized for three slots is too small for four
+    with pytest.raises(binding.AttnError, match="arena too small"):
+        binding.HostSession(p, arena, 0, 4)
+
+
+def _session_matches(w, chunk, slots, n_steps):
+    dev = torch.device("cuda:0")
+    xs = [synth.make_inputs(w, seed=w.seed + 100 * i) for i in range(n_steps)]
     for x in xs[1:]:  # a session's mask is fixed; q, k, v, dO differ per step
         if "add_mask" in x:
             x["add_mask"] = xs[0]["add_mask"]
@@ -115,9 +139,9 @@ def test_session_steps_overlap_and_match(w, chunk):
             assert torch.equal(x["seq_lengths"], lens)
     p = binding.problem(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.mask, w.ttt_step, 0.0, "fp32",
                         w.window, lens, am, host=True)
-    arena = torch.full((binding.step_host_arena_size(p, chunk),), 0xFF, dtype=torch.uint8,
+    arena = torch.full((binding.step_host_arena_size(p, chunk, slots),), 0xFF, dtype=torch.uint8,
                        device=dev)
-    sess = binding.HostSession(p, arena, chunk)
+    sess = binding.HostSession(p, arena, chunk, slots)
     ios = []
     for x in xs:
         io = {n: x[n].contiguous().pin_memory() for n in ("q", "k", "v", "dout")}
