@@ -22,7 +22,8 @@ STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID", 2: "ATTN_ERR_UNSUPPORTED", 3: "AT
           7: "ATTN_ERR_DEVICE_CHECK"}
 
 # Entry points of include/attn_train.h (checked against the header by the tests).
-EXPORTS = ("attn_train_supports", "attn_train_workspace_size", "attn_train_fwd",
+EXPORTS = ("attn_train_supports", "attn_train_describe", "attn_train_workspace_size",
+           "attn_train_fwd",
            "attn_train_fwd_workspace_size", "attn_train_fwd_ws", "attn_train_bwd",
            "attn_train_bwd_passes", "attn_train_bwd_noalloc", "attn_train_last_error", "attn_train_device_status", "attn_train_set_wait_budget_ns",
            "attn_train_mask_pattern", "attn_train_probe_mma", "attn_train_selftest_wait_timeout",
@@ -110,6 +111,8 @@ def load(path: str = LIB_PATH):
                                           ctypes.c_size_t, vp]),
             "attn_train_host_session_create": (st, [P, ctypes.c_int, vp, ctypes.c_size_t,
                                                     ctypes.POINTER(vp)]),
+            "attn_train_describe": (st, [P, ctypes.c_char_p, ctypes.c_size_t,
+                                         ctypes.POINTER(ctypes.c_size_t)]),
             "attn_train_host_session_arena_size": (st, [P, ctypes.c_int, ctypes.c_int,
                                                         ctypes.POINTER(ctypes.c_size_t)]),
             "attn_train_host_session_create_slots": (st, [P, ctypes.c_int, ctypes.c_int, vp,
@@ -207,6 +210,20 @@ def supports(p: Problem) -> bool:
 
 def check_supported(p: Problem):
     _check(load().attn_train_supports(ctypes.byref(p)))
+
+
+def describe(p: Problem) -> dict:
+    """attn_train_describe: the kernels, tiles, grids and pipeline depths the
+    entry points use for this problem (a host-side plan, no device work)."""
+    import json
+    lib = load()
+    n = ctypes.c_size_t(0)
+    lib.attn_train_describe(ctypes.byref(p), None, 0, ctypes.byref(n))
+    if n.value == 0:
+        _check(lib.attn_train_describe(ctypes.byref(p), None, 0, ctypes.byref(n)))
+    buf = ctypes.create_string_buffer(n.value)
+    _check(lib.attn_train_describe(ctypes.byref(p), buf, n.value, ctypes.byref(n)))
+    return json.loads(buf.value.decode())
 
 
 def workspace_size(p: Problem) -> int:

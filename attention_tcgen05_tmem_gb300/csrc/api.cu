@@ -351,6 +351,65 @@ attn_status attn_train_fwd_ws(const attn_problem* p, attn_tensor q, attn_tensor 
   return attn::fwd_with_split(p, split, q, k, v, o, lse, workspace, ws_bytes, stream);
 }
 
+attn_status attn_train_describe(const attn_problem* p, char* buf, size_t buf_len, size_t* needed) {
+  attn_status st = check_problem(p);
+  if (st != ATTN_OK) return st;
+  const Dims d = make_dims(p);
+  const int D = d.D;
+  const int W = needs_general_mask(d) ? 1 : 0;
+  const int M = d.addm != nullptr ? 1 : 0;
+  const int t = d.geom.ttt;
+  const attn::FwdSplit sp = attn::fwd_split_plan(d);
+  const attn::FwdShape fs = attn::fwd_shape(d);
+  const attn::BwdShape bs = attn::bwd_shape(D);
+  const int64_t n_qp = (p->Sq + 2 * attn::kBM - 1) / (2 * attn::kBM);
+  const int64_t fwd_ctas = n_qp * p->B * p->Hq * (sp.split > 0 ? sp.nchunk : 1);
+  const int64_t dkdv_ctas = (int64_t)((d.geom.kv_main + attn::kBN - 1) / attn::kBN) * p->B * p->Hkv;
+  const int64_t dq_ctas = (int64_t)((p->Sq + attn::kBM - 1) / attn::kBM) * p->B * p->Hq;
+  const char* mask = p->mask == ATTN_MASK_FULL     ? "full"
+                     : p->mask == ATTN_MASK_CAUSAL ? "causal"
+                     : p->mask == ATTN_MASK_TTT    ? "ttt"
+                                                   : "window";
+  const int ch = t <= 1 ? 1 : t <= 2 ? 2 : t <= 4 ? 4 : 8;
+  char out[2048];
+  int n = snprintf(
+      out, sizeof(out),
+      "{\"head_dim\":%d,\"mask\":\"%s\",\"ttt_step\":%d,\"general_mask\":%s,"
+      "\"additive_mask\":%s,\"outputs\":\"%s\","
+      "\"fwd\":{\"kernel\":\"fwd_kernel<%d,%d,%d,%d>\",\"rows_per_cta\":%d,"
+      "\"keys_per_tile\":%d,\"ctas\":%lld,\"kv_ring\":%d,\"score_buffers\":%d,"
+      "\"smem_bytes\":%d,\"split_key_tiles\":%d,\"split_chunks\":%d,"
+      "\"merge_pass\":%s,\"ttt_scores_prepass\":%s},"
+      "\"bwd_prep\":{\"kernel\":\"bwd_prep_kernel<%d,%d>\",\"rows\":%lld},"
+      "\"bwd_dkdv\":{\"kernel\":\"bwd_dkdv_kernel<%d,%d,%d>\",\"keys_per_cta\":%d,"
+      "\"queries_per_tile\":%d,\"ctas\":%lld,\"q_do_stages\":%d,\"smem_bytes\":%d},"
+      "\"bwd_dq\":{\"kernel\":\"bwd_dq_kernel<%d,%d,%d>\",\"rows_per_cta\":%d,"
+      "\"keys_per_tile\":%d,\"ctas\":%lld,\"k_ring\":%d,\"v_ring\":%d,\"smem_bytes\":%d}",
+      D, mask, t, W ? "true" : "false", M ? "true" : "false",
+      d.out_f32 ? "fp32" : "bf16", D, W, M, sp.split > 0 ? 1 : 0, 2 * attn::kBM, attn::kBN,
+      (long long)fwd_ctas, fs.ring, fs.three_buffers ? 3 : 2, fs.smem, sp.split, sp.nchunk,
+      sp.split > 0 ? "true" : "false",
+      (t > 0 && t * 4 <= D * (d.out_f32 ? 4 : 2)) ? "true" : "false", D, t > 0 ? 1 : 0,
+      (long long)p->B * p->Hq * p->Sq, D, W, M, attn::kBN, attn::kBM, (long long)dkdv_ctas,
+      bs.dkdv_stages, bs.dkdv_smem, D, W, M, attn::kBM, attn::kBN, (long long)dq_ctas,
+      bs.dq_k_ring, bs.dq_v_ring, bs.dq_smem);
+  if (t > 0 && n > 0 && n < (int)sizeof(out))
+    n += snprintf(out + n, sizeof(out) - (size_t)n,
+                  ",\"ttt_suffix\":{\"kernel\":\"ttt_diag_bwd_kernel<%d,%d>\","
+                  "\"key_rows\":%lld}",
+                  D, ch, (long long)p->B * p->Hkv * p->Sq);
+  if (M && n > 0 && n < (int)sizeof(out))
+    n += snprintf(out + n, sizeof(out) - (size_t)n,
+                  ",\"mask_transpose\":{\"kernel\":\"mask_transpose_kernel\"}");
+  if (n > 0 && n < (int)sizeof(out)) n += snprintf(out + n, sizeof(out) - (size_t)n, "}");
+  if (n <= 0 || n >= (int)sizeof(out)) return fail(ATTN_ERR_INVALID, "description too long");
+  if (needed != nullptr) *needed = (size_t)n + 1;
+  if (buf == nullptr || buf_len < (size_t)n + 1)
+    return fail(ATTN_ERR_INVALID, "describe: buffer of %zu bytes, %d needed", buf_len, n + 1);
+  memcpy(buf, out, (size_t)n + 1);
+  return ATTN_OK;
+}
+
 }  // extern "C"
 
 namespace attn {

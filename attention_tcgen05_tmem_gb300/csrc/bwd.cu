@@ -1211,6 +1211,22 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const Maps& m, unsigned passes, cudaS
 
 }  // namespace
 
+// Pipeline depths of the backward's tensor-core passes, for the plan description.
+template <int D>
+BwdShape bwd_shape_d() {
+  BwdShape b;
+  b.dkdv_stages = DkdvLayout<D>::NST;
+  b.dq_k_ring = DqLayout<D>::NK;
+  b.dq_v_ring = DqLayout<D>::NV;
+  b.dkdv_smem = DkdvLayout<D>::ALLOC;
+  b.dq_smem = DqLayout<D>::ALLOC;
+  return b;
+}
+BwdShape bwd_shape(int D) {
+  return D == 128 ? bwd_shape_d<128>() : D == 64 ? bwd_shape_d<64>()
+         : D == 32 ? bwd_shape_d<32>() : bwd_shape_d<16>();
+}
+
 cudaError_t launch_bwd(const BwdArgs& a, const Maps& m, unsigned passes, cudaStream_t s) {
   switch (a.d.D) {
     case 16: return launch_bwd_d<16>(a, m, passes, s);

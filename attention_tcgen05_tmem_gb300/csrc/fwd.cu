@@ -70,6 +70,20 @@ FwdSplit fwd_split_with(const Dims& d, int split) {
   return sp;
 }
 
+// Depth of the forward's K/V ring (entries of one 128-key K or V tile) and
+// whether the three-buffer score rotation is used, for the plan description.
+FwdShape fwd_shape(const Dims& d) {
+  FwdShape f;
+  f.ring = d.D == 128 ? FwdLayout<128>::NSLOT
+           : d.D == 64 ? FwdLayout<64>::NSLOT
+           : d.D == 32 ? FwdLayout<32>::NSLOT : FwdLayout<16>::NSLOT;
+  f.three_buffers = needs_general_mask(d) && d.D <= 64;
+  f.smem = d.D == 128 ? FwdLayout<128>::ALLOC
+           : d.D == 64 ? FwdLayout<64>::ALLOC
+           : d.D == 32 ? FwdLayout<32>::ALLOC : FwdLayout<16>::ALLOC;
+  return f;
+}
+
 cudaError_t launch_fwd(const FwdArgs& a, const Maps& m, cudaStream_t s) {
   return a.split > 0 ? launch_fwd_split(a, m, s) : launch_fwd_any<false>(a, m, s);
 }

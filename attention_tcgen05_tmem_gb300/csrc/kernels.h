@@ -109,6 +109,18 @@ struct LossArgs {
 cudaError_t launch_logsoftmax_loss_fwd(const LossArgs& a, cudaStream_t s);
 cudaError_t launch_logsoftmax_loss_bwd(const LossArgs& a, cudaStream_t s);
 
+// Pipeline shapes of the kernels a problem runs (attn_train_describe).
+struct FwdShape {
+  int ring = 0;                // K/V ring entries (128-key K or V tiles)
+  bool three_buffers = false;  // three rotating score buffers (general masks, D <= 64)
+  int smem = 0;                // dynamic shared memory per CTA, bytes
+};
+FwdShape fwd_shape(const Dims& d);
+struct BwdShape {
+  int dkdv_stages = 0, dq_k_ring = 0, dq_v_ring = 0, dkdv_smem = 0, dq_smem = 0;
+};
+BwdShape bwd_shape(int D);
+
 cudaError_t launch_fwd(const FwdArgs& a, const Maps& m, cudaStream_t s);
 // The split forward (a.split > 0) and its merge pass (fwd_split.cu).
 cudaError_t launch_fwd_split(const FwdArgs& a, const Maps& m, cudaStream_t s);

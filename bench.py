@@ -670,6 +670,46 @@ def merge_clocks(samples):
             "samples": sum(c["samples"] for c in got)}
 
 
+def kernel_plan(runner):
+    """The kernels, tiles, grids and pipeline depths the library uses for each
+    problem of the workload (attn_train_describe on the timed problems)."""
+    plans = [runner.binding.describe(c.p) for c in runner.cases]
+    return plans[0] if len(plans) == 1 else plans
+
+
+def run_env(device):
+    """GPU, driver, runtime and host the line was measured on."""
+    import platform
+
+    import torch
+    env = {"torch": torch.__version__, "cuda_runtime": torch.version.cuda,
+           "host_cores": os.cpu_count(), "host_arch": platform.machine()}
+    try:
+        prop = torch.cuda.get_device_properties(device)
+        env.update({"gpu": prop.name, "sms": prop.multi_processor_count,
+                    "gpu_mem_gib": round(prop.total_memory / 2**30, 1)})
+    except Exception:  # noqa: BLE001 -- descriptive only
+        pass
+    try:
+        r = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader",
+                            "-i", gpu_index_for(device)], capture_output=True, text=True,
+                           timeout=20)
+        if r.returncode == 0 and r.stdout.strip():
+            env["driver"] = r.stdout.strip().splitlines()[0]
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                key = ln.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "cpu part"):
+                    env["host_cpu"] = ln.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return env
+
+
 def describe(name, ws, out, n_gpus):
     cfg = dict(ws[0].describe()) if len(ws) == 1 else {
         "workload": name, "B": ws[0].B, "Hq": ws[0].Hq, "Hkv": ws[0].Hkv, "Sq": ws[0].Sq,
@@ -923,8 +963,10 @@ def main():
         for _ in range(args.repeats):
             for name in names:
                 e2es[name].append(runners[name].e2e())
+    plans = {name: kernel_plan(runners[name]) for name in names}
     for name in names:
         runners[name].close()
+    env = run_env(local_rank)
     for name in names:
         ws = table[name]
         F = sum(flops.flops_fwd_bwd(w) for w in ws)
@@ -972,6 +1014,8 @@ def main():
             "hbm_gbs_algorithmic": alg_bytes / (r["total_ms"] / K * 1e-3) / 1e9,
             "kernel_ms": {n: v / K for n, v in pk.items()},
             "roofline": roof,
+            "kernels": plans[name],
+            "env": env,
             "gpu_launches": runners[name].launches_per_step * K,
             "clocks": clocks,
             "repeats": {"n": len(totals), "steps_each": K,

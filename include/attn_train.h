@@ -191,6 +191,22 @@ attn_status attn_train_bwd(const attn_problem* p, attn_tensor q, attn_tensor k, 
                            attn_tensor dk, attn_tensor dv, void* workspace, size_t ws_bytes,
                            void* stream);
 
+/* The kernels a problem runs, as one JSON object (NUL-terminated) in `buf`:
+ * per pass the kernel instantiation (head dim and, for the attention kernels,
+ * whether the general-mask, additive-mask and split forms are used), the rows
+ * and keys a CTA or a tile covers, the grid size, the pipeline depths (K/V ring
+ * entries, Q/dO stages) and the dynamic shared memory per CTA; the forward's
+ * key-range split (it applies when attn_train_fwd_ws is given a workspace);
+ * the TTT suffix pass and the mask transpose when the problem has them.  Pure
+ * host function: it reports the plan the entry points follow for *p, for
+ * logs and benchmark records.  `needed` (may be NULL) receives the size the
+ * description takes, NUL included; a NULL or smaller `buf` returns
+ * ATTN_ERR_INVALID (after setting `needed`).  Same problem checks as
+ * attn_train_supports.  The pages have no counterpart: it is the record of the
+ * resolved kernel variant, tile sizes and stage counts that the benchmark lines
+ * carry. */
+attn_status attn_train_describe(const attn_problem* p, char* buf, size_t buf_len, size_t* needed);
+
 /* The backward's passes, for attn_train_bwd_passes. */
 typedef enum {
   ATTN_BWD_PREP = 1,  /* Delta = rowsum(dO * O) into the workspace */

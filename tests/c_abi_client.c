@@ -21,6 +21,13 @@ int main(void) {
   p.B = 1; p.Hq = 32; p.Hkv = 4; p.Sq = 16384; p.Skv = 16384; p.D = 128;
   p.mask = ATTN_MASK_CAUSAL; p.out_dtype = ATTN_OUT_F32;
   CHECK(attn_train_supports(&p) == ATTN_OK);
+  {
+    char desc[4096];
+    size_t need = 0;
+    CHECK(attn_train_describe(&p, NULL, 0, &need) == ATTN_ERR_INVALID && need > 1);
+    CHECK(attn_train_describe(&p, desc, sizeof(desc), &need) == ATTN_OK);
+    CHECK(strlen(desc) + 1 == need && strstr(desc, "\"bwd_dkdv\"") != NULL);
+  }
 
   size_t ws = 0;
   CHECK(attn_train_workspace_size(&p, &ws) == ATTN_OK);

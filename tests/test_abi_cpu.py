@@ -159,6 +159,51 @@ def test_host_session_arena_size_grows_by_one_slot_per_slot(lib):
             binding.step_host_arena_size(p, 1, bad)
 
 
+def test_describe_reports_the_plan(lib):
+    """attn_train_describe: one JSON object with the kernels each pass runs, their
+    grids and pipeline depths, consistent with the schedule the kernels use."""
+    p = binding.problem(1, 32, 4, 16384, 16384, 128, "causal", out="fp32")
+    d = binding.describe(p)
+    assert d["head_dim"] == 128 and d["mask"] == "causal" and d["outputs"] == "fp32"
+    assert d["fwd"]["kernel"] == "fwd_kernel<128,0,0,0>" and d["fwd"]["ctas"] == 64 * 32
+    assert d["fwd"]["split_key_tiles"] == 0 and not d["fwd"]["merge_pass"]
+    assert d["bwd_dkdv"]["ctas"] == 128 * 4 and d["bwd_dq"]["ctas"] == 128 * 32
+    assert d["fwd"]["smem_bytes"] <= 227 * 1024 and d["bwd_dq"]["smem_bytes"] <= 227 * 1024
+    assert "ttt_suffix" not in d and "mask_transpose" not in d
+    # a TTT step: the scores pre-pass and the suffix-key pass (8 segments per pass at t = 6)
+    d = binding.describe(binding.problem(1, 32, 8, 8192, 7 * 8192, 128, "ttt", 6, out="fp32"))
+    assert d["fwd"]["ttt_scores_prepass"] and d["bwd_prep"]["kernel"] == "bwd_prep_kernel<128,1>"
+    assert d["ttt_suffix"] == {"kernel": "ttt_diag_bwd_kernel<128,8>", "key_rows": 8 * 8192}
+    # a small grid takes the key-range split (the S = 4096 sweep: 9 key tiles per chunk)
+    d = binding.describe(binding.problem(8, 1, 1, 4096, 4096, 64, "causal"))
+    assert d["fwd"]["kernel"] == "fwd_kernel<64,0,0,1>" and d["fwd"]["merge_pass"]
+    assert d["fwd"]["split_key_tiles"] == 9
+    # general masks: window at D <= 64 rotates three score buffers; an additive mask
+    # adds the transpose pass
+    d = binding.describe(binding.problem(2, 16, 16, 12288, 12288, 64, "window", window=(1024, 1024)))
+    assert d["general_mask"] and d["fwd"]["score_buffers"] == 3
+    am = torch.zeros(300, 304, dtype=torch.bfloat16)[:, :300]
+    d = binding.describe(binding.problem(2, 2, 2, 300, 300, 64, "full", add_mask=am, host=True))
+    assert d["additive_mask"] and d["mask_transpose"] == {"kernel": "mask_transpose_kernel"}
+    assert d["fwd"]["kernel"] == "fwd_kernel<64,1,1,0>"
+
+
+def test_describe_buffer_protocol(lib):
+    p = binding.problem(1, 2, 2, 128, 128, 64, "causal")
+    need = ctypes.c_size_t(0)
+    assert lib.attn_train_describe(ctypes.byref(p), None, 0, ctypes.byref(need)) == 1
+    assert need.value > 1
+    small = ctypes.create_string_buffer(need.value - 1)
+    assert lib.attn_train_describe(ctypes.byref(p), small, need.value - 1, None) == 1
+    assert b"needed" in lib.attn_train_last_error()
+    buf = ctypes.create_string_buffer(need.value)
+    assert lib.attn_train_describe(ctypes.byref(p), buf, need.value, None) == 0
+    assert len(buf.value) + 1 == need.value
+    # invalid problems are refused like attn_train_supports refuses them
+    bad = binding.problem(1, 2, 2, 128, 128, 96, "causal")
+    assert lib.attn_train_describe(ctypes.byref(bad), buf, need.value, None) == 2
+
+
 def test_plain_c_client(lib, tmp_path):
     """The header is plain C: a C99 program includes it, links the library and
     calls the host-side entry points (validation, sizes, error messages)."""
