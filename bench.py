@@ -698,15 +698,24 @@ def run_env(device):
             env["driver"] = r.stdout.strip().splitlines()[0]
     except (OSError, subprocess.SubprocessError):
         pass
-    try:
-        with open("/proc/cpuinfo") as f:
-            for ln in f:
-                key = ln.split(":")[0].strip().lower()
-                if key in ("model name", "cpu model", "cpu part"):
-                    env["host_cpu"] = ln.split(":", 1)[1].strip()
-                    break
-    except OSError:
+    try:  # lscpu names Arm cores ("Neoverse-V2"); /proc/cpuinfo gives only a part number there
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=20)
+        for ln in r.stdout.splitlines():
+            if ln.lower().startswith("model name:"):
+                env["host_cpu"] = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
         pass
+    if "host_cpu" not in env:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for ln in f:
+                    key = ln.split(":")[0].strip().lower()
+                    if key in ("model name", "cpu model", "cpu part"):
+                        env["host_cpu"] = ln.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
     return env
 
 
