@@ -465,7 +465,7 @@ class Runner:
         import torch
         b, args = self.binding, self.args
         if args.e2e_slots:
-            return args.e2e_slots
+            return min(b.HOST_MAX_SLOTS, max(2, args.e2e_slots))
         est = self.step_ms or 8.0
         n = min(b.HOST_MAX_SLOTS, max(2, math.ceil(E2E_RIDE_MS / est) + 1))
         free, _ = torch.cuda.mem_get_info(self.dev)
