@@ -458,20 +458,12 @@ class Runner:
         return {"total_ms": total_ms, "per_kernel_ms": per_kernel, "clocks": clk.summary()}
 
     def _pick_slots(self, hps):
-        """Slots of the sessions: enough for E2E_RIDE_MS of compute (the device
-        step time measured by timed()), within a quarter of the free memory."""
-        import math
-
         import torch
         b, args = self.binding, self.args
-        if args.e2e_slots:
-            return min(b.HOST_MAX_SLOTS, max(2, args.e2e_slots))
-        est = self.step_ms or 8.0
-        n = min(b.HOST_MAX_SLOTS, max(2, math.ceil(E2E_RIDE_MS / est) + 1))
         free, _ = torch.cuda.mem_get_info(self.dev)
-        while n > 2 and sum(b.step_host_arena_size(hp, args.e2e_chunk, n) for hp in hps) > free / 4:
-            n -= 1
-        return n
+        return e2e_slots(args.e2e_slots, self.step_ms,
+                         lambda n: sum(b.step_host_arena_size(hp, args.e2e_chunk, n) for hp in hps),
+                         free, b.HOST_MAX_SLOTS)
 
     def _open_sessions(self):
         # end to end through the C ABI's host-memory session (attn_train_host_session_*):
@@ -480,7 +472,6 @@ class Runner:
         # same and the neighbouring steps, and the timed region ends after the last
         # step's copies (join + synchronize)
         import torch
-        import math
         b, args = self.binding, self.args
         self.hosts = []
         staged = []
@@ -501,9 +492,7 @@ class Runner:
             arena = torch.empty(b.step_host_arena_size(hp, args.e2e_chunk, n), dtype=torch.uint8,
                                 device=self.dev)
             self.hosts.append((b.HostSession(hp, arena, args.e2e_chunk, n), io, pin))
-        # timed steps: about args.e2e_seconds of device time
-        est = self.step_ms or 8.0
-        self.e2e_count = max(3, min(1000, math.ceil(args.e2e_seconds * 1e3 / est)))
+        self.e2e_count = e2e_steps(args.e2e_seconds, self.step_ms)
         self._e2e_steps(2)  # first use of the sessions
 
     def _e2e_steps(self, n):
@@ -547,6 +536,27 @@ class Runner:
         for gev in self.gevs or []:
             gev.close()
         self.graph, self.gevs = None, None
+
+
+def e2e_slots(requested, step_ms, arena_bytes, free_bytes, max_slots):
+    """Device slots of the end-to-end sessions: `requested` (clamped to 2 ..
+    max_slots) if given, else enough for E2E_RIDE_MS of compute at the measured
+    device step time (8 ms if not yet timed), reduced until the arenas
+    (arena_bytes(n) for n slots) take at most a quarter of the free memory."""
+    import math
+    if requested:
+        return min(max_slots, max(2, requested))
+    est = step_ms or 8.0
+    n = min(max_slots, max(2, math.ceil(E2E_RIDE_MS / est) + 1))
+    while n > 2 and arena_bytes(n) > free_bytes / 4:
+        n -= 1
+    return n
+
+
+def e2e_steps(seconds, step_ms):
+    """Timed end-to-end steps: about `seconds` of device time (3 to 1000)."""
+    import math
+    return max(3, min(1000, math.ceil(seconds * 1e3 / (step_ms or 8.0))))
 
 
 def median_run(runs):

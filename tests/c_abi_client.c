@@ -35,6 +35,13 @@ int main(void) {
 
   size_t arena = 0;
   CHECK(attn_train_step_host_arena_size(&p, 0, &arena) == ATTN_OK && arena > ws);
+  {
+    size_t two = 0, four = 0;
+    CHECK(attn_train_host_session_arena_size(&p, 0, 2, &two) == ATTN_OK && two == arena);
+    CHECK(attn_train_host_session_arena_size(&p, 0, 4, &four) == ATTN_OK && four > two);
+    CHECK(attn_train_host_session_arena_size(&p, 0, ATTN_HOST_MAX_SLOTS + 1, &four) ==
+          ATTN_ERR_INVALID);
+  }
 
   p.D = 96;  /* unsupported head dim: a status and a message, no fallback */
   CHECK(attn_train_supports(&p) == ATTN_ERR_UNSUPPORTED);
